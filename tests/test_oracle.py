@@ -1,0 +1,343 @@
+"""Pins for the float64 oracle: page figures, closed forms, brute force,
+library routines and the absorbed-vs-explicit MLA identity.  CPU only."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_decode_paged_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_figures.txt")
+
+
+def _golden_lines():
+    out = []
+    with open(GOLDEN, encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, cite = line.split("|", 1)
+            expr, expected = lhs.split("=")
+            parts = expr.split()
+            out.append((parts[0], [int(x) for x in parts[1:]], int(expected), cite.strip()))
+    return out
+
+
+@pytest.mark.parametrize("fn,args,expected,cite", _golden_lines())
+def test_page_figures(oracle, fn, args, expected, cite):
+    if fn == "cell_gqa":
+        got = oracle.cell_bytes_gqa(*args)
+    elif fn == "cell_mla":
+        got = oracle.cell_bytes_mla(*args)
+    elif fn == "page":
+        got = oracle.page_bytes(*args)
+    elif fn == "blocks":
+        got = oracle.blocks_for(*args)
+    elif fn == "tokens_gqa":
+        got = oracle.cell_bytes_gqa(*args[:5]) * args[5]
+    else:
+        raise AssertionError(fn)
+    assert got == expected, cite
+
+
+def test_page_ratios(oracle):
+    # "56.9x reduction" vs MHA and "71.9% smaller than GQA-8" (MLA page,
+    # Architectural Comparison); "4.77 MiB ... a 71x over-estimate" (KV cache
+    # size formula, DeepSeek-V3 note); 17 tokens -> 32 slots.
+    mla = oracle.cell_bytes_mla(1, 512, 64, 2)
+    assert round(oracle.cell_bytes_gqa(1, 128, 128, 128, 2) / mla, 1) == 56.9
+    assert round(100 * (1 - mla / oracle.cell_bytes_gqa(1, 8, 128, 128, 2)), 1) == 71.9
+    wrong = oracle.cell_bytes_gqa(61, 128, 192, 128, 2)
+    assert round(wrong / 2**20, 2) == 4.77
+    assert int(wrong / oracle.cell_bytes_mla(61, 512, 64, 2)) == 71
+    assert oracle.blocks_for(17, 16) * 16 == 32
+    # DeepSeek-V3 cell "68.6 KiB"
+    assert round(oracle.cell_bytes_mla(61, 512, 64, 2) / 1024, 1) == 68.6
+
+
+def test_intensity(oracle):
+    # GQA-8 bf16: I = 8, about 2.7% of an H100's 295 FLOP/byte ridge;
+    # MLA DeepSeek-V3: 242 at TP=1 (82% of the ridge), 30 at TP=8, 15 at TP=16
+    # ("MHA -> MQA -> GQA -> MLA": intro and the capacity-law discussion).
+    assert oracle.intensity_gqa(8, 2) == 8.0
+    assert round(100 * oracle.intensity_gqa(8, 2) / 295, 1) == 2.7
+    assert round(oracle.intensity_mla(128, 512, 64, 2)) == 242
+    assert round(100 * oracle.intensity_mla(128, 512, 64, 2) / 295) == 82
+    assert round(oracle.intensity_mla(16, 512, 64, 2)) == 30
+    assert round(oracle.intensity_mla(8, 512, 64, 2)) == 15
+    # I = FLOPs / bytes with the per-(token, kv head) accounting 4 g d over 2 d b
+    g, d, b = 8, 128, 2
+    assert oracle.intensity_gqa(g, b) == (4 * g * d) / (2 * d * b)
+
+
+# ---------------------------------------------------------------- formats --
+
+def test_bf16_widening_exact(oracle):
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 1 << 16, size=4096, dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_double(b) for b in bits])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_e4m3_decode_all_codes_vs_torch(oracle):
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in codes])
+    assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])
+    ok = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert ok.all()
+    # format facts: max finite 448, min normal 2^-6, min subnormal 2^-9, 1.0 = 0x38
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0xB8) == -1.0
+
+
+def test_e4m3_encode_vs_torch_in_range(oracle):
+    # every bf16 value with |x| <= 448: torch's float32 -> float8_e4m3fn cast
+    # rounds to nearest even; ours must agree code for code.
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = inputs.bf16_to_f32(bits)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 448.0)
+    vals = vals[keep][::7]  # every 7th value keeps the loop short
+    ref = torch.from_numpy(vals.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in vals], dtype=np.uint8)
+    assert (got == ref).all()
+
+
+def test_e4m3_encode_ties_and_saturation(oracle):
+    # midpoint between 1.0 (0x38) and 1.125 (0x39) rounds to the even code
+    assert oracle.e4m3_encode(1.0625) == 0x38
+    # midpoint between 1.125 (0x39) and 1.25 (0x3A) rounds to 0x3A
+    assert oracle.e4m3_encode(1.1875) == 0x3A
+    for x in (448.0, 449.0, 464.0, 1e6, float("inf")):
+        assert oracle.e4m3_encode(x) == 0x7E
+        assert oracle.e4m3_encode(-x) == 0xFE
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00      # half the min subnormal -> even (0)
+    assert oracle.e4m3_encode(3 * 2.0 ** -10) == 0x02  # 1.5 * min subnormal -> even (2)
+
+
+def test_quantize_divides_in_float32(oracle):
+    x = inputs.normal_bf16(inputs.rng_for(3, "x"), 4096)
+    xf = inputs.bf16_to_f32(x)
+    scale = np.float32(np.abs(xf).max()) / np.float32(448.0)
+    codes = oracle.quantize_e4m3(x, float(scale))
+    ref = torch.from_numpy((xf / scale).astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (codes == ref).all()
+    # amax maps to the largest code
+    assert np.abs(codes.astype(np.int32) & 0x7F).max() == 0x7E
+
+
+# ---------------------------------------------------------------- decode --
+
+def _sdpa_reference(q, k, v, scale):
+    """torch's scaled_dot_product_attention in float64 on one sequence
+    (q [h, d], k/v [s, h_kv, d]) with GQA head broadcasting, plus logsumexp."""
+    qt = torch.from_numpy(q)[None, :, None, :]            # [1, h, 1, d]
+    kt = torch.from_numpy(k).permute(1, 0, 2)[None]        # [1, h_kv, s, d]
+    vt = torch.from_numpy(v).permute(1, 0, 2)[None]
+    h, h_kv = q.shape[0], k.shape[1]
+    out = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, scale=scale, enable_gqa=(h != h_kv))[0, :, 0, :]
+    g = h // h_kv
+    krep = kt.repeat_interleave(g, dim=1)[0]               # [h, s, d]
+    logits = torch.einsum("hd,hsd->hs", torch.from_numpy(q), krep) * scale
+    return out.numpy(), torch.logsumexp(logits, dim=-1).numpy()
+
+
+@pytest.mark.parametrize("h,h_kv,d,s", [(4, 4, 16, 9), (8, 2, 32, 13), (6, 1, 8, 21), (8, 8, 64, 40)])
+def test_gqa_decode_matches_torch_sdpa(oracle, h, h_kv, d, s):
+    rng = np.random.default_rng(h * 100 + s)
+    q = inputs.bf16_bits(rng.standard_normal((h, d)).astype(np.float32))
+    k = inputs.bf16_bits(rng.standard_normal((s, h_kv, d)).astype(np.float32))
+    v = inputs.bf16_bits(rng.standard_normal((s, h_kv, d)).astype(np.float32))
+    scale = 1 / math.sqrt(d)
+    out, lse = oracle.gqa_decode(q, k, v, scale)
+    f = lambda a: inputs.bf16_to_f32(a).astype(np.float64)
+    ref_o, ref_l = _sdpa_reference(f(q), f(k), f(v), scale)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-12, atol=1e-13)
+
+
+def test_gqa_g1_is_mha_head_by_head(oracle):
+    # g = 1: each head is its own single-head attention
+    rng = np.random.default_rng(7)
+    h, d, s = 5, 16, 11
+    q = inputs.bf16_bits(rng.standard_normal((h, d)).astype(np.float32))
+    k = inputs.bf16_bits(rng.standard_normal((s, h, d)).astype(np.float32))
+    v = inputs.bf16_bits(rng.standard_normal((s, h, d)).astype(np.float32))
+    out, lse = oracle.gqa_decode(q, k, v, 0.25)
+    for i in range(h):
+        o1, l1 = oracle.gqa_decode(q[i:i + 1], k[:, i:i + 1], v[:, i:i + 1], 0.25)
+        np.testing.assert_array_equal(out[i], o1[0])
+        assert lse[i] == l1[0]
+
+
+def test_gqa_closed_forms(oracle):
+    rng = np.random.default_rng(11)
+    h, h_kv, d = 8, 2, 32
+    f = lambda a: inputs.bf16_to_f32(a).astype(np.float64)
+    q = inputs.bf16_bits(rng.standard_normal((h, d)).astype(np.float32))
+    # single cached token: out = V_0, lse = scale * q . K_0
+    k = inputs.bf16_bits(rng.standard_normal((1, h_kv, d)).astype(np.float32))
+    v = inputs.bf16_bits(rng.standard_normal((1, h_kv, d)).astype(np.float32))
+    out, lse = oracle.gqa_decode(q, k, v, 0.5)
+    for i in range(h):
+        np.testing.assert_array_equal(out[i], f(v)[0, i // 4])
+        assert lse[i] == pytest.approx(0.5 * f(q)[i] @ f(k)[0, i // 4], rel=1e-14)
+    # all keys equal: uniform weights, out = mean of V, lse = score + log s
+    s = 17
+    k1 = np.repeat(k, s, axis=0)
+    v2 = inputs.bf16_bits(rng.standard_normal((s, h_kv, d)).astype(np.float32))
+    out, lse = oracle.gqa_decode(q, k1, v2, 0.5)
+    for i in range(h):
+        np.testing.assert_allclose(out[i], f(v2)[:, i // 4].mean(axis=0), rtol=1e-12, atol=1e-14)
+        assert lse[i] == pytest.approx(0.5 * f(q)[i] @ f(k)[0, i // 4] + math.log(s), rel=1e-13)
+    # empty context: zeros and -inf
+    out, lse = oracle.gqa_decode(q, k[:0], v[:0], 0.5)
+    assert (out == 0).all() and np.isneginf(lse).all()
+
+
+def test_gqa_needle(oracle):
+    wl = inputs.make_workload("tiny", lens=[64, 80])
+    inputs.plant_needle(wl, b=1, head=5, t=33, strength=60.0)
+    sl = wl.seq_slice(1)
+    out, _ = oracle.gqa_decode(wl.q[1], wl.k[sl], wl.v[sl], wl.scale)
+    vt = inputs.bf16_to_f32(wl.v[sl][33, 5 // wl.g]).astype(np.float64)
+    np.testing.assert_allclose(out[5], vt, atol=1e-6)
+
+
+def test_gqa_fp8_format(oracle):
+    # E4M3 inputs: the oracle decodes codes * scale; equals the float64 path
+    rng = np.random.default_rng(5)
+    h, h_kv, d, s = 4, 2, 16, 9
+    q = inputs.bf16_bits(rng.standard_normal((h, d)).astype(np.float32))
+    kc = rng.integers(0, 0x7E, size=(s, h_kv, d), dtype=np.uint8) | (rng.integers(0, 2, size=(s, h_kv, d), dtype=np.uint8) << 7)
+    vc = rng.integers(0, 0x7E, size=(s, h_kv, d), dtype=np.uint8)
+    ks, vs = 0.01, 0.02
+    out, lse = oracle.gqa_decode(q, kc, vc, 0.25, fmt=oracle.FMT_E4M3, k_scale=ks, v_scale=vs)
+    dec = np.vectorize(oracle.e4m3_decode)
+    o2, l2 = oracle.gqa_decode(q, dec(kc) * ks, dec(vc) * vs, 0.25, fmt=oracle.FMT_F64)
+    np.testing.assert_array_equal(out, o2)
+    np.testing.assert_array_equal(lse, l2)
+
+
+def test_mla_matches_torch_sdpa(oracle):
+    # absorbed MLA is MQA over the 576-wide row with V = the first 512 columns
+    rng = np.random.default_rng(9)
+    h, d_c, d_r, s = 4, 512, 64, 23
+    q = inputs.bf16_bits((rng.standard_normal((h, d_c + d_r)) / 24).astype(np.float32))
+    rows = inputs.bf16_bits(rng.standard_normal((s, d_c + d_r)).astype(np.float32))
+    scale = 1 / math.sqrt(192)
+    out, lse = oracle.mla_decode(q, rows, d_c, scale)
+    f = lambda a: inputs.bf16_to_f32(a).astype(np.float64)
+    qt = torch.from_numpy(f(q))[None, :, None, :]
+    kt = torch.from_numpy(f(rows))[None, None]
+    vt = torch.from_numpy(f(rows)[:, :d_c].copy())[None, None]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale, enable_gqa=True)
+    np.testing.assert_allclose(out, ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-13)
+    ref_l = torch.logsumexp(torch.from_numpy(f(q)) @ torch.from_numpy(f(rows)).T * scale, dim=-1)
+    np.testing.assert_allclose(lse, ref_l.numpy(), rtol=1e-12)
+
+
+@pytest.mark.parametrize("h,d_hc,d_c,d_r,d_v,s", [(4, 16, 32, 8, 16, 5), (2, 128, 512, 64, 128, 7)])
+def test_mla_absorbed_equals_explicit(oracle, h, d_hc, d_c, d_r, d_v, s):
+    """Absorbed decode (q~ = W_UK^T q^C, latent weighted sum, W_UV afterwards)
+    equals the explicit form that expands k = W_UK c and v = W_UV c."""
+    rng = np.random.default_rng(h + s)
+    q_c = rng.standard_normal((h, d_hc))
+    q_r = rng.standard_normal((h, d_r))
+    c = rng.standard_normal((s, d_c))
+    k_r = rng.standard_normal((s, d_r))
+    w_uk = rng.standard_normal((h, d_hc, d_c)) / math.sqrt(d_c)
+    w_uv = rng.standard_normal((h, d_v, d_c)) / math.sqrt(d_c)
+    scale = 1 / math.sqrt(d_hc + d_r)
+    u_ref, lse_ref = oracle.mla_explicit(q_c, q_r, c, k_r, w_uk, w_uv, scale)
+    q_abs = np.concatenate([oracle.mla_absorb_query(q_c, w_uk), q_r], axis=1)
+    rows = np.concatenate([c, k_r], axis=1)
+    u_tilde, lse = oracle.mla_decode(q_abs, rows, d_c, scale, fmt=oracle.FMT_F64)
+    u = oracle.mla_apply_wuv(u_tilde, w_uv)
+    np.testing.assert_allclose(u, u_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12)
+    # the absorbed score equals the explicit content + RoPE score
+    sc_abs = q_abs @ rows.T
+    sc_exp = np.einsum("hj,hjc,sc->hs", q_c, w_uk, c) + q_r @ k_r.T
+    np.testing.assert_allclose(sc_abs, sc_exp, rtol=1e-12, atol=1e-12)
+
+
+def test_mla_absorb_query_brute(oracle):
+    rng = np.random.default_rng(2)
+    q_c = rng.standard_normal((3, 4))
+    w = rng.standard_normal((3, 4, 5))
+    got = oracle.mla_absorb_query(q_c, w)
+    for i in range(3):
+        np.testing.assert_allclose(got[i], w[i].T @ q_c[i], rtol=1e-14)
+
+
+# --------------------------------------------------------------- combine --
+
+@pytest.mark.parametrize("cuts", [[0, 40], [0, 1, 40], [0, 13, 13, 27, 40], [0, 5, 10, 15, 20, 25, 30, 35, 40]])
+def test_combine_of_splits_equals_unsplit(oracle, cuts):
+    rng = np.random.default_rng(len(cuts))
+    h, h_kv, d = 8, 2, 16
+    q = inputs.bf16_bits(rng.standard_normal((h, d)).astype(np.float32) * 3)
+    k = inputs.bf16_bits(rng.standard_normal((40, h_kv, d)).astype(np.float32))
+    v = inputs.bf16_bits(rng.standard_normal((40, h_kv, d)).astype(np.float32))
+    full_o, full_l = oracle.gqa_decode(q, k, v, 0.25)
+    parts_o, parts_l = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        o, l = oracle.gqa_decode(q, k[a:b], v[a:b], 0.25)
+        parts_o.append(o)
+        parts_l.append(l)
+    o, l = oracle.lse_combine(np.stack(parts_o), np.stack(parts_l))
+    np.testing.assert_allclose(o, full_o, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l, full_l, rtol=1e-13)
+
+
+def test_combine_empty(oracle):
+    o, l = oracle.lse_combine(np.zeros((2, 3, 4)), np.full((2, 3), -np.inf))
+    assert (o == 0).all() and np.isneginf(l).all()
+
+
+# ---------------------------------------------------------------- paging --
+
+def test_gqa_placement_roundtrip(oracle):
+    wl = inputs.make_workload("tiny", lens=[37, 100, 16, 1], block_size=16)
+    seq_idx, pos = wl.append_indices()
+    pool = oracle.expected_gqa_pool(wl.k, seq_idx, pos, wl.block_table, wl.num_blocks, 16,
+                                    fill=inputs.BF16_NAN)
+    # numpy fancy indexing through the documented [block][kv head][slot][dim]
+    # layout gives back each sequence's contiguous keys
+    for b in range(wl.B):
+        t = np.arange(wl.seq_lens[b])
+        got = pool[wl.block_table[b, t // 16], :, t % 16, :]
+        np.testing.assert_array_equal(got, wl.k[wl.seq_slice(b)])
+    # every written element is addressed exactly once; the rest is still poison
+    written = sum(int(s) for s in wl.seq_lens) * wl.h_kv * wl.d
+    assert int((pool != inputs.BF16_NAN).sum()) <= written
+    offs = {oracle.gqa_pool_offset(wl.block_table, 16, wl.h_kv, wl.d, b, t, kvh)
+            for b in range(wl.B) for t in range(wl.seq_lens[b]) for kvh in range(wl.h_kv)}
+    assert len(offs) == written // wl.d
+
+
+def test_mla_placement_roundtrip(oracle):
+    wl = inputs.make_workload("deepseek_v3_mla", lens=[65, 3, 128], block_size=64)
+    seq_idx, pos = wl.append_indices()
+    rows = np.concatenate([wl.c_kv, wl.k_r], axis=1)
+    pool = oracle.expected_mla_pool(rows, seq_idx, pos, wl.block_table, wl.num_blocks, 64,
+                                    fill=inputs.BF16_NAN)
+    for b in range(wl.B):
+        t = np.arange(wl.seq_lens[b])
+        np.testing.assert_array_equal(pool[wl.block_table[b, t // 64], t % 64], rows[wl.seq_slice(b)])
+
+
+def test_slot_block_range(oracle):
+    bt = np.array([[4, 7, -1]], dtype=np.int32)
+    assert oracle.gqa_pool_offset(bt, 16, 2, 8, 0, 17, 1) == ((7 * 2 + 1) * 16 + 1) * 8
+    assert oracle.gqa_pool_offset(bt, 16, 2, 8, 0, 48, 0) == -1   # beyond the table row
