@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Decode-attention layer-step benchmark on GB300.  Prints ONE JSON line.
+
+A step is one pass of the whole hot path over one batch: the paged append of
+each sequence's current token (its K/V, or c_KV/k_R, written through the block
+table) followed by the decode (split planner, decode kernel, split-KV combine)
+over all cached tokens.  Inputs are synthetic, seeded, resident in HBM and far
+larger than L2, so every step streams the KV cache from HBM.
+
+  python bench.py [--config llama3_8b] [--steps K] [--warmup W]
+  python bench.py --impl reference      # the float64 CPU oracle on a bounded sample
+  torchrun --nproc-per-node N bench.py --gpus N   # N independent replicas
+
+Metric: decode-attention KV-read GB/s (algorithmic KV bytes of a step / step
+time); also microseconds per layer-step and the fraction of ~8 TB/s.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV-read GB/s (% of ~8 TB/s HBM) and µs per layer-step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2**20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama3_8b")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
+    return ap.parse_args()
+
+
+def env_ranks():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def file_hash(*paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source(wl) -> str:
+    name = "decode_mla.cu" if wl.kind == "mla" else "decode_gqa.cu"
+    return os.path.join(ROOT, "kv_cache_decode_paged_gb300", "csrc", name)
+
+
+def recorded_traffic(wl, config):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f).get(config)
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha") != file_hash(kernel_source(wl)):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons in the background."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 6:
+                self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if not win:
+            win = [s for _, s in self.samples]
+            window = "whole run (no sample fell inside the timed region)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "nvidia-smi unavailable"}
+        sm = [float(s[0]) for s in win if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in win if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4) if s[2 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win), "window": window}
+
+
+def config_dict(wl, args):
+    d = {"workload": wl.name, "kind": wl.kind, "batch": wl.B, "h": wl.h,
+         "block_size": wl.block_size, "kv_dtype": wl.kv_dtype,
+         "total_tokens": wl.total_tokens, "kv_bytes_per_step": wl.kv_bytes(),
+         "seq_lens": {"min": int(wl.seq_lens.min()), "max": int(wl.seq_lens.max()),
+                      "mean": float(wl.seq_lens.mean())},
+         "seed": args.seed,
+         "l2": ("inputs larger than L2: every step reads %.2f GB of KV vs %d MB of L2"
+                % (wl.kv_bytes() / 1e9, L2_BYTES // 2**20)),
+         "parallelism": f"replicas x{args.gpus}"}
+    if wl.kind == "gqa":
+        d.update({"h_kv": wl.h_kv, "d_h": wl.d})
+    else:
+        d.update({"d_c": wl.d_c, "d_rope": wl.d_rope})
+    return d
+
+
+# ----------------------------------------------------------------------- oracle
+
+def oracle_sample_rate(wl, budget_s, oracle):
+    """Run the oracle over whole sequences until the time budget is spent.
+    Returns (GB/s of KV read, seconds, sample description)."""
+    done_bytes, t_total, seqs = 0, 0.0, []
+    per_tok = wl.kv_bytes() / max(1, wl.total_tokens)
+    import numpy as np
+    order = list(np.random.default_rng(123).permutation(wl.B))
+    for b in order:
+        sl = wl.seq_slice(b)
+        t0 = time.perf_counter()
+        if wl.kind == "mla":
+            rows = np.concatenate([wl.c_kv[sl], wl.k_r[sl]], axis=1)
+            oracle.mla_decode(wl.q[b], rows, wl.d_c, wl.scale)
+        elif wl.kv_dtype == "fp8":
+            kc = oracle.quantize_e4m3(wl.k[sl], wl.k_scale)
+            vc = oracle.quantize_e4m3(wl.v[sl], wl.v_scale)
+            t0 = time.perf_counter()
+            oracle.gqa_decode(wl.q[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
+                              k_scale=wl.k_scale, v_scale=wl.v_scale)
+        else:
+            oracle.gqa_decode(wl.q[b], wl.k[sl], wl.v[sl], wl.scale)
+        t_total += time.perf_counter() - t0
+        done_bytes += int(wl.seq_lens[b]) * per_tok
+        seqs.append(int(b))
+        if t_total >= budget_s:
+            break
+    gbs = done_bytes / t_total / 1e9 if t_total > 0 else 0.0
+    return gbs, t_total, f"{len(seqs)} of {wl.B} sequences ({done_bytes / 1e6:.1f} MB of KV), all heads"
+
+
+def run_reference(args, wl, rank):
+    """The reference arm: the float64 CPU oracle as it stands."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    per_tok = wl.kv_bytes() / max(1, wl.total_tokens)
+    steps, warm = args.steps, args.warmup
+    # size one step (a few KV heads of one sequence) so the whole run ends in ~2 minutes
+    budget_per_step = min(0.5, 120.0 / max(1, steps + warm))
+    order = list(np.argsort(wl.seq_lens))[len(wl.seq_lens) // 2:] or [0]
+
+    def one(i, heads):
+        b = int(order[i % len(order)])
+        sl = wl.seq_slice(b)
+        if wl.kind == "mla":
+            rows = np.concatenate([wl.c_kv[sl], wl.k_r[sl]], axis=1)
+            hq = max(1, heads)
+            oracle.mla_decode(wl.q[b, :hq], rows, wl.d_c, wl.scale)
+            return int(wl.seq_lens[b]) * per_tok * hq / wl.h
+        g = wl.g
+        if wl.kv_dtype == "fp8":
+            kc = oracle.quantize_e4m3(wl.k[sl, :heads], wl.k_scale)
+            vc = oracle.quantize_e4m3(wl.v[sl, :heads], wl.v_scale)
+            oracle.gqa_decode(wl.q[b, :heads * g], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
+                              k_scale=wl.k_scale, v_scale=wl.v_scale)
+        else:
+            oracle.gqa_decode(wl.q[b, :heads * g], wl.k[sl, :heads], wl.v[sl, :heads], wl.scale)
+        return int(wl.seq_lens[b]) * per_tok * heads / wl.h_kv
+
+    units = wl.h if wl.kind == "mla" else wl.h_kv
+    heads = units
+    t0 = time.perf_counter()
+    one(0, heads)
+    dt = time.perf_counter() - t0
+    while heads > 1 and dt * heads / units > budget_per_step and dt > budget_per_step:
+        heads = max(1, heads // 2)
+        dt /= 2
+    for i in range(warm):
+        one(i, heads)
+    total_bytes = 0.0
+    t0 = time.perf_counter()
+    for i in range(steps):
+        total_bytes += one(i, heads)
+    el = time.perf_counter() - t0
+    value = total_bytes / el / 1e9
+    cores = oracle.num_threads()
+    sample = (f"each step: one sequence of the upper half of the length mix, "
+              f"{heads} of {units} {'query' if wl.kind == 'mla' else 'KV'} heads")
+    line = {"metric": METRIC, "impl": "reference", "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+            "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(wl, args),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------------- ours
+
+def run_ours(args, wl, rank, world, local):
+    import numpy as np
+    import torch
+
+    import kv_cache_decode_paged_gb300 as kv
+    from kv_cache_decode_paged_gb300.device import GpuWorkload, dev_bits
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+
+    kv.load_library()
+    g = GpuWorkload(wl, poison=False, device=dev)     # pools filled by kvattn_append (untimed)
+    torch.cuda.synchronize()
+
+    # the current token of every non-empty sequence: position s_b - 1
+    live = np.nonzero(wl.seq_lens > 0)[0]
+    last = (wl.cu_seqlens[1:] - 1)[live]
+    seq_idx = torch.from_numpy(live.astype(np.int32)).to(dev)
+    pos = torch.from_numpy((wl.seq_lens[live] - 1).astype(np.int32)).to(dev)
+    if wl.kind == "gqa":
+        new0, new1 = dev_bits(wl.k[last], dev), dev_bits(wl.v[last], dev)
+        dv = wl.d
+    else:
+        new0, new1 = dev_bits(wl.c_kv[last], dev), dev_bits(wl.k_r[last], dev)
+        dv = wl.d_c
+    ws = g.workspace()
+    out = torch.empty((wl.B, wl.h, dv), dtype=torch.float32, device=dev)
+    lse = torch.empty((wl.B, wl.h), dtype=torch.float32, device=dev)
+    desc = g.cache.descriptor()
+    stream = torch.cuda.current_stream()
+
+    def decode():
+        if wl.kind == "gqa":
+            kv.kvattn_decode_gqa(g.q, desc, g.bt, g.seq_lens, wl.h, wl.h_kv, wl.d, wl.scale,
+                                 out, lse, ws, err=g.err, stream=stream)
+        else:
+            kv.kvattn_decode_mla(g.q, desc, g.bt, g.seq_lens, wl.h, wl.d_c, wl.d_rope, wl.scale,
+                                 out, lse, ws, err=g.err, stream=stream)
+
+    def step(ev=None):
+        kv.kvattn_append(desc, new0, new1, seq_idx, pos, g.bt, err=g.err, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        decode()
+        if ev is not None:
+            ev[1].record(stream)
+
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid).replace("GPU-", "")
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0 = time.monotonic()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.monotonic()
+    if dist:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    time.sleep(0.05)
+    clocks = sampler.summary(w0, w1)
+    sampler.stop()
+    err_bits = g.err_bits()
+
+    # ---- end to end: host buffers in, result out, every step
+    e2e_steps = args.e2e_steps or args.steps
+    h_q = torch.from_numpy(np.ascontiguousarray(wl.q).view(np.int16)).pin_memory()
+    h_new0 = new0.cpu().pin_memory()
+    h_new1 = new1.cpu().pin_memory()
+    h_pos = pos.cpu().pin_memory()
+    h_sl = g.seq_lens.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_new0, h_new1, h_pos, h_sl))
+    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+
+    def e2e_step():
+        g.q.copy_(h_q, non_blocking=True)
+        new0.copy_(h_new0, non_blocking=True)
+        new1.copy_(h_new1, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        g.seq_lens.copy_(h_sl, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+        dist.barrier()
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    kvb = wl.kv_bytes()
+    ms_step = ms_total / args.steps
+    value = kvb * world / (ms_step * 1e-3) / 1e9
+    dec_mean = statistics.mean(dec_ms)
+    achieved = kvb / (dec_mean * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.kv_dtype == "bf16" else "fp8-e4m3 cache, bf16 q",
+        "data": "synthetic", "config": config_dict(wl, args),
+        "us_per_layer_step": ms_step * 1e3,
+        "us_decode_call": dec_mean * 1e3,
+        "pct_of_8tbs": 100.0 * (value / world) / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": recorded_traffic(wl, args.config),
+                     "kernel": "decode call (planner + decode kernel + combine), CUDA events",
+                     "algorithmic_bytes_per_launch": kvb},
+        "e2e": {"value": kvb * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "device_err_bits": err_bits,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        gbs, secs, sample = oracle_sample_rate(wl, args.cpu_budget_s, oracle)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": sample, "seconds": secs}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    rank, world, local = env_ranks()
+    from kv_cache_decode_paged_gb300 import inputs
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl = inputs.make_workload(args.config, seed=args.seed)
+        run_reference(args, wl, rank)
+        return
+    wl = inputs.make_workload(args.config, seed=args.seed)
+    run_ours(args, wl, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,111 @@
+// internal.h -- host-side plumbing shared by the translation units of libkvattn.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvattn.h"
+
+namespace kv {
+
+// A decode splits the flattened page list of all units -- GQA unit = (sequence,
+// KV head), MLA unit = sequence; pages ordered (b, kvh, page) -- into G equal
+// contiguous ranges, one per CTA.  The plan kernel writes, into the caller's
+// workspace:
+//   cum[B+1]         prefix sums over sequences of pages per unit
+//   cta_start[G+1]   (b, kvh, page) where CTA c's range starts
+//   split_first[U]   first partial slot of unit u (slot = u + c for CTA c)
+//   split_count[U]   how many CTAs touched unit u (0, 1 or more)
+// and the decode kernel writes partial outputs for units it did not finish.
+struct WsLayout {
+  size_t cum, cta, split_first, split_count, part_lse, part_out, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int B, int units, int G, int rows, int dv) {
+  WsLayout L;
+  size_t off = 0;
+  L.cum = off;
+  off = align256(off + size_t(B + 1) * 8);
+  L.cta = off;
+  off = align256(off + size_t(G + 1) * 16);
+  L.split_first = off;
+  off = align256(off + size_t(units) * 4);
+  L.split_count = off;
+  off = align256(off + size_t(units) * 4);
+  L.part_lse = off;
+  off = align256(off + size_t(units + G) * rows * 4);
+  L.part_out = off;
+  off = align256(off + size_t(units + G) * rows * size_t(dv) * 4);
+  L.total = off;
+  return L;
+}
+
+struct PlanArgs {
+  const int32_t* seq_lens;
+  int B;
+  int units_per_seq;   // h_kv for GQA, 1 for MLA
+  int block_size;
+  int max_blocks;
+  int G;
+  int64_t* cum;
+  int4* cta_start;
+  int32_t* split_first;
+  int32_t* split_count;
+  int32_t* err;
+};
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
+                           const int32_t* count, int n_units, int rows, int dv, float* out,
+                           float* lse, bool skip_single, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device), or -1.
+int device_sm_count();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (so the
+// library does not link libcuda directly).  Returns false on failure.
+bool encode_tensor_map_3d(void* map, CUtensorMapDataType dtype, const void* base,
+                          const uint64_t dims[3], const uint64_t strides_bytes[2],
+                          const uint32_t box[3], CUtensorMapSwizzle swizzle);
+
+struct GqaArgs {
+  const void* q;
+  const kvattn_cache* cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int B, max_blocks, h, h_kv, d;
+  float scale;
+  float* out;
+  float* lse;
+  void* workspace;
+  size_t ws_bytes;
+  int G;
+  int32_t* err;
+  cudaStream_t stream;
+};
+kvattn_status run_decode_gqa(const GqaArgs& a);
+int gqa_default_ctas(int dtype, int h, int h_kv, int d);
+
+struct MlaArgs {
+  const void* q;
+  const kvattn_cache* cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int B, max_blocks, h, d_c, d_rope;
+  float scale;
+  float* out;
+  float* lse;
+  void* workspace;
+  size_t ws_bytes;
+  int G;
+  int32_t* err;
+  cudaStream_t stream;
+};
+kvattn_status run_decode_mla(const MlaArgs& a);
+int mla_default_ctas(int h);
+
+}  // namespace kv

@@ -1,0 +1,225 @@
+// plan_combine.cu -- split-KV planner, log-sum-exp combine, device helpers.
+//
+// Variable-length batches are split so every CTA streams the same number of
+// pages: short sequences do not waste CTAs and long ones do not straggle
+// ("MLA：为什么一份 Latent 可以代替多头 KV Cache", section "FlashMLA 解决的不是
+// 模型公式本身": tile scheduler metadata and split info, then a stable merge of
+// each split's local max, normaliser and output).
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kv {
+
+// One CTA.  cum[] over sequences, then each CTA's start, then each unit's split
+// slots.  With T pages in total and G' = min(G, T) working CTAs, CTA c < G'
+// owns flattened pages [floor(c*T/G'), floor((c+1)*T/G')) -- at least one --
+// and page p belongs to CTA ((p+1)*G' - 1) / T.  The slot of (unit u, CTA c) is u + c,
+// unique because walking the page list increases u or c (or both) at every
+// segment boundary.
+__global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
+  __shared__ int64_t warp_tot[32];
+  __shared__ int64_t carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  if (tid == 0) {
+    carry_s = 0;
+    a.cum[0] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < a.B; base += blockDim.x) {
+    const int i = base + tid;
+    int64_t n = 0;
+    if (i < a.B) {
+      int s = a.seq_lens[i];
+      if (s < 0) {
+        report(a.err, KVATTN_DEVERR_SEQ_LEN);
+        s = 0;
+      }
+      n = (int64_t(s) + a.block_size - 1) / a.block_size;
+      if (n > a.max_blocks) {
+        report(a.err, KVATTN_DEVERR_SEQ_LEN);
+        n = a.max_blocks;
+      }
+    }
+    int64_t x = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int64_t w = lane < nw ? warp_tot[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nw) warp_tot[lane] = w;
+    }
+    __syncthreads();
+    const int64_t carry = carry_s;
+    if (i < a.B) a.cum[i + 1] = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + x;
+    __syncthreads();
+    if (tid == 0) carry_s = carry + warp_tot[nw - 1];
+    __syncthreads();
+  }
+  const int64_t* cum = a.cum;
+  const int64_t U = a.units_per_seq;
+  const int64_t T = U * cum[a.B];
+  // With more CTAs than pages, only the first T CTAs get work (one page or
+  // more each); the rest get empty ranges.  Every CTA between the first and
+  // the last one touching a unit then owns part of that unit, so the unit's
+  // partial slots u + c0 .. u + c1 are all written.
+  const int64_t G = T < a.G ? T : a.G;
+  for (int c = tid; c <= a.G; c += blockDim.x) {
+    const int64_t p = c <= G ? (int64_t(c) * T) / (G > 0 ? G : 1) : T;
+    int4 st = make_int4(a.B, 0, 0, 0);
+    if (p < T) {
+      int lo = 0, hi = a.B - 1;  // largest b with U*cum[b] <= p
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (U * cum[mid] <= p)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const int64_t r = p - U * cum[lo];
+      const int64_t n = cum[lo + 1] - cum[lo];
+      st = make_int4(lo, int(r / n), int(r % n), 0);
+    }
+    a.cta_start[c] = st;
+  }
+  const int64_t units = int64_t(a.B) * U;
+  for (int64_t u = tid; u < units; u += blockDim.x) {
+    const int64_t b = u / U, kvh = u % U;
+    const int64_t n = cum[b + 1] - cum[b];
+    if (n == 0) {
+      a.split_first[u] = 0;
+      a.split_count[u] = 0;
+      continue;
+    }
+    const int64_t u0 = U * cum[b] + kvh * n, u1 = u0 + n;
+    const int64_t c0 = ((u0 + 1) * G - 1) / T;
+    const int64_t c1 = (u1 * G - 1) / T;
+    a.split_first[u] = int32_t(u + c0);
+    a.split_count[u] = int32_t(c1 - c0 + 1);
+  }
+}
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// Merge the partial results of every split unit.  grid.x = unit; each thread
+// owns a float4 of one row.  skip_single leaves units with one split alone
+// (the decode kernel already wrote their final rows).
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
+                                                      const float* __restrict__ part_lse,
+                                                      const int32_t* __restrict__ first,
+                                                      const int32_t* __restrict__ count,
+                                                      int rows, int dv, float* __restrict__ out,
+                                                      float* __restrict__ lse, int skip_single) {
+  const int u = blockIdx.x;
+  const int cnt = count[u];
+  if (cnt == 1 && skip_single) return;
+  const int f = first[u];
+  const int v4 = dv >> 2;
+  for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < rows * v4;
+       idx += gridDim.y * blockDim.x) {
+    const int r = idx / v4, c = idx - r * v4;
+    float4* o4 = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv) + c;
+    float M = -INFINITY;
+    for (int w = 0; w < cnt; ++w) M = fmaxf(M, part_lse[size_t(f + w) * rows + r]);
+    if (M == -INFINITY) {
+      *o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c == 0) lse[size_t(u) * rows + r] = -INFINITY;
+      continue;
+    }
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < cnt; ++w) {
+      const float lw = part_lse[size_t(f + w) * rows + r];
+      if (lw == -INFINITY) continue;
+      const float e = exp2_approx((lw - M) * kLog2e);
+      den += e;
+      const float4 p = reinterpret_cast<const float4*>(part_out + (size_t(f + w) * rows + r) * dv)[c];
+      acc.x += e * p.x;
+      acc.y += e * p.y;
+      acc.z += e * p.z;
+      acc.w += e * p.w;
+    }
+    const float inv = 1.f / den;
+    *o4 = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (c == 0) lse[size_t(u) * rows + r] = M + log2_approx(den) * kLn2;
+  }
+}
+
+cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
+                           const int32_t* count, int n_units, int rows, int dv, float* out,
+                           float* lse, bool skip_single, cudaStream_t s) {
+  if (n_units <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int work = rows * (dv / 4);
+  const int gy = (work + threads - 1) / threads;
+  dim3 grid(n_units, gy > 0 ? gy : 1);
+  combine_kernel<<<grid, threads, 0, s>>>(part_out, part_lse, first, count, rows, dv, out, lse,
+                                          skip_single ? 1 : 0);
+  return cudaGetLastError();
+}
+
+// ---- device queries -----------------------------------------------------------
+
+int device_sm_count() {
+  static int cache[64];
+  static std::once_flag flags[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::call_once(flags[dev], [dev] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = -1;
+    cache[dev] = n;
+  });
+  return cache[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_tensor_map_3d(void* map, CUtensorMapDataType dtype, const void* base,
+                          const uint64_t dims[3], const uint64_t strides_bytes[2],
+                          const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3] = {dims[0], dims[1], dims[2]};
+  cuuint64_t gstr[2] = {strides_bytes[0], strides_bytes[1]};
+  cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(reinterpret_cast<CUtensorMap*>(map), dtype, 3, const_cast<void*>(base), gdim,
+                  gstr, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace kv
