@@ -211,6 +211,39 @@ KVATTN_API kvattn_status kvattn_combine(const float* part_out, const float* part
                              const int32_t* split_first, const int32_t* split_count, int n_units,
                              int rows_per_unit, int dv, float* out, float* lse, void* stream);
 
+/* Size of the scratch array built into the library for
+ * kvattn_decode_gqa_noalloc: 8 MiB of device memory on every GPU that loads
+ * the library, held until the process exits. */
+#define KVATTN_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* GQA / MQA / MHA decode that allocates nothing and takes no workspace.
+ *   The pages have no counterpart: this exists for callers that cannot give
+ *   the library device memory -- a plugin or custom-op interface that passes
+ *   only the op's inputs and outputs, a runtime whose memory all belongs to
+ *   its own pool, or a path where cudaMalloc (which may synchronise the
+ *   device) is not allowed.
+ *   Arguments and results are those of kvattn_decode_gqa without `workspace`
+ *   and `workspace_bytes`; the plan and the partial outputs go to a fixed
+ *   scratch array inside the library (KVATTN_NOALLOC_SCRATCH_BYTES).
+ *   - A problem whose kvattn_decode_workspace_bytes(KVATTN_GQA, batch, h, h_kv,
+ *     d_h, num_ctas) exceeds KVATTN_NOALLOC_SCRATCH_BYTES is rejected with
+ *     KVATTN_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before capturing any stream.
+ *   - All calls on a device share the one array and it keeps what the last
+ *     call left there; nothing in it needs to start at zero.  Calls whose work
+ *     overlaps on the GPU (different streams, or different host threads without
+ *     ordering) race on the array and corrupt each other's results: order them
+ *     on one stream.
+ *   - No cudaMalloc, cudaFree or other allocating call is made. */
+KVATTN_API kvattn_status kvattn_decode_gqa_noalloc(const void* q, const kvattn_cache* cache,
+                                                   const int32_t* block_table,
+                                                   const int32_t* seq_lens, int batch,
+                                                   int max_blocks_per_seq, int h, int h_kv,
+                                                   int d_h, float scale, float* out, float* lse,
+                                                   int num_ctas, int32_t* err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

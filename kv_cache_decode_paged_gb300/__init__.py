@@ -36,8 +36,10 @@ KVATTN_FP8_E4M3 = 1
 EXPORTED = [
     "kvattn_status_string", "kvattn_abi_version", "kvattn_page_bytes", "kvattn_cell_bytes",
     "kvattn_append", "kvattn_decode_workspace_bytes", "kvattn_default_num_ctas",
-    "kvattn_decode_gqa", "kvattn_decode_mla", "kvattn_combine",
+    "kvattn_decode_gqa", "kvattn_decode_mla", "kvattn_combine", "kvattn_decode_gqa_noalloc",
 ]
+
+KVATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class KvattnError(RuntimeError):
@@ -92,6 +94,8 @@ def load_library(build: bool = True) -> ctypes.CDLL:
             "kvattn_decode_mla": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz,
                                         i32, P, P]),
             "kvattn_combine": (i32, [P, P, P, P, i32, i32, i32, P, P, P]),
+            "kvattn_decode_gqa_noalloc": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P,
+                                                i32, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -161,6 +165,19 @@ def kvattn_decode_gqa(q, cache: kvattn_cache, block_table, seq_lens, h, h_kv, d_
         _ptr(q), ctypes.byref(cache), _ptr(block_table), _ptr(seq_lens), int(batch),
         int(max_blocks), int(h), int(h_kv), int(d_h), float(scale), _ptr(out), _ptr(lse),
         _ptr(workspace), int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
+        int(num_ctas), _ptr(err), _stream(stream)))
+
+
+def kvattn_decode_gqa_noalloc(q, cache: kvattn_cache, block_table, seq_lens, h, h_kv, d_h,
+                              scale, out, lse, num_ctas=0, err=None, stream=None):
+    """kvattn_decode_gqa without a workspace: for callers that cannot provide
+    device memory.  The scratch is a fixed array inside the library
+    (KVATTN_NOALLOC_SCRATCH_BYTES per GPU); larger problems are rejected, and
+    calls that overlap on the GPU race on it."""
+    batch, max_blocks = block_table.shape
+    _check("kvattn_decode_gqa_noalloc", load_library().kvattn_decode_gqa_noalloc(
+        _ptr(q), ctypes.byref(cache), _ptr(block_table), _ptr(seq_lens), int(batch),
+        int(max_blocks), int(h), int(h_kv), int(d_h), float(scale), _ptr(out), _ptr(lse),
         int(num_ctas), _ptr(err), _stream(stream)))
 
 
