@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="llama3_8b")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch size (smaller profiling cases); 0 = the config's")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
@@ -429,13 +431,14 @@ def main():
     args = parse()
     rank, world, local = env_ranks()
     from kv_cache_decode_paged_gb300 import inputs
+    batch = args.batch or None
     if args.impl == "reference":
         if rank != 0:
             return
-        wl = inputs.make_workload(args.config, seed=args.seed)
+        wl = inputs.make_workload(args.config, seed=args.seed, batch=batch)
         run_reference(args, wl, rank)
         return
-    wl = inputs.make_workload(args.config, seed=args.seed)
+    wl = inputs.make_workload(args.config, seed=args.seed, batch=batch)
     run_ours(args, wl, rank, world, local)
 
 
