@@ -257,3 +257,14 @@ def plant_needle(wl: Workload, b: int, head: int, t: int, strength: float = 30.0
     qv = bf16_to_f32(wl.q[b, head]).astype(np.float64)
     vec = strength * qv / np.linalg.norm(qv)
     wl.k[int(wl.cu_seqlens[b]) + t, head // wl.g] = bf16_bits(vec.astype(np.float32))
+
+
+def plant_needle_mla(wl: Workload, b: int, head: int, t: int, strength: float = 300.0):
+    """Overwrite latent row t of sequence b with ``strength * q~/|q~|`` of one
+    head, so that row dominates that head's softmax."""
+    assert wl.kind == "mla"
+    qv = bf16_to_f32(wl.q[b, head]).astype(np.float64)
+    vec = (strength * qv / np.linalg.norm(qv)).astype(np.float32)
+    n = int(wl.cu_seqlens[b]) + t
+    wl.c_kv[n] = bf16_bits(vec[: wl.d_c])
+    wl.k_r[n] = bf16_bits(vec[wl.d_c:])
