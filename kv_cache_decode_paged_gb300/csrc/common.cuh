@@ -9,12 +9,14 @@
 
 #define KV_DEVI __device__ __forceinline__
 
-// Iteration limit for every spin on an mbarrier.  mbarrier.try_wait already
-// suspends the thread for a hardware-defined interval per call, so this bound
-// is seconds of wall time: far beyond any legitimate wait, short enough that a
-// protocol bug ends the kernel with KVATTN_DEVERR_TIMEOUT instead of a hang.
+// Iteration limit for every spin on an mbarrier.  mbarrier.try_wait may
+// suspend the thread for a hardware-defined interval per call, so this bound
+// is between tens of milliseconds and about a second of wall time: far beyond
+// any legitimate wait inside these kernels (each runs well under a
+// millisecond), short enough that a protocol bug ends the kernel with
+// KVATTN_DEVERR_TIMEOUT quickly instead of hanging.
 #ifndef KV_MAX_SPIN
-#define KV_MAX_SPIN (1u << 22)
+#define KV_MAX_SPIN (1u << 20)
 #endif
 
 namespace kv {
@@ -167,6 +169,18 @@ KV_DEVI void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also ANDs a predicate over the participating threads.
+KV_DEVI bool named_bar_and(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
 }  // namespace kv
 
 // ---- thread-block clusters and distributed shared memory -----------------------
@@ -190,6 +204,28 @@ KV_DEVI void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
                "f"(c), "f"(d)
                : "memory");
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory; its bytes count
+// as completed transactions on that CTA's mbarrier `remote_bar` (no fence, the
+// storing thread does not wait).
+KV_DEVI void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+      : "memory");
+}
+
+// Bulk copy `bytes` (multiple of 16) from this CTA's shared memory to another
+// CTA's shared memory; completes as transaction bytes on that CTA's mbarrier.
+KV_DEVI void bulk_copy_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                               uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
+      : "memory");
 }
 
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's

@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
     for (int k = stream; k < nchunks && ok; k += C::NSTREAM) {
       const uint32_t itk = it + k;
       const int s = itk % C::NSTAGE;
-      if (!mbar_wait(&full[s], (itk / C::NSTAGE) & 1)) {
+      // warp-uniform result: the mma.sync / ldmatrix below need all 32 lanes
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], (itk / C::NSTAGE) & 1) ? 1 : 0)) {
         report(p.err, KVATTN_DEVERR_TIMEOUT);
         *reinterpret_cast<volatile int*>(abort_flag) = 1;
         ok = false;

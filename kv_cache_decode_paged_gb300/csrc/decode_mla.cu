@@ -9,20 +9,31 @@
 //
 // One latent row serves all 128 heads, so this is a dense contraction at about
 // 242 FLOP/byte -- at the GB300 ridge.  It runs on tcgen05 with M = 128 heads.
-// Two facts shape the kernel: O[128 x 512] in fp32 needs all 512 TMEM columns
-// of an SM, and Q[128 x 576] in bf16 needs 147 KB of shared memory.  So a
-// cluster of two CTAs (two SMs) shares each tile of 64 tokens:
+// O[128 x 512] in fp32 would fill all 512 TMEM columns of an SM and Q[128 x 576]
+// would take 147 KB of shared memory, so a cluster of two CTAs (two SMs) shares
+// each tile of 64 latent rows:
 //   * the score contraction is split by K: rank 0 holds Q[:, 0:288], rank 1
-//     Q[:, 288:576]; each computes a partial S[128 x 64] and the two partials are
-//     exchanged through distributed shared memory and added;
-//   * both ranks then compute the same softmax, and each accumulates half of
-//     the output, O[:, 256r : 256r + 256] += P . C[:, 256r : 256r + 256], in its
-//     own TMEM (P is written to TMEM as bf16 and used as the A operand).
-// Each rank loads the five 64-column boxes of every row it needs (dims
-// 256r .. 256r + 319), so box 4 (dims 256..319) is read by both.
+//     Q[:, 288:576] in shared memory; each computes a partial S[128 x 64],
+//     scales it to log2 units, rounds it to f16 and pushes it to the other
+//     rank with one bulk copy; both ranks add the same two f16 partials, so
+//     their softmax inputs are bit-identical;
+//   * both ranks then compute the same softmax, write P to TMEM as bf16 and
+//     accumulate their half O[:, 256r : 256r + 256] += P . C[:, 256r : +256].
+// Rank 0 loads latent dims 0..287 of each row, rank 1 dims 256..575 (dims
+// 256..287 by both); the 32-dim pieces use 64-byte swizzled half boxes.
 //
-// Warps: 0 = TMA producer, 1 = MMA issuer (+ TMEM allocation), 2..5 = softmax,
-// exchange, correction and epilogue (thread = head row).
+// Measured on GB300: a K=16 MMA with M = 128 costs about the same for N = 32,
+// 64 or 128 (~80 cycles), and distributed shared memory sustains only ~20
+// bytes per clock per SM for bulk pushes (~10 for per-thread stores) with ~1000
+// cycles of round-trip latency.  Hence tiles of 64 rows, score MMAs from
+// shared memory, a half-size (f16) exchange moved by the bulk-copy engine, and
+// tile t+1's exchange issued right after P(t) so its latency overlaps P.V(t)
+// and S(t+2) on the tensor pipe.
+//
+// Warps: 0 = TMA producer (3-stage ring), 1 = MMA issuer and TMEM owner,
+// 2..9 = softmax group: two threads per head row, 32 of the tile's 64 tokens
+// each (the pair combines its row max through shared memory).
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include <mutex>
@@ -38,27 +49,32 @@ namespace mla {
 constexpr int ROWW = 576;              // latent row width (d_c + d_rope)
 constexpr int DC = 512;
 constexpr int BS = 64;                 // tokens per page = tokens per tile
-constexpr int NBOX = 5;                // 64-column boxes per rank
-constexpr int QBOX_BYTES = 128 * 128;  // [128 heads x 64 dims] bf16
-constexpr int KBOX_BYTES = BS * 128;   // [64 tokens x 64 dims] bf16
-constexpr int Q_BYTES = NBOX * QBOX_BYTES;         // 80 KB
-constexpr int STAGE_BYTES = NBOX * KBOX_BYTES;     // 40 KB
-constexpr int NSTAGE = 2;
-constexpr int XROW = 64 * 4;                       // one row of a partial score tile
-constexpr int XSLOT = 128 * XROW;                  // 32 KB
-constexpr int NXSLOT = 2;
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + Q_BYTES;
-constexpr int OFF_X = OFF_KV + NSTAGE * STAGE_BYTES;
-constexpr int OFF_BAR = OFF_X + NXSLOT * XSLOT;
-constexpr int NBARS = 32;
+constexpr int QF_BYTES = 128 * 128;    // full Q box [128 heads x 64 dims]
+constexpr int QH_BYTES = 128 * 64;     // half Q box [128 heads x 32 dims]
+constexpr int KF_BYTES = BS * 128;     // full latent box [64 rows x 64 dims]
+constexpr int KH_BYTES = BS * 64;      // half latent box [64 rows x 32 dims]
+constexpr int OFF_QF = 0;              // 4 full Q boxes
+constexpr int OFF_QH = 4 * QF_BYTES;   // 1 half Q box
+constexpr int Q_BYTES = 4 * QF_BYTES + QH_BYTES;        // 72 KB
+constexpr int STAGE_BYTES = 5 * KF_BYTES;               // 40 KB (rank 0 uses 36 KB)
+constexpr int NSTAGE = 3;
+constexpr int OFF_KV = 73728;          // 1024-aligned
+constexpr int XROW = BS * 2;           // one row of a partial score tile, f16 (128 B)
+constexpr int XBYTES = 128 * XROW;     // 16 KB
+constexpr int OFF_X = OFF_KV + NSTAGE * STAGE_BYTES;   // receive buffer (written by the peer)
+constexpr int OFF_XS = OFF_X + XBYTES;                 // send staging
+constexpr int OFF_MX = OFF_XS + XBYTES;   // row-max exchange between the two halves of a row
+constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
+constexpr int NBARS = 24;
 constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
-constexpr int THREADS = 192;
-constexpr int KSTEPS = 18;             // 288 / 16 score k-steps per rank
+constexpr int NSW = 256;               // softmax group: two threads per head row
+constexpr int THREADS = 64 + NSW;
+constexpr int KSTEPS = 18;             // 288 score dims per rank / 16
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;           // S slots at columns 0 and 64 (P aliases them)
+constexpr uint32_t TM_S = 0;           // two S/P slots at columns 0 and 64
 constexpr uint32_t TM_O = 256;         // O half: columns 256..511
 constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the max grows by 2^8
+static_assert(OFF_KV >= Q_BYTES && OFF_KV % 1024 == 0, "layout");
 }  // namespace mla
 
 struct MlaParams {
@@ -78,16 +94,22 @@ struct MlaParams {
 
 // Barrier indices
 enum : int {
-  kQFull = 0, kQEmpty, kOFree,
-  kKVFull0, kKVFull1, kKVEmpty0, kKVEmpty1,
-  kSFull0, kSFull1, kPFull0, kPFull1, kPVDone0, kPVDone1,
-  kXFull0, kXFull1, kXEmpty0, kXEmpty1,
-  kAbort = 31
+  kQFull = 0, kQEmpty = 1, kOFree = 2,
+  kSFull0 = 3,      // 2: S(t) landed in slot t % 2
+  kPFull0 = 5,      // 2: P(t) written to slot t % 2
+  kPVDone0 = 7,     // 2: P.V of tile t finished (by t % 2)
+  kXFull = 9,       // the peer's partial of the next tile is in the exchange buffer (tx bytes)
+  kXEmpty = 10,     // the peer has read this CTA's partial of the last sent tile
+  kKVFull0 = 11,    // 3
+  kKVEmpty0 = 14,   // 3
+  kAbort = 20
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmL, const MlaParams p) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tmQF,
+                      const __grid_constant__ CUtensorMap tmQH,
+                      const __grid_constant__ CUtensorMap tmLF,
+                      const __grid_constant__ CUtensorMap tmLH, const MlaParams p) {
   using namespace mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -105,18 +127,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars[kQFull], 1);
     mbar_init(&bars[kQEmpty], 1);
-    mbar_init(&bars[kOFree], 128);
+    mbar_init(&bars[kOFree], NSW);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kSFull0 + i], 1);
+      mbar_init(&bars[kPFull0 + i], NSW);
+      mbar_init(&bars[kPVDone0 + i], 1);
+    }
+    mbar_init(&bars[kXFull], 1);     // one local expect_tx arrival + the peer's bytes
+    mbar_init(&bars[kXEmpty], 1);    // one arrival from the peer's softmax group
+    for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&bars[kKVFull0 + i], 1);
       mbar_init(&bars[kKVEmpty0 + i], 1);
-      mbar_init(&bars[kSFull0 + i], 1);
-      mbar_init(&bars[kPFull0 + i], 128);
-      mbar_init(&bars[kPVDone0 + i], 1);
-      mbar_init(&bars[kXFull0 + i], 128);   // arrivals from the peer's 128 threads
-      mbar_init(&bars[kXEmpty0 + i], 128);
     }
     *abort_flag = 0;
     fence_barrier_init();
+    mbar_arrive_expect_tx(&bars[kXFull], XBYTES);  // phase 0: the peer's tile 0
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -124,16 +149,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   }
   tc_fence_before();
   // Both CTAs of the cluster start together; this makes each one's barriers
-  // visible to the other before any remote arrive.
+  // visible to the other before any remote access.
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // this rank's latent / query columns: full boxes and the 32-wide half box
+  const int fx0 = rank == 0 ? 0 : 256;     // first full latent box (PV dims)
+  const int qx0 = rank == 0 ? 0 : 320;     // first full Q box
+  const int hx = rank == 0 ? 256 : 288;    // half box (Q; latent for rank 0)
+  const uint32_t stage_tx = rank == 0 ? uint32_t(4 * KF_BYTES + KH_BYTES) : uint32_t(5 * KF_BYTES);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmL);
+      tma_prefetch_desc(&tmQF);
+      tma_prefetch_desc(&tmQH);
+      tma_prefetch_desc(&tmLF);
+      tma_prefetch_desc(&tmLH);
       const uint64_t pol = policy_evict_first();
       Walker w{p.cum, 1, st, en};
       Seg sg;
@@ -142,9 +174,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       while (ok && w.next(sg)) {
         if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
-        for (int i = 0; i < NBOX; ++i)
-          tma_load_3d_nohint(smem + OFF_Q + i * QBOX_BYTES, &tmQ, 64 * (4 * int(rank) + i), 0,
-                             sg.b, &bars[kQFull]);
+        for (int i = 0; i < 4; ++i)
+          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, qx0 + 64 * i, 0, sg.b,
+                             &bars[kQFull]);
+        tma_load_3d_nohint(smem + OFF_QH, &tmQH, hx, 0, sg.b, &bars[kQFull]);
         const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
         for (int j = sg.j0; j < sg.j1 && ok; ++j, ++it) {
           const int s = it % NSTAGE;
@@ -155,10 +188,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             report(p.err, KVATTN_DEVERR_BLOCK_ID);
           else
             page = blk;
-          mbar_arrive_expect_tx(&bars[kKVFull0 + s], STAGE_BYTES);
-          for (int i = 0; i < NBOX; ++i)
-            tma_load_3d(smem + OFF_KV + s * STAGE_BYTES + i * KBOX_BYTES, &tmL,
-                        64 * (4 * int(rank) + i), 0, page, &bars[kKVFull0 + s], pol);
+          uint8_t* stg = smem + OFF_KV + s * STAGE_BYTES;
+          mbar_arrive_expect_tx(&bars[kKVFull0 + s], stage_tx);
+          for (int i = 0; i < 4; ++i)
+            tma_load_3d(stg + i * KF_BYTES, &tmLF, fx0 + 64 * i, 0, page, &bars[kKVFull0 + s], pol);
+          if (rank == 0)
+            tma_load_3d(stg + 4 * KF_BYTES, &tmLH, 256, 0, page, &bars[kKVFull0 + s], pol);
+          else
+            tma_load_3d(stg + 4 * KF_BYTES, &tmLF, 512, 0, page, &bars[kKVFull0 + s], pol);
           if (*abort_flag) ok = false;
         }
         ++seg;
@@ -171,56 +208,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(128, 64, false);
+      const uint32_t id_s = idesc_bf16(128, BS, false);
       const uint32_t id_o = idesc_bf16(128, 256, true);
-      const uint32_t q_base = smem_u32(smem + OFF_Q);
+      const uint32_t qf = smem_u32(smem + OFF_QF), qh = smem_u32(smem + OFF_QH);
       const uint32_t kv_base = smem_u32(smem + OFF_KV);
-      const int j_first = 2 * int(rank);  // first of this rank's 18 score k-steps
       Walker w{p.cum, 1, st, en};
       Seg sg;
       uint32_t it = 0, seg = 0;
       bool ok = true;
-      // issue S(t) = Q_r . K_r(t)^T into S slot t % 2
+      // S(t) = Q_r . K_r(t)^T into S slot t % 2 (18 MMAs, K = 16 each)
       auto issue_s = [&](uint32_t t) -> bool {
         const int s = t % NSTAGE;
         if (!mbar_wait(&bars[kKVFull0 + s], (t / NSTAGE) & 1)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + TM_S + 64 * (t & 1);
+        const uint32_t d = tmem + TM_S + BS * (t & 1);
+        const uint32_t kb = kv_base + s * STAGE_BYTES;
 #pragma unroll 1
-        for (int k = 0; k < KSTEPS; ++k) {
-          const int j = j_first + k;
-          const uint64_t a = sdesc_sw128(q_base + (j >> 2) * QBOX_BYTES + (j & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(kv_base + s * STAGE_BYTES + (j >> 2) * KBOX_BYTES +
-                                             (j & 3) * 32, 16, 1024);
-          umma_ss(d, a, b, id_s, k > 0);
+        for (int j = 0; j < KSTEPS; ++j) {
+          uint64_t a, b;
+          if (rank == 0) {
+            if (j < 16) {
+              a = sdesc_sw128(qf + (j >> 2) * QF_BYTES + (j & 3) * 32, 16, 1024);
+              b = sdesc_sw128(kb + (j >> 2) * KF_BYTES + (j & 3) * 32, 16, 1024);
+            } else {
+              a = sdesc_sw64(qh + (j - 16) * 32, 512);
+              b = sdesc_sw64(kb + 4 * KF_BYTES + (j - 16) * 32, 512);
+            }
+          } else {
+            if (j < 2) {
+              a = sdesc_sw64(qh + j * 32, 512);
+              b = sdesc_sw128(kb + (2 + j) * 32, 16, 1024);
+            } else {
+              const int m = j - 2;
+              a = sdesc_sw128(qf + (m >> 2) * QF_BYTES + (m & 3) * 32, 16, 1024);
+              b = sdesc_sw128(kb + ((m >> 2) + 1) * KF_BYTES + (m & 3) * 32, 16, 1024);
+            }
+          }
+          umma_ss(d, a, b, id_s, j > 0);
         }
         umma_commit(&bars[kSFull0 + (t & 1)]);
         return true;
       };
       while (ok && w.next(sg)) {
-        if (!mbar_wait(&bars[kQFull], seg & 1)) { ok = false; break; }
         const uint32_t n = uint32_t(sg.j1 - sg.j0);
+        if (!mbar_wait(&bars[kQFull], seg & 1)) { ok = false; break; }
+        tc_fence_after();
         const uint32_t it0 = it;
         if (!issue_s(it0)) { ok = false; break; }
+        if (n > 1 && !issue_s(it0 + 1)) { ok = false; break; }
+        if (n <= 2) umma_commit(&bars[kQEmpty]);  // every score MMA of this segment is issued
         for (uint32_t k = 0; k < n && ok; ++k) {
           const uint32_t t = it0 + k;
-          if (k + 1 < n) {
-            if (!issue_s(t + 1)) { ok = false; break; }
-          } else {
-            umma_commit(&bars[kQEmpty]);  // all score MMAs of this segment issued
-          }
           if (k == 0 && seg > 0 && !mbar_wait(&bars[kOFree], (seg - 1) & 1)) { ok = false; break; }
           if (!mbar_wait(&bars[kPFull0 + (t & 1)], (t >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           const int s = t % NSTAGE;
-          const uint32_t pa = tmem + TM_S + 64 * (t & 1);
+          const uint32_t pa = tmem + TM_S + BS * (t & 1);
 #pragma unroll
           for (int kk = 0; kk < BS / 16; ++kk) {
-            const uint64_t b = sdesc_sw128(kv_base + s * STAGE_BYTES + kk * 2048, KBOX_BYTES, 1024);
+            const uint64_t b = sdesc_sw128(kv_base + s * STAGE_BYTES + kk * 2048, KF_BYTES, 1024);
             umma_ts(tmem + TM_O, pa + 8 * kk, b, id_o, (k > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&bars[kKVEmpty0 + s]);
           umma_commit(&bars[kPVDone0 + (t & 1)]);
+          // S(t+2) reuses P(t)'s slot; MMAs run in issue order, so it lands after
+          // P.V(t) has read P(t)
+          if (k + 2 < n) {
+            if (!issue_s(t + 2)) { ok = false; break; }
+            if (k + 3 == n) umma_commit(&bars[kQEmpty]);
+          }
         }
         it += n;
         ++seg;
@@ -234,129 +290,198 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   } else {
     // ------------------------------------- softmax / exchange / epilogue warps
     const int r = 32 * (warp & 3) + lane;          // head row = TMEM lane
+    const int hh = (warp - 2) >> 2;                // which 32 tokens (and 128 O columns)
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-    const int tid = threadIdx.x - 64;              // 0..127
+    const int tid = threadIdx.x - 64;              // 0..255
     uint8_t* xbuf = smem + OFF_X;
-    const uint32_t xrow_local = smem_u32(xbuf) + r * XROW;
-    const uint32_t xrow_peer = map_peer(xrow_local, peer);
-    const uint32_t xfull_peer0 = map_peer(smem_u32(&bars[kXFull0]), peer);
-    const uint32_t xempty_peer0 = map_peer(smem_u32(&bars[kXEmpty0]), peer);
+    uint8_t* xstage = smem + OFF_XS;
+    float* mx_s = reinterpret_cast<float*>(smem + OFF_MX);   // [2][128]
+    const uint32_t xbuf_peer = map_peer(smem_u32(xbuf), peer);
+    const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull]), peer);
+    const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty]), peer);
     Walker w{p.cum, 1, st, en};
     Seg sg;
     uint32_t it = 0;
     bool ok = true;
+    // Every wait result is made warp-uniform: the warp-collective TMEM
+    // instructions that follow must be executed by all 32 lanes or none.
+    auto wait_all = [](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
+    };
+    auto wait_all_cluster = [](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity) ? 1 : 0) != 0;
+    };
+    // This thread's 32 partial scores of tile t, in log2 units, as f16 pairs.
+    auto own_partial = [&](uint32_t t, uint32_t (&h)[16]) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + TM_S + BS * (t & 1) + 32 * hh, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        h[j] = pack_f16(__uint_as_float(v[2 * j]) * p.scale_log2,
+                        __uint_as_float(v[2 * j + 1]) * p.scale_log2);
+    };
+    // Push this rank's partial of tile t to the peer: stage it locally (row r,
+    // 16-byte chunks XOR-swizzled by r), then one bulk copy after the peer has
+    // released the previous tile (which also means the previous copy has
+    // finished reading the staging buffer).  `good` is the caller's state; the
+    // result is uniform over the group (the named barrier ANDs it).
+    auto send = [&](uint32_t t, bool good, uint32_t (&h)[16]) -> bool {
+      good = good && wait_all(&bars[kSFull0 + (t & 1)], (t >> 1) & 1);
+      if (good) {
+        tc_fence_after();
+        own_partial(t, h);
+        good = wait_all_cluster(&bars[kXEmpty], (t & 1) ^ 1);
+        if (good) {
+          uint4* srow = reinterpret_cast<uint4*>(xstage + r * XROW);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            srow[(4 * hh + c) ^ (r & 7)] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+      }
+      good = named_bar_and(2, NSW, good);
+      if (good && tid == 0) bulk_copy_to_peer(xbuf_peer, xstage, XBYTES, xfull_peer);
+      return good;
+    };
+
+    uint32_t hcur[16], hnext[16];
     while (ok && w.next(sg)) {
-      int len = p.seq_lens[sg.b];
-      len = max(0, min(len, sg.n * BS));
+      const int len = max(0, min(p.seq_lens[sg.b], sg.n * BS));
       const uint32_t n = uint32_t(sg.j1 - sg.j0);
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
+      if (!send(it, true, hcur)) { ok = false; break; }
       for (uint32_t k = 0; k < n && ok; ++k) {
         const uint32_t t = it + k;
         const int slot = t & 1;
-        if (!mbar_wait(&bars[kSFull0 + slot], (t >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t sa[32], sb[32];
-        tmem_ld32(tmem + lane_off + TM_S + 64 * slot, sa);
-        tmem_ld32(tmem + lane_off + TM_S + 64 * slot + 32, sb);
-        tmem_ld_wait();
-        // send my partial scores to the peer (XOR-swizzled 16-byte chunks)
-        if (!mbar_wait(&bars[kXEmpty0 + slot], ((t >> 1) & 1) ^ 1)) { ok = false; break; }
-        const uint32_t xs = uint32_t(slot) * XSLOT;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t* src = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
-          st_cluster_v4(xrow_peer + xs + ((c ^ (r & 15)) << 4), __uint_as_float(src[0]),
-                        __uint_as_float(src[1]), __uint_as_float(src[2]), __uint_as_float(src[3]));
-        }
-        mbar_arrive_remote(xfull_peer0 + 8 * slot);
-        if (!mbar_wait_cluster(&bars[kXFull0 + slot], (t >> 1) & 1)) { ok = false; break; }
-        float sc[64];
-        const float4* xr = reinterpret_cast<const float4*>(xbuf + xs + r * XROW);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 v = xr[c ^ (r & 15)];
-          const uint32_t* src = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
-          sc[4 * c + 0] = __uint_as_float(src[0]) + v.x;
-          sc[4 * c + 1] = __uint_as_float(src[1]) + v.y;
-          sc[4 * c + 2] = __uint_as_float(src[2]) + v.z;
-          sc[4 * c + 3] = __uint_as_float(src[3]) + v.w;
-        }
-        mbar_arrive_remote(xempty_peer0 + 8 * slot);  // done reading what the peer sent
-
-        const int valid = len - (sg.j0 + int(k)) * BS;
+        // A failed (bounded) wait below does not leave the loop at once: the
+        // warp skips its work and the group agrees to stop at the next barrier.
+        bool good = wait_all_cluster(&bars[kXFull], t & 1);
+        float sc[32];
         float mx = -INFINITY;
+        const int valid = len - (sg.j0 + int(k)) * BS - 32 * hh;
+        if (good) {
+          if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull], XBYTES);  // next tile's bytes
+          const uint4* xr = reinterpret_cast<const uint4*>(xbuf + r * XROW);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          sc[j] = j < valid ? sc[j] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sc[j]);
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = xr[(4 * hh + c) ^ (r & 7)];
+            const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              // both ranks add the same two f16 partials: bit-identical scores
+              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&hcur[4 * c + q]));
+              const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&pv[q]));
+              sc[8 * c + 2 * q] = a.x + b.x;
+              sc[8 * c + 2 * q + 1] = a.y + b.y;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            sc[j] = j < valid ? sc[j] : -INFINITY;
+            mx = fmaxf(mx, sc[j]);
+          }
+          mx_s[hh * 128 + r] = mx;
         }
-        if (k == 0) {
-          m_ref = mx;
-        } else if (mx > m_ref + RESCALE_THRESHOLD) {
-          // the running max grew a lot: rescale O (after the previous P.V landed) and l
-          if (!mbar_wait(&bars[kPVDone0 + ((t - 1) & 1)], ((t - 1) >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const float alpha = exp2_approx(m_ref - mx);
-          m_ref = mx;
-          l *= alpha;
+        // the row max over both halves of the tile
+        good = named_bar_and(3, NSW, good);
+        // Every thread has read the peer's partial (before the barrier): release
+        // the exchange buffer.  One thread that has issued no bulk copy does it,
+        // so its cluster-scope release does not wait for an outgoing copy.
+        if (good && tid == 32) mbar_arrive_remote(xempty_peer);
+        if (good) {
+          mx = fmaxf(mx, mx_s[(hh ^ 1) * 128 + r]);
+          if (k == 0) {
+            m_ref = mx;
+          } else if (__any_sync(0xffffffffu, mx > m_ref + RESCALE_THRESHOLD)) {
+            // Some row's running max grew a lot: rescale this thread's half of
+            // O (after the previous P.V landed) and l.  Both warps of a row pair
+            // see the same maxima, so they take this branch together; TMEM
+            // accesses are warp-collective, rows that keep their max scale by 1.
+            good = wait_all(&bars[kPVDone0 + ((t - 1) & 1)], ((t - 1) >> 1) & 1);
+            if (good) {
+              tc_fence_after();
+              const float m_new = mx > m_ref + RESCALE_THRESHOLD ? mx : m_ref;
+              const float alpha = exp2_approx(m_ref - m_new);
+              m_ref = m_new;
+              l *= alpha;
 #pragma unroll 1
-          for (int cb = 0; cb < 256; cb += 32) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + TM_O + cb, o);
-            tmem_ld_wait();
+              for (int cb = 0; cb < 128; cb += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + TM_O + 128 * hh + cb, o);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(tmem + lane_off + TM_O + cb, o);
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                tmem_st32(tmem + lane_off + TM_O + 128 * hh + cb, o);
+              }
+              tmem_st_wait();
+            }
           }
-          tmem_st_wait();
-        }
-        uint32_t pk[32];
-        float lsum = 0.f;
+          if (good) {
+            uint32_t pk[16];
+            float lsum = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = exp2_approx(sc[2 * j] - m_ref), p1 = exp2_approx(sc[2 * j + 1] - m_ref);
-          lsum += p0 + p1;
-          pk[j] = pack_bf16(p0, p1);
-        }
-        l += lsum;
-        tmem_st32(tmem + lane_off + TM_S + 64 * slot, pk);
-        tmem_st_wait();
-        if (valid < BS) {
-          // Zero the latent rows past the end of the sequence in the four boxes
-          // the P.V product reads: P is 0 there, but 0 * NaN would be NaN.
-          uint8_t* stg = smem + OFF_KV + (t % NSTAGE) * STAGE_BYTES;
-          const int nrow = BS - max(valid, 0);
-          for (int idx = tid; idx < nrow * 4 * 8; idx += 128) {
-            const int row = max(valid, 0) + idx / 32, rem = idx % 32;
-            *reinterpret_cast<uint4*>(stg + (rem >> 3) * KBOX_BYTES + row * 128 + (rem & 7) * 16) =
-                make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 16; ++j) {
+              const float p0 = exp2_approx(sc[2 * j] - m_ref), p1 = exp2_approx(sc[2 * j + 1] - m_ref);
+              lsum += p0 + p1;
+              pk[j] = pack_bf16(p0, p1);
+            }
+            l += lsum;
+            tmem_st16(tmem + lane_off + TM_S + BS * slot + 16 * hh, pk);
+            tmem_st_wait();
+            const int vt = len - (sg.j0 + int(k)) * BS;   // valid rows of the whole tile
+            if (vt < BS) {
+              // Zero the latent rows past the end of the sequence in the four
+              // boxes the P.V product reads: P is 0 there, but 0 * NaN is NaN.
+              uint8_t* stg = smem + OFF_KV + (t % NSTAGE) * STAGE_BYTES;
+              const int v0 = max(vt, 0);
+              for (int idx = tid; idx < (BS - v0) * 4 * 8; idx += NSW) {
+                const int row = v0 + idx / 32, rem = idx % 32;
+                *reinterpret_cast<uint4*>(stg + (rem >> 3) * KF_BYTES + row * 128 + (rem & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[kPFull0 + slot]);
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
-        tc_fence_before();
-        mbar_arrive(&bars[kPFull0 + slot]);
+        if (k + 1 < n) {
+          ok = send(t + 1, good, hnext);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) hcur[j] = hnext[j];
+        } else {
+          ok = named_bar_and(2, NSW, good);
+        }
       }
       if (!ok) break;
-      // epilogue: O / l for this segment's rows
+      // ---- epilogue: O / l for this segment's rows (each thread: 128 columns)
       const uint32_t last = it + n - 1;
-      if (!mbar_wait(&bars[kPVDone0 + (last & 1)], (last >> 1) & 1)) { ok = false; break; }
+      // group-uniform, like every failure decision of this group
+      if (!named_bar_and(2, NSW, wait_all(&bars[kPVDone0 + (last & 1)], (last >> 1) & 1))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
+      mx_s[hh * 128 + r] = l;
+      named_bar_sync(3, NSW);
+      const float lrow = l + mx_s[(hh ^ 1) * 128 + r];
       const bool row_ok = r < p.h;
       float* dst;
       float* dl;
       if (sg.full) {
-        dst = p.out + (int64_t(sg.b) * p.h + r) * DC + 256 * rank;
+        dst = p.out + (int64_t(sg.b) * p.h + r) * DC + 256 * rank + 128 * hh;
         dl = p.lse + int64_t(sg.b) * p.h + r;
       } else {
         const int64_t slot_idx = int64_t(sg.b) + pair;
-        dst = p.part_out + (slot_idx * p.h + r) * DC + 256 * rank;
+        dst = p.part_out + (slot_idx * p.h + r) * DC + 256 * rank + 128 * hh;
         dl = p.part_lse + slot_idx * p.h + r;
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
 #pragma unroll 1
-      for (int cb = 0; cb < 256; cb += 32) {
+      for (int cb = 0; cb < 128; cb += 32) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + TM_O + cb, o);
+        tmem_ld32(tmem + lane_off + TM_O + 128 * hh + cb, o);
         tmem_ld_wait();
         if (row_ok) {
           float4* d4 = reinterpret_cast<float4*>(dst + cb);
@@ -366,20 +491,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
                                 __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
         }
       }
-      if (row_ok && rank == 0) *dl = (l > 0.f) ? (m_ref + log2_approx(l)) * kLn2 : -INFINITY;
+      if (row_ok && rank == 0 && hh == 0)
+        *dl = (lrow > 0.f) ? (m_ref + log2_approx(lrow)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&bars[kOFree]);
       it += n;
-      if (*abort_flag) ok = false;
+      // the row-sum slots are rewritten next segment only after this barrier
+      ok = named_bar_and(2, NSW, *abort_flag == 0);
     }
     if (!ok) {
       report(p.err, KVATTN_DEVERR_TIMEOUT);
       *abort_flag = 1;
     }
-    // Drain: the peer's last two "done reading" arrivals target this CTA's
-    // barriers; wait for them so this CTA's shared memory outlives every access.
-    for (uint32_t t = it > 2 ? it - 2 : 0; t < it; ++t)
-      mbar_wait_cluster(&bars[kXEmpty0 + (t & 1)], (t >> 1) & 1);
+    // Drain: the peer's last "done reading" arrival targets this CTA's barrier;
+    // wait for it so this CTA's shared memory outlives every remote access.
+    if (it > 0) mbar_wait_cluster(&bars[kXEmpty], (it - 1) & 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -444,21 +570,25 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   pa.err = a.err;
   if (launch_plan(pa, a.stream) != cudaSuccess) return KVATTN_ERR_CUDA;
 
-  alignas(64) CUtensorMap tmQ, tmL;
+  alignas(64) CUtensorMap tmQF, tmQH, tmLF, tmLH;
   {
     const uint64_t dims[3] = {uint64_t(mla::ROWW), uint64_t(a.h), uint64_t(a.B)};
     const uint64_t strides[2] = {uint64_t(mla::ROWW) * 2, uint64_t(mla::ROWW) * 2 * a.h};
-    const uint32_t box[3] = {64u, 128u, 1u};
-    if (!encode_tensor_map_3d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, dims, strides, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint32_t boxf[3] = {64u, 128u, 1u}, boxh[3] = {32u, 128u, 1u};
+    if (!encode_tensor_map_3d(&tmQF, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, dims, strides, boxf,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_3d(&tmQH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, dims, strides, boxh,
+                              CU_TENSOR_MAP_SWIZZLE_64B))
       return KVATTN_ERR_CUDA;
   }
   {
     const uint64_t dims[3] = {uint64_t(mla::ROWW), uint64_t(mla::BS), uint64_t(cc->num_blocks)};
     const uint64_t strides[2] = {uint64_t(mla::ROWW) * 2, uint64_t(mla::ROWW) * 2 * mla::BS};
-    const uint32_t box[3] = {64u, uint32_t(mla::BS), 1u};
-    if (!encode_tensor_map_3d(&tmL, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->latent, dims, strides,
-                              box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint32_t boxf[3] = {64u, uint32_t(mla::BS), 1u}, boxh[3] = {32u, uint32_t(mla::BS), 1u};
+    if (!encode_tensor_map_3d(&tmLF, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->latent, dims, strides,
+                              boxf, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_3d(&tmLH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->latent, dims, strides,
+                              boxh, CU_TENSOR_MAP_SWIZZLE_64B))
       return KVATTN_ERR_CUDA;
   }
   MlaParams prm;
@@ -476,7 +606,7 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   prm.num_blocks = cc->num_blocks;
   prm.scale_log2 = a.scale * kLog2e;
   prm.err = a.err;
-  mla_decode_kernel<<<2 * G, mla::THREADS, mla::SMEM, a.stream>>>(tmQ, tmL, prm);
+  mla_decode_kernel<<<2 * G, mla::THREADS, mla::SMEM, a.stream>>>(tmQF, tmQH, tmLF, tmLH, prm);
   if (cudaGetLastError() != cudaSuccess) return KVATTN_ERR_CUDA;
   if (launch_combine(prm.part_out, prm.part_lse, pa.split_first, pa.split_count, a.B, a.h,
                      mla::DC, a.out, a.lse, true, a.stream) != cudaSuccess)

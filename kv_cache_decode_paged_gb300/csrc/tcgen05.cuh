@@ -57,6 +57,18 @@ KV_DEVI uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// Same for a 64-byte swizzled K-major operand (rows of 64 bytes, 8-row atoms
+// `sbo` bytes apart).
+KV_DEVI uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFF);
+  d |= uint64_t(1) << 16;  // leading byte offset unused for swizzled K-major
+  d |= uint64_t((sbo >> 4) & 0x3FFF) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(4) << 61;  // 64-byte swizzle
+  return d;
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 KV_DEVI void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                      uint32_t accumulate) {
@@ -107,6 +119,13 @@ KV_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
           taddr),
       KV_W8(0), KV_W8(8), KV_W8(16), KV_W8(24)
+      : "memory");
+}
+KV_DEVI void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      KV_W8(0), KV_W8(8)
       : "memory");
 }
 KV_DEVI void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
