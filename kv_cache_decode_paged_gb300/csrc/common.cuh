@@ -67,6 +67,19 @@ KV_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test: has the phase with the given parity completed?
+KV_DEVI bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.
 KV_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < KV_MAX_SPIN; ++i)
@@ -181,6 +194,18 @@ KV_DEVI bool named_bar_and(int id, int threads, bool pred) {
   return r != 0;
 }
 
+// Same, OR over the threads of the barrier.
+KV_DEVI bool named_bar_or(int id, int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
 }  // namespace kv
 
 // ---- thread-block clusters and distributed shared memory -----------------------
@@ -232,6 +257,14 @@ KV_DEVI void bulk_copy_to_peer(uint32_t dst_cluster, const void* src, uint32_t b
 // prior writes (including its distributed shared memory stores) at cluster scope.
 KV_DEVI void mbar_arrive_remote(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster without ordering this
+// thread's memory accesses: for "done reading" signals whose reads have
+// already returned their values.
+KV_DEVI void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                : "memory");
 }
 

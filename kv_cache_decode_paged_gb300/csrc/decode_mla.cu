@@ -11,28 +11,34 @@
 // 242 FLOP/byte -- at the GB300 ridge.  It runs on tcgen05 with M = 128 heads.
 // O[128 x 512] in fp32 would fill all 512 TMEM columns of an SM and Q[128 x 576]
 // would take 147 KB of shared memory, so a cluster of two CTAs (two SMs) shares
-// each tile of 64 latent rows:
-//   * the score contraction is split by K: rank 0 holds Q[:, 0:288], rank 1
-//     Q[:, 288:576] in shared memory; each computes a partial S[128 x 64],
-//     scales it to log2 units, rounds it to f16 and pushes it to the other
-//     rank with one bulk copy; both ranks add the same two f16 partials, so
-//     their softmax inputs are bit-identical;
-//   * both ranks then compute the same softmax, write P to TMEM as bf16 and
-//     accumulate their half O[:, 256r : 256r + 256] += P . C[:, 256r : +256].
-// Rank 0 loads latent dims 0..287 of each row, rank 1 dims 256..575 (dims
-// 256..287 by both); the 32-dim pieces use 64-byte swizzled half boxes.
+// each tile of 64 latent rows, split by latent dimension:
+//   rank r owns dims D_r = [256r, 256r + 256) U [512 + 32r, 544 + 32r),
+// i.e. half of c_KV and half of k_R.  It loads only those 288 dims of Q and of
+// every row (no byte is loaded twice), computes the partial score
+// S_r = Q[:, D_r] . row[:, D_r]^T  (M = 128 heads, N = 64 rows, K = 288), and
+// its half of the output O[:, 256r : 256r + 256] += P . c[:, 256r : 256r + 256]
+// (the c_KV part of D_r is exactly the value columns it needs).
+// The two partial scores meet through distributed shared memory: each rank
+// scales its partial to log2 units, rounds it to f16 and pushes it to the
+// other with one bulk copy; both ranks add the same two f16 partials, so their
+// softmax inputs and P are bit-identical.
 //
-// Measured on GB300: a K=16 MMA with M = 128 costs about the same for N = 32,
-// 64 or 128 (~80 cycles), and distributed shared memory sustains only ~20
-// bytes per clock per SM for bulk pushes (~10 for per-thread stores) with ~1000
-// cycles of round-trip latency.  Hence tiles of 64 rows, score MMAs from
-// shared memory, a half-size (f16) exchange moved by the bulk-copy engine, and
-// tile t+1's exchange issued right after P(t) so its latency overlaps P.V(t)
-// and S(t+2) on the tensor pipe.
-//
-// Warps: 0 = TMA producer (3-stage ring), 1 = MMA issuer and TMEM owner,
-// 2..9 = softmax group: two threads per head row, 32 of the tile's 64 tokens
-// each (the pair combines its row max through shared memory).
+// Measured on GB300: a K = 16 MMA with M = 128 reading both operands from
+// shared memory costs ~78 cycles for any N <= 128 (and 128 cycles at N = 256);
+// with A in tensor memory ~123 cycles for N <= 128 and ~136 at N = 256.  A
+// distributed-shared-memory push has ~1000 cycles of latency.  The kernel is
+// therefore organised so that the exchange of tile t+1 overlaps the softmax of
+// tile t:
+//   warp 0      TMA producer: Q per sequence; per tile 4 value boxes (3-stage
+//               ring) and one rope box (2-slot ring, freed once S is computed)
+//   warp 1      MMA issuer and TMEM owner: S(t) into one of two S slots, P.V(t)
+//               from one of two P slots, issued in whichever order their inputs
+//               become ready
+//   warps 10-13 senders: S(t) partial -> f16 -> staging -> bulk copy to the peer
+//               (one thread per head row)
+//   warps 2-9   softmax: peer partial + own partial, online softmax with lazy
+//               rescaling, P(t) -> TMEM, epilogue (two threads per head row,
+//               32 of the tile's 64 rows each)
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -49,32 +55,40 @@ namespace mla {
 constexpr int ROWW = 576;              // latent row width (d_c + d_rope)
 constexpr int DC = 512;
 constexpr int BS = 64;                 // tokens per page = tokens per tile
-constexpr int QF_BYTES = 128 * 128;    // full Q box [128 heads x 64 dims]
-constexpr int QH_BYTES = 128 * 64;     // half Q box [128 heads x 32 dims]
-constexpr int KF_BYTES = BS * 128;     // full latent box [64 rows x 64 dims]
-constexpr int KH_BYTES = BS * 64;      // half latent box [64 rows x 32 dims]
-constexpr int OFF_QF = 0;              // 4 full Q boxes
-constexpr int OFF_QH = 4 * QF_BYTES;   // 1 half Q box
-constexpr int Q_BYTES = 4 * QF_BYTES + QH_BYTES;        // 72 KB
-constexpr int STAGE_BYTES = 5 * KF_BYTES;               // 40 KB (rank 0 uses 36 KB)
-constexpr int NSTAGE = 3;
-constexpr int OFF_KV = 73728;          // 1024-aligned
-constexpr int XROW = BS * 2;           // one row of a partial score tile, f16 (128 B)
-constexpr int XBYTES = 128 * XROW;     // 16 KB
-constexpr int OFF_X = OFF_KV + NSTAGE * STAGE_BYTES;   // receive buffer (written by the peer)
-constexpr int OFF_XS = OFF_X + XBYTES;                 // send staging
-constexpr int OFF_MX = OFF_XS + XBYTES;   // row-max exchange between the two halves of a row
+constexpr int QF_BYTES = 128 * 128;    // Q box [128 heads x 64 dims], 128-byte swizzle
+constexpr int QH_BYTES = 128 * 64;     // Q box [128 heads x 32 rope dims], 64-byte swizzle
+constexpr int VF_BYTES = BS * 128;     // latent box [64 rows x 64 dims]
+constexpr int RH_BYTES = BS * 64;      // latent box [64 rows x 32 rope dims]
+constexpr int OFF_QF = 0;
+constexpr int OFF_QH = 4 * QF_BYTES;
+constexpr int Q_BYTES = 4 * QF_BYTES + QH_BYTES;          // 72 KB
+constexpr int NSTAGE = 3;                                 // value ring
+constexpr int VSTAGE = 4 * VF_BYTES;                      // 32 KB
+constexpr int OFF_V = Q_BYTES;
+constexpr int NROPE = 2;                                  // rope ring
+constexpr int OFF_R = OFF_V + NSTAGE * VSTAGE;
+constexpr int XROW = BS * 2;                              // a row of a partial tile, f16
+constexpr int XBYTES = 128 * XROW;                        // 16 KB
+constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // 2 receive slots (peer writes)
+constexpr int OFF_XS = OFF_X + 2 * XBYTES;                // send staging
+constexpr int OFF_MX = OFF_XS + XBYTES;                   // row max / row sum exchange
 constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
-constexpr int NBARS = 24;
+constexpr int NBARS = 26;
 constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
-constexpr int NSW = 256;               // softmax group: two threads per head row
-constexpr int THREADS = 64 + NSW;
+constexpr int NSW = 256;               // softmax warps: two threads per head row
+constexpr int NSEND = 128;             // sender warps: one thread per head row
+constexpr int SW0 = 64, SEND0 = 64 + NSW;
+constexpr int THREADS = 64 + NSW + NSEND;
 constexpr int KSTEPS = 18;             // 288 score dims per rank / 16
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;           // two S/P slots at columns 0 and 64
+constexpr uint32_t TM_S = 0;           // two S slots of 64 columns
+constexpr uint32_t TM_P = 128;         // two P slots of 32 columns (bf16 pairs)
 constexpr uint32_t TM_O = 256;         // O half: columns 256..511
 constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the max grows by 2^8
-static_assert(OFF_KV >= Q_BYTES && OFF_KV % 1024 == 0, "layout");
+static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
+                  OFF_XS % 1024 == 0,
+              "swizzled tiles need 1024-byte alignment");
+static_assert(SMEM <= 232448, "shared memory");
 }  // namespace mla
 
 struct MlaParams {
@@ -95,15 +109,24 @@ struct MlaParams {
 // Barrier indices
 enum : int {
   kQFull = 0, kQEmpty = 1, kOFree = 2,
-  kSFull0 = 3,      // 2: S(t) landed in slot t % 2
-  kPFull0 = 5,      // 2: P(t) written to slot t % 2
-  kPVDone0 = 7,     // 2: P.V of tile t finished (by t % 2)
-  kXFull = 9,       // the peer's partial of the next tile is in the exchange buffer (tx bytes)
-  kXEmpty = 10,     // the peer has read this CTA's partial of the last sent tile
-  kKVFull0 = 11,    // 3
-  kKVEmpty0 = 14,   // 3
-  kAbort = 20
+  kSFull0 = 3,      // 2: S(t) landed in S slot t % 2
+  kSRead0 = 5,      // 2: the senders and the softmax warps have read S slot t % 2
+  kPFull0 = 7,      // 2: P(t) written to P slot t % 2
+  kPVDone0 = 9,     // 2: P.V of tile t finished
+  kXFull0 = 11,     // 2: the peer's partial of tile t is in receive slot t % 2 (tx bytes)
+  kXEmpty0 = 13,    // 2: the peer has read this rank's partial from its receive slot t % 2
+  kXSent = 15,      // the peer has received this rank's last partial: staging is free
+  kKVFull0 = 16,    // 3: value boxes (and the rope box) of the tile landed
+  kKVEmpty0 = 19,   // 3: P.V finished with the value stage
+  kRopeEmpty0 = 22, // 2: S finished with the rope slot
+  kAbort = 24
 };
+
+// One f16 pair of scaled partial scores: senders and softmax warps round the
+// same fp32 values the same way.
+KV_DEVI uint32_t partial_pair(uint32_t a, uint32_t b, float scale_log2) {
+  return pack_f16(__uint_as_float(a) * scale_log2, __uint_as_float(b) * scale_log2);
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmQF,
@@ -130,18 +153,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     mbar_init(&bars[kOFree], NSW);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kSFull0 + i], 1);
+      mbar_init(&bars[kSRead0 + i], (NSW + NSEND) / 32);  // one arrival per reading warp
       mbar_init(&bars[kPFull0 + i], NSW);
       mbar_init(&bars[kPVDone0 + i], 1);
+      mbar_init(&bars[kXFull0 + i], 1);    // one local expect_tx arrival + the peer's bytes
+      mbar_init(&bars[kXEmpty0 + i], 1);   // one arrival from the peer's softmax warps
+      mbar_init(&bars[kRopeEmpty0 + i], 1);
     }
-    mbar_init(&bars[kXFull], 1);     // one local expect_tx arrival + the peer's bytes
-    mbar_init(&bars[kXEmpty], 1);    // one arrival from the peer's softmax group
+    mbar_init(&bars[kXSent], 1);           // one arrival from the peer's softmax warps
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&bars[kKVFull0 + i], 1);
       mbar_init(&bars[kKVEmpty0 + i], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bars[kXFull], XBYTES);  // phase 0: the peer's tile 0
+    mbar_arrive_expect_tx(&bars[kXFull0], XBYTES);      // the peer's tiles 0 and 1
+    mbar_arrive_expect_tx(&bars[kXFull0 + 1], XBYTES);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -153,11 +180,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // this rank's latent / query columns: full boxes and the 32-wide half box
-  const int fx0 = rank == 0 ? 0 : 256;     // first full latent box (PV dims)
-  const int qx0 = rank == 0 ? 0 : 320;     // first full Q box
-  const int hx = rank == 0 ? 256 : 288;    // half box (Q; latent for rank 0)
-  const uint32_t stage_tx = rank == 0 ? uint32_t(4 * KF_BYTES + KH_BYTES) : uint32_t(5 * KF_BYTES);
+  const int vx0 = 256 * int(rank);       // first value dim of this rank
+  const int rx = 512 + 32 * int(rank);   // first rope dim of this rank
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -175,27 +199,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
         for (int i = 0; i < 4; ++i)
-          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, qx0 + 64 * i, 0, sg.b,
+          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 64 * i, 0, sg.b,
                              &bars[kQFull]);
-        tma_load_3d_nohint(smem + OFF_QH, &tmQH, hx, 0, sg.b, &bars[kQFull]);
+        tma_load_3d_nohint(smem + OFF_QH, &tmQH, rx, 0, sg.b, &bars[kQFull]);
         const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
         for (int j = sg.j0; j < sg.j1 && ok; ++j, ++it) {
-          const int s = it % NSTAGE;
-          if (!mbar_wait(&bars[kKVEmpty0 + s], ((it / NSTAGE) & 1) ^ 1)) { ok = false; break; }
+          const int s = it % NSTAGE, q = it & 1;
+          if (!mbar_wait(&bars[kKVEmpty0 + s], ((it / NSTAGE) & 1) ^ 1) ||
+              !mbar_wait(&bars[kRopeEmpty0 + q], ((it >> 1) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
           const int blk = row[j];
           int page = int(p.num_blocks);  // out of range: zero fill
           if (blk < 0 || int64_t(blk) >= p.num_blocks)
             report(p.err, KVATTN_DEVERR_BLOCK_ID);
           else
             page = blk;
-          uint8_t* stg = smem + OFF_KV + s * STAGE_BYTES;
-          mbar_arrive_expect_tx(&bars[kKVFull0 + s], stage_tx);
+          uint8_t* stg = smem + OFF_V + s * VSTAGE;
+          mbar_arrive_expect_tx(&bars[kKVFull0 + s], uint32_t(VSTAGE + RH_BYTES));
           for (int i = 0; i < 4; ++i)
-            tma_load_3d(stg + i * KF_BYTES, &tmLF, fx0 + 64 * i, 0, page, &bars[kKVFull0 + s], pol);
-          if (rank == 0)
-            tma_load_3d(stg + 4 * KF_BYTES, &tmLH, 256, 0, page, &bars[kKVFull0 + s], pol);
-          else
-            tma_load_3d(stg + 4 * KF_BYTES, &tmLF, 512, 0, page, &bars[kKVFull0 + s], pol);
+            tma_load_3d(stg + i * VF_BYTES, &tmLF, vx0 + 64 * i, 0, page, &bars[kKVFull0 + s], pol);
+          tma_load_3d(smem + OFF_R + q * RH_BYTES, &tmLH, rx, 0, page, &bars[kKVFull0 + s], pol);
           if (*abort_flag) ok = false;
         }
         ++seg;
@@ -211,74 +236,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       const uint32_t id_s = idesc_bf16(128, BS, false);
       const uint32_t id_o = idesc_bf16(128, 256, true);
       const uint32_t qf = smem_u32(smem + OFF_QF), qh = smem_u32(smem + OFF_QH);
-      const uint32_t kv_base = smem_u32(smem + OFF_KV);
+      const uint32_t v_base = smem_u32(smem + OFF_V), r_base = smem_u32(smem + OFF_R);
       Walker w{p.cum, 1, st, en};
       Seg sg;
       uint32_t it = 0, seg = 0;
       bool ok = true;
-      // S(t) = Q_r . K_r(t)^T into S slot t % 2 (18 MMAs, K = 16 each)
-      auto issue_s = [&](uint32_t t) -> bool {
-        const int s = t % NSTAGE;
-        if (!mbar_wait(&bars[kKVFull0 + s], (t / NSTAGE) & 1)) return false;
+      // Descriptors are built once; a K step only moves the start address, whose
+      // field is the low bits of the descriptor (address / 16, no carry below
+      // 256 KB).  The issue loop is unrolled so that one thread can feed the
+      // tensor core back to back: with the address arithmetic in the loop the
+      // issue, not the tensor core, set the pace.
+      const uint64_t qa0 = sdesc_sw128(qf, 16, 1024), qh0 = sdesc_sw64(qh, 512);
+      // S(t) = Q[:, D_r] . row(t)[:, D_r]^T into S slot t % 2 (18 MMAs, K = 16 each)
+      auto issue_s = [&](uint32_t t) {
         tc_fence_after();
         const uint32_t d = tmem + TM_S + BS * (t & 1);
-        const uint32_t kb = kv_base + s * STAGE_BYTES;
-#pragma unroll 1
+        const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VSTAGE, 16, 1024);
+        const uint64_t rb0 = sdesc_sw64(r_base + (t & 1) * RH_BYTES, 512);
+#pragma unroll
         for (int j = 0; j < KSTEPS; ++j) {
-          uint64_t a, b;
-          if (rank == 0) {
-            if (j < 16) {
-              a = sdesc_sw128(qf + (j >> 2) * QF_BYTES + (j & 3) * 32, 16, 1024);
-              b = sdesc_sw128(kb + (j >> 2) * KF_BYTES + (j & 3) * 32, 16, 1024);
-            } else {
-              a = sdesc_sw64(qh + (j - 16) * 32, 512);
-              b = sdesc_sw64(kb + 4 * KF_BYTES + (j - 16) * 32, 512);
-            }
-          } else {
-            if (j < 2) {
-              a = sdesc_sw64(qh + j * 32, 512);
-              b = sdesc_sw128(kb + (2 + j) * 32, 16, 1024);
-            } else {
-              const int m = j - 2;
-              a = sdesc_sw128(qf + (m >> 2) * QF_BYTES + (m & 3) * 32, 16, 1024);
-              b = sdesc_sw128(kb + ((m >> 2) + 1) * KF_BYTES + (m & 3) * 32, 16, 1024);
-            }
-          }
-          umma_ss(d, a, b, id_s, j > 0);
+          if (j < 16)
+            umma_ss(d, qa0 + uint64_t(((j >> 2) * QF_BYTES + (j & 3) * 32) >> 4),
+                    vb0 + uint64_t(((j >> 2) * VF_BYTES + (j & 3) * 32) >> 4), id_s, j > 0);
+          else
+            umma_ss(d, qh0 + uint64_t(((j - 16) * 32) >> 4), rb0 + uint64_t(((j - 16) * 32) >> 4),
+                    id_s, 1u);
         }
         umma_commit(&bars[kSFull0 + (t & 1)]);
-        return true;
+        umma_commit(&bars[kRopeEmpty0 + (t & 1)]);
+      };
+      // O[:, 256r:+256] (+)= P(t) . c(t)[:, 256r:+256]  (4 MMAs, A = P from TMEM)
+      auto issue_pv = [&](uint32_t t, bool first) {
+        tc_fence_after();
+        const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VSTAGE, VF_BYTES, 1024);
+        const uint32_t pa = tmem + TM_P + 32 * (t & 1);
+#pragma unroll
+        for (int kk = 0; kk < BS / 16; ++kk)
+          umma_ts(tmem + TM_O, pa + 8 * kk, vb0 + uint64_t((kk * 2048) >> 4), id_o,
+                  (!first || kk > 0) ? 1u : 0u);
+        umma_commit(&bars[kKVEmpty0 + (t % NSTAGE)]);
+        umma_commit(&bars[kPVDone0 + (t & 1)]);
       };
       while (ok && w.next(sg)) {
-        const uint32_t n = uint32_t(sg.j1 - sg.j0);
+        const uint32_t end = it + uint32_t(sg.j1 - sg.j0);
         if (!mbar_wait(&bars[kQFull], seg & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t it0 = it;
-        if (!issue_s(it0)) { ok = false; break; }
-        if (n > 1 && !issue_s(it0 + 1)) { ok = false; break; }
-        if (n <= 2) umma_commit(&bars[kQEmpty]);  // every score MMA of this segment is issued
-        for (uint32_t k = 0; k < n && ok; ++k) {
-          const uint32_t t = it0 + k;
-          if (k == 0 && seg > 0 && !mbar_wait(&bars[kOFree], (seg - 1) & 1)) { ok = false; break; }
-          if (!mbar_wait(&bars[kPFull0 + (t & 1)], (t >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          const int s = t % NSTAGE;
-          const uint32_t pa = tmem + TM_S + BS * (t & 1);
-#pragma unroll
-          for (int kk = 0; kk < BS / 16; ++kk) {
-            const uint64_t b = sdesc_sw128(kv_base + s * STAGE_BYTES + kk * 2048, KF_BYTES, 1024);
-            umma_ts(tmem + TM_O, pa + 8 * kk, b, id_o, (k > 0 || kk > 0) ? 1u : 0u);
+        uint32_t ns = it, np = it, idle = 0;
+        // S(ns) needs its rows and a free S slot; P.V(np) needs P(np) (and, for
+        // the first tile of a later sequence, the previous epilogue to be done
+        // with O).  Issue whichever is ready.
+        while (np < end) {
+          bool prog = false;
+          if (ns < end &&
+              (ns < 2 || mbar_test(&bars[kSRead0 + (ns & 1)], ((ns - 2) >> 1) & 1)) &&
+              mbar_test(&bars[kKVFull0 + ns % NSTAGE], (ns / NSTAGE) & 1)) {
+            issue_s(ns);
+            ++ns;
+            if (ns == end) umma_commit(&bars[kQEmpty]);  // every score MMA of this sequence is issued
+            prog = true;
           }
-          umma_commit(&bars[kKVEmpty0 + s]);
-          umma_commit(&bars[kPVDone0 + (t & 1)]);
-          // S(t+2) reuses P(t)'s slot; MMAs run in issue order, so it lands after
-          // P.V(t) has read P(t)
-          if (k + 2 < n) {
-            if (!issue_s(t + 2)) { ok = false; break; }
-            if (k + 3 == n) umma_commit(&bars[kQEmpty]);
+          if (np < ns && mbar_test(&bars[kPFull0 + (np & 1)], (np >> 1) & 1) &&
+              (np != it || seg == 0 || mbar_test(&bars[kOFree], (seg - 1) & 1))) {
+            issue_pv(np, np == it);
+            ++np;
+            prog = true;
+          }
+          if (prog) {
+            idle = 0;
+          } else if (++idle > KV_MAX_SPIN || ((idle & 1023) == 0 && *abort_flag)) {
+            ok = false;
+            break;
           }
         }
-        it += n;
+        it = end;
         ++seg;
         if (*abort_flag) ok = false;
       }
@@ -287,18 +316,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         *abort_flag = 1;
       }
     }
-  } else {
-    // ------------------------------------- softmax / exchange / epilogue warps
+  } else if (warp >= SEND0 / 32) {
+    // ---------------------------------------------------------------- senders
     const int r = 32 * (warp & 3) + lane;          // head row = TMEM lane
-    const int hh = (warp - 2) >> 2;                // which 32 tokens (and 128 O columns)
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-    const int tid = threadIdx.x - 64;              // 0..255
-    uint8_t* xbuf = smem + OFF_X;
+    const int stid = threadIdx.x - SEND0;          // 0..127
     uint8_t* xstage = smem + OFF_XS;
+    const uint32_t xbuf_peer = map_peer(smem_u32(smem + OFF_X), peer);
+    const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull0]), peer);
+    auto wait_all = [](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
+    };
+    auto wait_all_cluster = [](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity) ? 1 : 0) != 0;
+    };
+    Walker w{p.cum, 1, st, en};
+    Seg sg;
+    uint32_t u = 0;
+    bool ok = true;
+    while (ok && w.next(sg)) {
+      for (int k = sg.j0; k < sg.j1; ++k, ++u) {
+        const uint32_t slot = u & 1;
+        bool good = wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
+        uint32_t hx[32];
+        if (good) {
+          tc_fence_after();
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + lane_off + TM_S + BS * slot, v0);
+          tmem_ld32(tmem + lane_off + TM_S + BS * slot + 32, v1);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            hx[j] = partial_pair(v0[2 * j], v0[2 * j + 1], p.scale_log2);
+            hx[16 + j] = partial_pair(v1[2 * j], v1[2 * j + 1], p.scale_log2);
+          }
+        }
+        // staging is free once the peer has received the previous partial; the
+        // peer's receive slot once it has read the partial sent two tiles ago
+        good = good && (u == 0 || wait_all_cluster(&bars[kXSent], (u - 1) & 1));
+        good = good && (u < 2 || wait_all_cluster(&bars[kXEmpty0 + slot], ((u - 2) >> 1) & 1));
+        if (good) {
+          uint4* srow = reinterpret_cast<uint4*>(xstage + r * XROW);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            srow[c ^ (r & 7)] = make_uint4(hx[4 * c], hx[4 * c + 1], hx[4 * c + 2], hx[4 * c + 3]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        // the abort flag is read by every thread but decided for the group
+        if (!named_bar_and(4, NSEND, good && *abort_flag == 0)) { ok = false; break; }
+        if (stid == 0)
+          bulk_copy_to_peer(xbuf_peer + slot * XBYTES, xstage, XBYTES, xfull_peer + 8 * slot);
+      }
+    }
+    if (!ok) {
+      report(p.err, KVATTN_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // Drain: the peer's last arrivals on this CTA's barriers (received / read)
+    if (u > 0) {
+      mbar_wait_cluster(&bars[kXSent], (u - 1) & 1);
+      mbar_wait_cluster(&bars[kXEmpty0 + ((u - 1) & 1)], ((u - 1) >> 1) & 1);
+      if (u > 1) mbar_wait_cluster(&bars[kXEmpty0 + (u & 1)], ((u - 2) >> 1) & 1);
+    }
+  } else {
+    // ------------------------------------------ softmax / epilogue warps (2..9)
+    const int r = 32 * (warp & 3) + lane;          // head row = TMEM lane
+    const int hh = (warp - 2) >> 2;                // which 32 rows of the tile (and 128 O columns)
+    const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+    const int tid = threadIdx.x - SW0;             // 0..255
+    const uint8_t* xbuf = smem + OFF_X;
     float* mx_s = reinterpret_cast<float*>(smem + OFF_MX);   // [2][128]
-    const uint32_t xbuf_peer = map_peer(smem_u32(xbuf), peer);
-    const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull]), peer);
-    const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty]), peer);
+    const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty0]), peer);
+    const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent]), peer);
     Walker w{p.cum, 1, st, en};
     Seg sg;
     uint32_t it = 0;
@@ -311,69 +403,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     auto wait_all_cluster = [](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity) ? 1 : 0) != 0;
     };
-    // This thread's 32 partial scores of tile t, in log2 units, as f16 pairs.
-    auto own_partial = [&](uint32_t t, uint32_t (&h)[16]) {
-      uint32_t v[32];
-      tmem_ld32(tmem + lane_off + TM_S + BS * (t & 1) + 32 * hh, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        h[j] = pack_f16(__uint_as_float(v[2 * j]) * p.scale_log2,
-                        __uint_as_float(v[2 * j + 1]) * p.scale_log2);
-    };
-    // Push this rank's partial of tile t to the peer: stage it locally (row r,
-    // 16-byte chunks XOR-swizzled by r), then one bulk copy after the peer has
-    // released the previous tile (which also means the previous copy has
-    // finished reading the staging buffer).  `good` is the caller's state; the
-    // result is uniform over the group (the named barrier ANDs it).
-    auto send = [&](uint32_t t, bool good, uint32_t (&h)[16]) -> bool {
-      good = good && wait_all(&bars[kSFull0 + (t & 1)], (t >> 1) & 1);
-      if (good) {
-        tc_fence_after();
-        own_partial(t, h);
-        good = wait_all_cluster(&bars[kXEmpty], (t & 1) ^ 1);
-        if (good) {
-          uint4* srow = reinterpret_cast<uint4*>(xstage + r * XROW);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            srow[(4 * hh + c) ^ (r & 7)] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
-      }
-      good = named_bar_and(2, NSW, good);
-      if (good && tid == 0) bulk_copy_to_peer(xbuf_peer, xstage, XBYTES, xfull_peer);
-      return good;
-    };
-
-    uint32_t hcur[16], hnext[16];
     while (ok && w.next(sg)) {
       const int len = max(0, min(p.seq_lens[sg.b], sg.n * BS));
       const uint32_t n = uint32_t(sg.j1 - sg.j0);
       float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
-      if (!send(it, true, hcur)) { ok = false; break; }
-      for (uint32_t k = 0; k < n && ok; ++k) {
+      bool good = true;
+      for (uint32_t k = 0; k < n; ++k) {
         const uint32_t t = it + k;
-        const int slot = t & 1;
-        // A failed (bounded) wait below does not leave the loop at once: the
-        // warp skips its work and the group agrees to stop at the next barrier.
-        bool good = wait_all_cluster(&bars[kXFull], t & 1);
+        const uint32_t slot = t & 1;
+        good = good && wait_all_cluster(&bars[kXFull0 + slot], (t >> 1) & 1);
+        if (good && tid == 0) {
+          // the bulk copy has landed, so it has read the peer's staging buffer
+          mbar_arrive_remote_relaxed(xsent_peer);
+          mbar_arrive_expect_tx(&bars[kXFull0 + slot], XBYTES);    // arm for tile t + 2
+        }
+        good = good && wait_all(&bars[kSFull0 + slot], (t >> 1) & 1);
         float sc[32];
         float mx = -INFINITY;
-        const int valid = len - (sg.j0 + int(k)) * BS - 32 * hh;
         if (good) {
-          if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull], XBYTES);  // next tile's bytes
-          const uint4* xr = reinterpret_cast<const uint4*>(xbuf + r * XROW);
+          tc_fence_after();
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + TM_S + BS * slot + 32 * hh, v);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
+          const int valid = len - (sg.j0 + int(k)) * BS - 32 * hh;
+          const uint4* xr = reinterpret_cast<const uint4*>(xbuf + slot * XBYTES + r * XROW);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 v = xr[(4 * hh + c) ^ (r & 7)];
-            const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+            const uint4 pv4 = xr[(4 * hh + c) ^ (r & 7)];
+            const uint32_t pw[4] = {pv4.x, pv4.y, pv4.z, pv4.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              // both ranks add the same two f16 partials: bit-identical scores
-              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&hcur[4 * c + q]));
-              const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&pv[q]));
-              sc[8 * c + 2 * q] = a.x + b.x;
-              sc[8 * c + 2 * q + 1] = a.y + b.y;
+              const int j = 8 * c + 2 * q;
+              const uint32_t own = partial_pair(v[j], v[j + 1], p.scale_log2);
+              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&own));
+              const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&pw[q]));
+              sc[j] = a.x + b.x;
+              sc[j + 1] = a.y + b.y;
             }
           }
 #pragma unroll
@@ -381,84 +449,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             sc[j] = j < valid ? sc[j] : -INFINITY;
             mx = fmaxf(mx, sc[j]);
           }
+        }
+        // One barrier per tile in the common case: every thread has read the
+        // receive slot, and no row's max has outgrown its reference by the
+        // threshold.  Otherwise the two halves of each row exchange maxima.
+        const bool slow = named_bar_or(3, NSW, !good || mx > m_ref + RESCALE_THRESHOLD);
+        if (slow) {
           mx_s[hh * 128 + r] = mx;
-        }
-        // the row max over both halves of the tile
-        good = named_bar_and(3, NSW, good);
-        // Every thread has read the peer's partial (before the barrier): release
-        // the exchange buffer.  One thread that has issued no bulk copy does it,
-        // so its cluster-scope release does not wait for an outgoing copy.
-        if (good && tid == 32) mbar_arrive_remote(xempty_peer);
-        if (good) {
+          good = named_bar_and(3, NSW, good);
+          if (!good) break;
           mx = fmaxf(mx, mx_s[(hh ^ 1) * 128 + r]);
-          if (k == 0) {
-            m_ref = mx;
-          } else if (__any_sync(0xffffffffu, mx > m_ref + RESCALE_THRESHOLD)) {
-            // Some row's running max grew a lot: rescale this thread's half of
-            // O (after the previous P.V landed) and l.  Both warps of a row pair
-            // see the same maxima, so they take this branch together; TMEM
-            // accesses are warp-collective, rows that keep their max scale by 1.
-            good = wait_all(&bars[kPVDone0 + ((t - 1) & 1)], ((t - 1) >> 1) & 1);
-            if (good) {
-              tc_fence_after();
-              const float m_new = mx > m_ref + RESCALE_THRESHOLD ? mx : m_ref;
-              const float alpha = exp2_approx(m_ref - m_new);
-              m_ref = m_new;
-              l *= alpha;
+          const bool grow = mx > m_ref + RESCALE_THRESHOLD;
+          if (__any_sync(0xffffffffu, grow)) {
+            // Both warps of a row pair see the same maxima, so they take this
+            // branch together; rows that keep their reference scale by 1.
+            const float m_new = grow ? mx : m_ref;
+            const float alpha = grow ? exp2_approx(m_ref - m_new) : 1.f;
+            if (k > 0) {
+              // O holds earlier tiles: rescale this thread's half after the
+              // previous P.V has landed
+              good = wait_all(&bars[kPVDone0 + ((t - 1) & 1)], ((t - 1) >> 1) & 1);
+              if (good) {
+                tc_fence_after();
 #pragma unroll 1
-              for (int cb = 0; cb < 128; cb += 32) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + TM_O + 128 * hh + cb, o);
-                tmem_ld_wait();
+                for (int cb = 0; cb < 128; cb += 32) {
+                  uint32_t o[32];
+                  tmem_ld32(tmem + lane_off + TM_O + 128 * hh + cb, o);
+                  tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                tmem_st32(tmem + lane_off + TM_O + 128 * hh + cb, o);
+                  for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                  tmem_st32(tmem + lane_off + TM_O + 128 * hh + cb, o);
+                }
+                tmem_st_wait();
               }
-              tmem_st_wait();
             }
-          }
-          if (good) {
-            uint32_t pk[16];
-            float lsum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float p0 = exp2_approx(sc[2 * j] - m_ref), p1 = exp2_approx(sc[2 * j + 1] - m_ref);
-              lsum += p0 + p1;
-              pk[j] = pack_bf16(p0, p1);
-            }
-            l += lsum;
-            tmem_st16(tmem + lane_off + TM_S + BS * slot + 16 * hh, pk);
-            tmem_st_wait();
-            const int vt = len - (sg.j0 + int(k)) * BS;   // valid rows of the whole tile
-            if (vt < BS) {
-              // Zero the latent rows past the end of the sequence in the four
-              // boxes the P.V product reads: P is 0 there, but 0 * NaN is NaN.
-              uint8_t* stg = smem + OFF_KV + (t % NSTAGE) * STAGE_BYTES;
-              const int v0 = max(vt, 0);
-              for (int idx = tid; idx < (BS - v0) * 4 * 8; idx += NSW) {
-                const int row = v0 + idx / 32, rem = idx % 32;
-                *reinterpret_cast<uint4*>(stg + (rem >> 3) * KF_BYTES + row * 128 + (rem & 7) * 16) =
-                    make_uint4(0, 0, 0, 0);
-              }
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-            tc_fence_before();
-            mbar_arrive(&bars[kPFull0 + slot]);
+            l = k > 0 ? l * alpha : 0.f;
+            m_ref = m_new;
           }
         }
-        if (k + 1 < n) {
-          ok = send(t + 1, good, hnext);
+        // receive slot read: every thread's loads from it returned before the barrier
+        if (good && tid == 32) mbar_arrive_remote_relaxed(xempty_peer + 8 * slot);
+        // P slot t % 2 was last read by P.V(t - 2)
+        good = good && (t < 2 || wait_all(&bars[kPVDone0 + slot], ((t - 2) >> 1) & 1));
+        if (good) {
+          tc_fence_after();
+          uint32_t pk[16];
+          float lsum = 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) hcur[j] = hnext[j];
-        } else {
-          ok = named_bar_and(2, NSW, good);
+          for (int j = 0; j < 16; ++j) {
+            const float p0 = exp2_approx(sc[2 * j] - m_ref), p1 = exp2_approx(sc[2 * j + 1] - m_ref);
+            lsum += p0 + p1;
+            pk[j] = pack_bf16(p0, p1);
+          }
+          l += lsum;
+          tmem_st16(tmem + lane_off + TM_P + 32 * slot + 16 * hh, pk);
+          tmem_st_wait();
+          const int vt = len - (sg.j0 + int(k)) * BS;   // valid rows of the whole tile
+          if (vt < BS) {
+            // Zero the latent rows past the end of the sequence in the value
+            // boxes that P.V reads: P is 0 there, but 0 * NaN is NaN.
+            uint8_t* stg = smem + OFF_V + (t % NSTAGE) * VSTAGE;
+            const int v0 = max(vt, 0);
+            for (int idx = tid; idx < (BS - v0) * 4 * 8; idx += NSW) {
+              const int row = v0 + idx / 32, rem = idx % 32;
+              *reinterpret_cast<uint4*>(stg + (rem >> 3) * VF_BYTES + row * 128 + (rem & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          tc_fence_before();
+          mbar_arrive(&bars[kPFull0 + slot]);
         }
       }
-      if (!ok) break;
       // ---- epilogue: O / l for this segment's rows (each thread: 128 columns)
       const uint32_t last = it + n - 1;
       // group-uniform, like every failure decision of this group
-      if (!named_bar_and(2, NSW, wait_all(&bars[kPVDone0 + (last & 1)], (last >> 1) & 1))) {
+      if (!named_bar_and(2, NSW, good && wait_all(&bars[kPVDone0 + (last & 1)], (last >> 1) & 1))) {
         ok = false;
         break;
       }
@@ -503,9 +569,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       report(p.err, KVATTN_DEVERR_TIMEOUT);
       *abort_flag = 1;
     }
-    // Drain: the peer's last "done reading" arrival targets this CTA's barrier;
-    // wait for it so this CTA's shared memory outlives every remote access.
-    if (it > 0) mbar_wait_cluster(&bars[kXEmpty], (it - 1) & 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -513,6 +576,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  // Neither CTA leaves while the other may still address its shared memory.
+  cluster_sync_all();
 }
 
 // ---------------------------------------------------------------- host side
