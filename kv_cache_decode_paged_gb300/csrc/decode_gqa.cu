@@ -559,6 +559,7 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   pa.block_size = cc->block_size;
   pa.max_blocks = a.max_blocks;
   pa.G = G;
+  pa.whole_unit_slack = -1;
   pa.cum = reinterpret_cast<int64_t*>(ws + L.cum);
   pa.cta_start = reinterpret_cast<int4*>(ws + L.cta);
   pa.split_first = reinterpret_cast<int32_t*>(ws + L.split_first);

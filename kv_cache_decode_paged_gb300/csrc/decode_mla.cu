@@ -28,13 +28,16 @@
 // with A in tensor memory ~123 cycles for N <= 128 and ~136 at N = 256.  A
 // distributed-shared-memory push has ~1000 cycles of latency.  The kernel is
 // therefore organised so that the exchange of tile t+1 overlaps the softmax of
-// tile t:
-//   warp 0      TMA producer: Q per sequence; per tile 4 value boxes (3-stage
-//               ring) and one rope box (2-slot ring, freed once S is computed)
-//   warp 1      MMA issuer and TMEM owner: S(t) into one of two S slots, P.V(t)
-//               from one of two P slots, issued in whichever order their inputs
-//               become ready
-//   warps 10-13 senders: S(t) partial -> f16 -> staging -> bulk copy to the peer
+// tile t, and so that four value stages fit: the first 128 c_KV dims of this
+// rank's Q sit in TMEM (score K steps 0..7 read A from TMEM), the other 128
+// and the 32 rope dims in shared memory.
+//   warp 0      TMA producer: per sequence the shared-memory part of Q; per
+//               tile 4 value boxes (4-stage ring) and one rope box (2-slot
+//               ring, freed once S is computed)
+//   warp 1      TMEM owner and S issuer: S(t) into one of two S slots
+//   warp 14     P.V issuer: P.V(t) with P from one of two P slots
+//   warps 10-13 senders: per sequence Q[:, 256r : 256r + 128] into TMEM; per
+//               tile S(t) partial -> f16 -> staging -> bulk copy to the peer
 //               (one thread per head row)
 //   warps 2-9   softmax: peer partial + own partial, online softmax with lazy
 //               rescaling, P(t) -> TMEM, epilogue (two threads per head row,
@@ -43,6 +46,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -59,11 +63,15 @@ constexpr int QF_BYTES = 128 * 128;    // Q box [128 heads x 64 dims], 128-byte 
 constexpr int QH_BYTES = 128 * 64;     // Q box [128 heads x 32 rope dims], 64-byte swizzle
 constexpr int VF_BYTES = BS * 128;     // latent box [64 rows x 64 dims]
 constexpr int RH_BYTES = BS * 64;      // latent box [64 rows x 32 rope dims]
-constexpr int OFF_QF = 0;
-constexpr int OFF_QH = 4 * QF_BYTES;
-constexpr int Q_BYTES = 4 * QF_BYTES + QH_BYTES;          // 72 KB
-constexpr int NSTAGE = 3;                                 // value ring
+constexpr int OFF_QF = 0;                                 // Q dims 256r+128 .. 256r+255
+constexpr int OFF_QH = 2 * QF_BYTES;                      // Q rope dims
+constexpr int Q_BYTES = 2 * QF_BYTES + QH_BYTES;          // 40 KB
+constexpr int NSTAGE = 4;                                 // value ring
 constexpr int VSTAGE = 4 * VF_BYTES;                      // 32 KB
+// The value ring is laid out box-major: box i (dims 64i .. 64i+63 of this
+// rank) of stage s sits at OFF_V + i * VBOX + s * VF_BYTES, so that the rows
+// of two consecutive stages form one 128-row operand.
+constexpr int VBOX = NSTAGE * VF_BYTES;
 constexpr int OFF_V = Q_BYTES;
 constexpr int NROPE = 2;                                  // rope ring
 constexpr int OFF_R = OFF_V + NSTAGE * VSTAGE;
@@ -73,16 +81,18 @@ constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // 2 receive slots (pe
 constexpr int OFF_XS = OFF_X + 2 * XBYTES;                // send staging
 constexpr int OFF_MX = OFF_XS + XBYTES;                   // row max / row sum exchange
 constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
-constexpr int NBARS = 26;
+constexpr int NBARS = 32;
 constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
 constexpr int NSW = 256;               // softmax warps: two threads per head row
 constexpr int NSEND = 128;             // sender warps: one thread per head row
 constexpr int SW0 = 64, SEND0 = 64 + NSW;
-constexpr int THREADS = 64 + NSW + NSEND;
+constexpr int PV_WARP = (SEND0 + NSEND) / 32;   // the P.V issuer
+constexpr int THREADS = 64 + NSW + NSEND + 32;
 constexpr int KSTEPS = 18;             // 288 score dims per rank / 16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;           // two S slots of 64 columns
 constexpr uint32_t TM_P = 128;         // two P slots of 32 columns (bf16 pairs)
+constexpr uint32_t TM_Q = 192;         // Q dims 256r .. 256r+127 (bf16 pairs)
 constexpr uint32_t TM_O = 256;         // O half: columns 256..511
 constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the max grows by 2^8
 static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
@@ -92,6 +102,7 @@ static_assert(SMEM <= 232448, "shared memory");
 }  // namespace mla
 
 struct MlaParams {
+  const uint16_t* q;       // absorbed queries, [B][h][576] bf16
   const int32_t* bt;
   const int32_t* seq_lens;
   const int64_t* cum;
@@ -116,11 +127,15 @@ enum : int {
   kXFull0 = 11,     // 2: the peer's partial of tile t is in receive slot t % 2 (tx bytes)
   kXEmpty0 = 13,    // 2: the peer has read this rank's partial from its receive slot t % 2
   kXSent = 15,      // the peer has received this rank's last partial: staging is free
-  kKVFull0 = 16,    // 3: value boxes (and the rope box) of the tile landed
-  kKVEmpty0 = 19,   // 3: P.V finished with the value stage
-  kRopeEmpty0 = 22, // 2: S finished with the rope slot
-  kAbort = 24
+  kQTmem = 16,      // the sender warps have written this sequence's Q columns to TMEM
+  kMmaDrain = 17,   // 2: each MMA issuer's last operations completed (exit path)
+  kKVFull0 = 19,                          // NSTAGE: value boxes (and rope box) landed
+  kKVEmpty0 = kKVFull0 + mla::NSTAGE,     // NSTAGE: P.V finished with the value stage
+  kRopeEmpty0 = kKVEmpty0 + mla::NSTAGE,  // 2: S finished with the rope slot
+  kAbort = kRopeEmpty0 + 2,               // an int flag in this slot
+  kNumBars = kAbort + 1
 };
+static_assert(kNumBars <= mla::NBARS, "barrier slots");
 
 // One f16 pair of scaled partial scores: senders and softmax warps round the
 // same fp32 values the same way.
@@ -161,6 +176,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       mbar_init(&bars[kRopeEmpty0 + i], 1);
     }
     mbar_init(&bars[kXSent], 1);           // one arrival from the peer's softmax warps
+    mbar_init(&bars[kQTmem], NSEND / 32);
+    mbar_init(&bars[kMmaDrain], 1);
+    mbar_init(&bars[kMmaDrain + 1], 1);
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&bars[kKVFull0 + i], 1);
       mbar_init(&bars[kKVEmpty0 + i], 1);
@@ -198,8 +216,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       while (ok && w.next(sg)) {
         if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
-        for (int i = 0; i < 4; ++i)
-          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 64 * i, 0, sg.b,
+        for (int i = 0; i < 2; ++i)
+          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 128 + 64 * i, 0, sg.b,
                              &bars[kQFull]);
         tma_load_3d_nohint(smem + OFF_QH, &tmQH, rx, 0, sg.b, &bars[kQFull]);
         const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
@@ -216,10 +234,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             report(p.err, KVATTN_DEVERR_BLOCK_ID);
           else
             page = blk;
-          uint8_t* stg = smem + OFF_V + s * VSTAGE;
+          uint8_t* stg = smem + OFF_V + s * VF_BYTES;
           mbar_arrive_expect_tx(&bars[kKVFull0 + s], uint32_t(VSTAGE + RH_BYTES));
           for (int i = 0; i < 4; ++i)
-            tma_load_3d(stg + i * VF_BYTES, &tmLF, vx0 + 64 * i, 0, page, &bars[kKVFull0 + s], pol);
+            tma_load_3d(stg + i * VBOX, &tmLF, vx0 + 64 * i, 0, page, &bars[kKVFull0 + s], pol);
           tma_load_3d(smem + OFF_R + q * RH_BYTES, &tmLH, rx, 0, page, &bars[kKVFull0 + s], pol);
           if (*abort_flag) ok = false;
         }
@@ -229,115 +247,164 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         report(p.err, KVATTN_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
+      // Every load this thread issued lands before the CTA can exit (on the
+      // normal path the consumers have waited for all of them already).
+      if (seg > 0) mbar_wait(&bars[kQFull], (seg - 1) & 1);
+      for (uint32_t k = it > uint32_t(NSTAGE) ? it - NSTAGE : 0; k < it; ++k)
+        mbar_wait(&bars[kKVFull0 + k % NSTAGE], (k / NSTAGE) & 1);
     }
-  } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == PV_WARP) {
+    // ------------------------------------------ MMA issuers: S (warp 1), P.V
+    // Two threads feed the tensor core: one tcgen05.mma takes about as long to
+    // issue as to run at these shapes, so a single issuer would set the pace.
+    // Their operands and accumulators are disjoint (S slots vs P slots and O).
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16(128, BS, false);
-      const uint32_t id_o = idesc_bf16(128, 256, true);
-      const uint32_t qf = smem_u32(smem + OFF_QF), qh = smem_u32(smem + OFF_QH);
       const uint32_t v_base = smem_u32(smem + OFF_V), r_base = smem_u32(smem + OFF_R);
       Walker w{p.cum, 1, st, en};
       Seg sg;
       uint32_t it = 0, seg = 0;
       bool ok = true;
-      // Descriptors are built once; a K step only moves the start address, whose
-      // field is the low bits of the descriptor (address / 16, no carry below
-      // 256 KB).  The issue loop is unrolled so that one thread can feed the
-      // tensor core back to back: with the address arithmetic in the loop the
-      // issue, not the tensor core, set the pace.
-      const uint64_t qa0 = sdesc_sw128(qf, 16, 1024), qh0 = sdesc_sw64(qh, 512);
-      // S(t) = Q[:, D_r] . row(t)[:, D_r]^T into S slot t % 2 (18 MMAs, K = 16 each)
-      auto issue_s = [&](uint32_t t) {
-        tc_fence_after();
-        const uint32_t d = tmem + TM_S + BS * (t & 1);
-        const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VSTAGE, 16, 1024);
-        const uint64_t rb0 = sdesc_sw64(r_base + (t & 1) * RH_BYTES, 512);
+      if (warp == 1) {
+        const uint32_t id_s = idesc_bf16(128, BS, false);
+        const uint32_t qf = smem_u32(smem + OFF_QF), qh = smem_u32(smem + OFF_QH);
+        // Descriptors are built once; a K step only moves the start address,
+        // whose field is the low bits of the descriptor (address / 16, no carry
+        // below 256 KB).  The issue loop is unrolled: with the address
+        // arithmetic in the loop the issue, not the tensor core, set the pace.
+        const uint64_t qa0 = sdesc_sw128(qf, 16, 1024), qh0 = sdesc_sw64(qh, 512);
+        // S(t) = Q[:, D_r] . row(t)[:, D_r]^T into S slot t % 2, K steps [J0, J1)
+        // of 18 (K = 16 each).  Steps 0 and 1 are the rope dims, so that the
+        // small rope ring can be refilled as soon as they are done; steps 2..9
+        // take Q from TMEM, 10..17 from shared memory.
+        auto issue_s = [&](uint32_t t, auto j0c, auto j1c) {
+          constexpr int J0 = decltype(j0c)::value, J1 = decltype(j1c)::value;
+          const uint32_t d = tmem + TM_S + BS * (t & 1);
+          const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VF_BYTES, 16, 1024);
+          const uint64_t rb0 = sdesc_sw64(r_base + (t & 1) * RH_BYTES, 512);
 #pragma unroll
-        for (int j = 0; j < KSTEPS; ++j) {
-          if (j < 16)
-            umma_ss(d, qa0 + uint64_t(((j >> 2) * QF_BYTES + (j & 3) * 32) >> 4),
-                    vb0 + uint64_t(((j >> 2) * VF_BYTES + (j & 3) * 32) >> 4), id_s, j > 0);
-          else
-            umma_ss(d, qh0 + uint64_t(((j - 16) * 32) >> 4), rb0 + uint64_t(((j - 16) * 32) >> 4),
-                    id_s, 1u);
-        }
-        umma_commit(&bars[kSFull0 + (t & 1)]);
-        umma_commit(&bars[kRopeEmpty0 + (t & 1)]);
-      };
-      // O[:, 256r:+256] (+)= P(t) . c(t)[:, 256r:+256]  (4 MMAs, A = P from TMEM)
-      auto issue_pv = [&](uint32_t t, bool first) {
-        tc_fence_after();
-        const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VSTAGE, VF_BYTES, 1024);
-        const uint32_t pa = tmem + TM_P + 32 * (t & 1);
-#pragma unroll
-        for (int kk = 0; kk < BS / 16; ++kk)
-          umma_ts(tmem + TM_O, pa + 8 * kk, vb0 + uint64_t((kk * 2048) >> 4), id_o,
-                  (!first || kk > 0) ? 1u : 0u);
-        umma_commit(&bars[kKVEmpty0 + (t % NSTAGE)]);
-        umma_commit(&bars[kPVDone0 + (t & 1)]);
-      };
-      while (ok && w.next(sg)) {
-        const uint32_t end = it + uint32_t(sg.j1 - sg.j0);
-        if (!mbar_wait(&bars[kQFull], seg & 1)) { ok = false; break; }
-        uint32_t ns = it, np = it, idle = 0;
-        // S(ns) needs its rows and a free S slot; P.V(np) needs P(np) (and, for
-        // the first tile of a later sequence, the previous epilogue to be done
-        // with O).  Issue whichever is ready.
-        while (np < end) {
-          bool prog = false;
-          if (ns < end &&
-              (ns < 2 || mbar_test(&bars[kSRead0 + (ns & 1)], ((ns - 2) >> 1) & 1)) &&
-              mbar_test(&bars[kKVFull0 + ns % NSTAGE], (ns / NSTAGE) & 1)) {
-            issue_s(ns);
-            ++ns;
-            if (ns == end) umma_commit(&bars[kQEmpty]);  // every score MMA of this sequence is issued
-            prog = true;
+          for (int j = J0; j < J1; ++j) {
+            if (j < 2) {        // rope dims of this rank
+              umma_ss(d, qh0 + uint64_t((j * 32) >> 4), rb0 + uint64_t((j * 32) >> 4), id_s, j > 0);
+            } else {
+              const int m = j - 2;  // c_KV dims 16m .. 16m+15 of this rank
+              const uint64_t b = vb0 + uint64_t(((m >> 2) * VBOX + (m & 3) * 32) >> 4);
+              if (m < 8)
+                umma_ts(d, tmem + TM_Q + 8 * m, b, id_s, 1u);
+              else
+                umma_ss(d, qa0 + uint64_t((((m - 8) >> 2) * QF_BYTES + (m & 3) * 32) >> 4), b,
+                        id_s, 1u);
+            }
           }
-          if (np < ns && mbar_test(&bars[kPFull0 + (np & 1)], (np >> 1) & 1) &&
-              (np != it || seg == 0 || mbar_test(&bars[kOFree], (seg - 1) & 1))) {
-            issue_pv(np, np == it);
-            ++np;
-            prog = true;
-          }
-          if (prog) {
-            idle = 0;
-          } else if (++idle > KV_MAX_SPIN || ((idle & 1023) == 0 && *abort_flag)) {
+        };
+        using C0 = std::integral_constant<int, 0>;
+        using C2 = std::integral_constant<int, 2>;
+        using C18 = std::integral_constant<int, KSTEPS>;
+        while (ok && w.next(sg)) {
+          const uint32_t end = it + uint32_t(sg.j1 - sg.j0);
+          if (!mbar_wait(&bars[kQFull], seg & 1) || !mbar_wait(&bars[kQTmem], seg & 1)) {
             ok = false;
             break;
           }
+          for (uint32_t t = it; t < end; ++t) {
+            // the tile's rows, and its S slot: both readers are done with S(t-2)
+            if ((t >= 2 && !mbar_wait(&bars[kSRead0 + (t & 1)], ((t - 2) >> 1) & 1)) ||
+                !mbar_wait(&bars[kKVFull0 + t % NSTAGE], (t / NSTAGE) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, C0{}, C2{});
+            umma_commit(&bars[kRopeEmpty0 + (t & 1)]);
+            issue_s(t, C2{}, C18{});
+            umma_commit(&bars[kSFull0 + (t & 1)]);
+          }
+          if (!ok) break;
+          umma_commit(&bars[kQEmpty]);  // every score MMA of this sequence is issued
+          it = end;
+          ++seg;
+          if (*abort_flag) ok = false;
         }
-        it = end;
-        ++seg;
-        if (*abort_flag) ok = false;
+      } else {
+        const uint32_t id_o = idesc_bf16(128, 256, true);
+        while (ok && w.next(sg)) {
+          const uint32_t end = it + uint32_t(sg.j1 - sg.j0);
+          for (uint32_t t = it; t < end; ++t) {
+            // P(t), and for the first tile of a later sequence the previous
+            // epilogue must be done with O
+            if ((t == it && seg > 0 && !mbar_wait(&bars[kOFree], (seg - 1) & 1)) ||
+                !mbar_wait(&bars[kPFull0 + (t & 1)], (t >> 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // O[:, 256r:+256] (+)= P(t) . c(t)[:, 256r:+256]  (4 MMAs, A = P from TMEM)
+            const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VF_BYTES, VBOX, 1024);
+            const uint32_t pa = tmem + TM_P + 32 * (t & 1);
+#pragma unroll
+            for (int kk = 0; kk < BS / 16; ++kk)
+              umma_ts(tmem + TM_O, pa + 8 * kk, vb0 + uint64_t((kk * 2048) >> 4), id_o,
+                      (t > it || kk > 0) ? 1u : 0u);
+            umma_commit(&bars[kKVEmpty0 + (t % NSTAGE)]);
+            umma_commit(&bars[kPVDone0 + (t & 1)]);
+          }
+          if (!ok) break;
+          it = end;
+          ++seg;
+          if (*abort_flag) ok = false;
+        }
       }
       if (!ok) {
         report(p.err, KVATTN_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
+      // no MMA of this thread may still write TMEM when it is released
+      umma_commit(&bars[kMmaDrain + (warp == 1 ? 0 : 1)]);
+      mbar_wait(&bars[kMmaDrain + (warp == 1 ? 0 : 1)], 0);
     }
-  } else if (warp >= SEND0 / 32) {
+  } else if (warp >= SEND0 / 32) {   // (warps SEND0/32 .. PV_WARP-1)
     // ---------------------------------------------------------------- senders
     const int r = 32 * (warp & 3) + lane;          // head row = TMEM lane
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-    const int stid = threadIdx.x - SEND0;          // 0..127
     uint8_t* xstage = smem + OFF_XS;
     const uint32_t xbuf_peer = map_peer(smem_u32(smem + OFF_X), peer);
     const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull0]), peer);
     auto wait_all = [](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
     };
-    auto wait_all_cluster = [](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity) ? 1 : 0) != 0;
-    };
     Walker w{p.cum, 1, st, en};
     Seg sg;
-    uint32_t u = 0;
+    uint32_t u = 0, seg = 0;
     bool ok = true;
     while (ok && w.next(sg)) {
+      // This sequence's Q[:, 256r : 256r + 128] into TMEM, once the previous
+      // sequence's score MMAs (which read it) have completed.  Rows past h are 0.
+      bool qgood = seg == 0 || wait_all(&bars[kQEmpty], (seg - 1) & 1);
+      if (qgood) {
+        tc_fence_after();
+        const uint4* src =
+            reinterpret_cast<const uint4*>(p.q + (int64_t(sg.b) * p.h + r) * ROWW + 256 * rank);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 x = r < p.h ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
+            qv[4 * i] = x.x;
+            qv[4 * i + 1] = x.y;
+            qv[4 * i + 2] = x.z;
+            qv[4 * i + 3] = x.w;
+          }
+          tmem_st32(tmem + lane_off + TM_Q + 32 * half, qv);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kQTmem]);
+      }
+      ++seg;
       for (int k = sg.j0; k < sg.j1; ++k, ++u) {
         const uint32_t slot = u & 1;
-        bool good = wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
+        bool good = qgood && wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
         uint32_t hx[32];
         if (good) {
           tc_fence_after();
@@ -354,21 +421,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             hx[16 + j] = partial_pair(v1[2 * j], v1[2 * j + 1], p.scale_log2);
           }
         }
-        // staging is free once the peer has received the previous partial; the
-        // peer's receive slot once it has read the partial sent two tiles ago
-        good = good && (u == 0 || wait_all_cluster(&bars[kXSent], (u - 1) & 1));
-        good = good && (u < 2 || wait_all_cluster(&bars[kXEmpty0 + slot], ((u - 2) >> 1) & 1));
-        if (good) {
-          uint4* srow = reinterpret_cast<uint4*>(xstage + r * XROW);
+        // Staging is free once the peer has received the previous partial; the
+        // peer's receive slot once it has read the partial sent two tiles ago.
+        // Both signals only say that reads have finished, so waits at CTA
+        // scope suffice.
+        good = good && (u == 0 || wait_all(&bars[kXSent], (u - 1) & 1));
+        good = good && (u < 2 || wait_all(&bars[kXEmpty0 + slot], ((u - 2) >> 1) & 1));
+        // the abort flag is read by every lane but decided for the warp
+        good = good && !__any_sync(0xffffffffu, *abort_flag != 0);
+        if (!good) { ok = false; break; }
+        // Each warp stages and pushes its own 32 rows (4 KB): no barrier across
+        // the sender warps; the peer's barrier counts the bytes of all four.
+        uint4* srow = reinterpret_cast<uint4*>(xstage + r * XROW);
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            srow[c ^ (r & 7)] = make_uint4(hx[4 * c], hx[4 * c + 1], hx[4 * c + 2], hx[4 * c + 3]);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int c = 0; c < 8; ++c)
+          srow[c ^ (r & 7)] = make_uint4(hx[4 * c], hx[4 * c + 1], hx[4 * c + 2], hx[4 * c + 3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t off = uint32_t(32 * (warp & 3)) * XROW;
+          bulk_copy_to_peer(xbuf_peer + slot * XBYTES + off, xstage + off, 32 * XROW,
+                            xfull_peer + 8 * slot);
         }
-        // the abort flag is read by every thread but decided for the group
-        if (!named_bar_and(4, NSEND, good && *abort_flag == 0)) { ok = false; break; }
-        if (stid == 0)
-          bulk_copy_to_peer(xbuf_peer + slot * XBYTES, xstage, XBYTES, xfull_peer + 8 * slot);
       }
     }
     if (!ok) {
@@ -393,15 +467,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent]), peer);
     Walker w{p.cum, 1, st, en};
     Seg sg;
-    uint32_t it = 0;
+    uint32_t it = 0, received = 0;
     bool ok = true;
     // Every wait result is made warp-uniform: the warp-collective TMEM
     // instructions that follow must be executed by all 32 lanes or none.
     auto wait_all = [](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
-    };
-    auto wait_all_cluster = [](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity) ? 1 : 0) != 0;
     };
     while (ok && w.next(sg)) {
       const int len = max(0, min(p.seq_lens[sg.b], sg.n * BS));
@@ -411,15 +482,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       for (uint32_t k = 0; k < n; ++k) {
         const uint32_t t = it + k;
         const uint32_t slot = t & 1;
-        good = good && wait_all_cluster(&bars[kXFull0 + slot], (t >> 1) & 1);
-        if (good && tid == 0) {
-          // the bulk copy has landed, so it has read the peer's staging buffer
-          mbar_arrive_remote_relaxed(xsent_peer);
-          mbar_arrive_expect_tx(&bars[kXFull0 + slot], XBYTES);    // arm for tile t + 2
-        }
+        // This rank's own partial is ready well before the peer's arrives:
+        // read it first, so that only the addition waits for the exchange.
         good = good && wait_all(&bars[kSFull0 + slot], (t >> 1) & 1);
-        float sc[32];
-        float mx = -INFINITY;
+        uint32_t own[16];
         if (good) {
           tc_fence_after();
           uint32_t v[32];
@@ -428,6 +494,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) own[j] = partial_pair(v[2 * j], v[2 * j + 1], p.scale_log2);
+        }
+        // The peer's bulk copy writes this CTA's shared memory and completes on
+        // this CTA's barrier: observing the phase makes the bytes visible.
+        good = good && wait_all(&bars[kXFull0 + slot], (t >> 1) & 1);
+        received += good ? 1u : 0u;
+        if (good && tid == 0) {
+          // the bulk copy has landed, so it has read the peer's staging buffer
+          mbar_arrive_remote_relaxed(xsent_peer);
+          mbar_arrive_expect_tx(&bars[kXFull0 + slot], XBYTES);    // arm for tile t + 2
+        }
+        float sc[32];
+        float mx = -INFINITY;
+        if (good) {
           const int valid = len - (sg.j0 + int(k)) * BS - 32 * hh;
           const uint4* xr = reinterpret_cast<const uint4*>(xbuf + slot * XBYTES + r * XROW);
 #pragma unroll
@@ -437,8 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int j = 8 * c + 2 * q;
-              const uint32_t own = partial_pair(v[j], v[j + 1], p.scale_log2);
-              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&own));
+              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&own[4 * c + q]));
               const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&pw[q]));
               sc[j] = a.x + b.x;
               sc[j + 1] = a.y + b.y;
@@ -508,11 +588,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           if (vt < BS) {
             // Zero the latent rows past the end of the sequence in the value
             // boxes that P.V reads: P is 0 there, but 0 * NaN is NaN.
-            uint8_t* stg = smem + OFF_V + (t % NSTAGE) * VSTAGE;
+            uint8_t* stg = smem + OFF_V + (t % NSTAGE) * VF_BYTES;
             const int v0 = max(vt, 0);
             for (int idx = tid; idx < (BS - v0) * 4 * 8; idx += NSW) {
               const int row = v0 + idx / 32, rem = idx % 32;
-              *reinterpret_cast<uint4*>(stg + (rem >> 3) * VF_BYTES + row * 128 + (rem & 7) * 16) =
+              *reinterpret_cast<uint4*>(stg + (rem >> 3) * VBOX + row * 128 + (rem & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -568,6 +648,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     if (!ok) {
       report(p.err, KVATTN_DEVERR_TIMEOUT);
       *abort_flag = 1;
+      // The peer may have pushed up to two partials that were not consumed;
+      // they land before this CTA's shared memory goes away.
+      uint32_t total = 0;
+      Walker w2{p.cum, 1, st, en};
+      Seg s2;
+      while (w2.next(s2)) total += uint32_t(s2.j1 - s2.j0);
+      for (uint32_t k = received; k < total && k < received + 2; ++k)
+        mbar_wait_cluster(&bars[kXFull0 + (k & 1)], (k >> 1) & 1);
     }
   }
   tc_fence_before();
@@ -628,6 +716,10 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   pa.block_size = cc->block_size;
   pa.max_blocks = a.max_blocks;
   pa.G = G;
+  // A pair that crosses a sequence boundary drains its pipeline (epilogue,
+  // Q reload: about as long as 7 tiles) and a split sequence costs a combine
+  // pass; below this many extra tiles one pair per sequence is faster.
+  pa.whole_unit_slack = 12;
   pa.cum = reinterpret_cast<int64_t*>(ws + L.cum);
   pa.cta_start = reinterpret_cast<int4*>(ws + L.cta);
   pa.split_first = reinterpret_cast<int32_t*>(ws + L.split_first);
@@ -657,6 +749,7 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
       return KVATTN_ERR_CUDA;
   }
   MlaParams prm;
+  prm.q = static_cast<const uint16_t*>(a.q);
   prm.bt = a.block_table;
   prm.seq_lens = a.seq_lens;
   prm.cum = pa.cum;

@@ -51,6 +51,10 @@ struct PlanArgs {
   int block_size;
   int max_blocks;
   int G;
+  // >= 0: give every unit its own CTA (no split, no combine) when there are at
+  // most G units and the longest is at most this many pages longer than the
+  // balanced share ceil(T / G); < 0: always balance by splitting
+  int whole_unit_slack;
   int64_t* cum;
   int4* cta_start;
   int32_t* split_first;

@@ -20,12 +20,18 @@ namespace kv {
 // and page p belongs to CTA ((p+1)*G' - 1) / T.  The slot of (unit u, CTA c) is u + c,
 // unique because walking the page list increases u or c (or both) at every
 // segment boundary.
+// Whole-unit mode (see PlanArgs::whole_unit_slack): CTA c owns unit c, split
+// counts are 1 (0 for empty units) and no partial slot is used.  It wins when
+// the split would save little: a CTA that crosses a unit boundary drains its
+// pipeline, and every split unit costs a combine pass over its partials.
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
   __shared__ int64_t warp_tot[32];
   __shared__ int64_t carry_s;
+  __shared__ unsigned long long maxn_s;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
   if (tid == 0) {
     carry_s = 0;
+    maxn_s = 0;
     a.cum[0] = 0;
   }
   __syncthreads();
@@ -43,6 +49,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
         report(a.err, KVATTN_DEVERR_SEQ_LEN);
         n = a.max_blocks;
       }
+      atomicMax(&maxn_s, static_cast<unsigned long long>(n));
     }
     int64_t x = n;
 #pragma unroll
@@ -76,6 +83,19 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
   // the last one touching a unit then owns part of that unit, so the unit's
   // partial slots u + c0 .. u + c1 are all written.
   const int64_t G = T < a.G ? T : a.G;
+  const int64_t units = int64_t(a.B) * U;
+  const bool whole = a.whole_unit_slack >= 0 && T > 0 && units <= a.G &&
+                     int64_t(maxn_s) <= (T + G - 1) / G + a.whole_unit_slack;
+  if (whole) {
+    for (int c = tid; c <= a.G; c += blockDim.x)
+      a.cta_start[c] = c < units ? make_int4(int(c / U), int(c % U), 0, 0) : make_int4(a.B, 0, 0, 0);
+    for (int64_t u = tid; u < units; u += blockDim.x) {
+      const int64_t b = u / U;
+      a.split_first[u] = int32_t(2 * u);
+      a.split_count[u] = cum[b + 1] > cum[b] ? 1 : 0;
+    }
+    return;
+  }
   for (int c = tid; c <= a.G; c += blockDim.x) {
     const int64_t p = c <= G ? (int64_t(c) * T) / (G > 0 ? G : 1) : T;
     int4 st = make_int4(a.B, 0, 0, 0);
@@ -94,7 +114,6 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     }
     a.cta_start[c] = st;
   }
-  const int64_t units = int64_t(a.B) * U;
   for (int64_t u = tid; u < units; u += blockDim.x) {
     const int64_t b = u / U, kvh = u % U;
     const int64_t n = cum[b + 1] - cum[b];
