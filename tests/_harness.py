@@ -8,8 +8,8 @@ import kv_cache_decode_paged_gb300 as kv
 from kv_cache_decode_paged_gb300.device import GpuWorkload, dev_bits  # noqa: F401
 from kv_cache_decode_paged_gb300 import inputs
 
-# the benchmark spec tolerances: bf16 caches max |err| <= 2e-2 and relative RMS <= 1e-2;
-# FP8 caches max |err| <= 5e-2.
+# Parity tolerances of the decode outputs: bf16 caches max |err| <= 2e-2 and
+# relative RMS <= 1e-2; FP8 caches max |err| <= 5e-2.
 TOL_ABS_BF16 = 2e-2
 TOL_RELRMS = 1e-2
 TOL_ABS_FP8 = 5e-2
