@@ -57,6 +57,7 @@ struct GqaCfg {
   static constexpr int TILE_BYTES = 16 * ROWB;      // K (or V) of one 16-token chunk
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int NSTAGE = 65536 / STAGE_BYTES;
+  static constexpr int GROUP = NSTAGE / 2 < 16 ? NSTAGE / 2 : 16;  // producer lanes per issue round
   static constexpr int NC = 4;                      // consumer warps
   static constexpr int NSTREAM = NC / MT;
   static constexpr int THREADS = 32 * (NC + 1);
@@ -145,18 +146,23 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
             page = blk * p.hkv + sg.kvh;
         }
         const int cnt = min(32, sg.j1 - jb);
-        for (int x = 0; x < cnt && ok; ++x) {
-          const int pg = __shfl_sync(0xffffffffu, page, x);
-          if (lane == 0) {
-            for (int sub = 0; sub < cpp; ++sub, ++it) {
-              const int s = it % C::NSTAGE;
-              const uint32_t ph = (it / C::NSTAGE) & 1;
-              if (!mbar_wait(&empty[s], ph ^ 1)) {
-                report(p.err, KVATTN_DEVERR_TIMEOUT);
-                *reinterpret_cast<volatile int*>(abort_flag) = 1;
-                ok = false;
-                break;
-              }
+        const int nchunk = cnt * cpp;
+        // Chunks go out C::GROUP at a time, one lane each: a wait on an mbarrier
+        // and a TMA issue cost a few hundred cycles apiece, which one lane
+        // issuing chunk by chunk could not hide (it would set the stream rate).
+        // The chunks of a group use distinct stages, last filled at least one
+        // group earlier, so their waits do not depend on each other.
+        for (int c0 = 0; c0 < nchunk && ok; c0 += C::GROUP) {
+          const int cl = c0 + lane;
+          const int pg = __shfl_sync(0xffffffffu, page, min(cl / cpp, 31));
+          bool lok = true;
+          if (lane < C::GROUP && cl < nchunk) {
+            const uint32_t ic = it + uint32_t(cl);
+            const int s = ic % C::NSTAGE;
+            const int sub = cl % cpp;
+            if (!mbar_wait(&empty[s], ((ic / C::NSTAGE) & 1) ^ 1)) {
+              lok = false;
+            } else {
               mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
               uint8_t* dst = stages + s * C::STAGE_BYTES;
 #pragma unroll
@@ -167,10 +173,15 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
                             sub * 16, pg, &full[s], pol);
               }
             }
-            if (*reinterpret_cast<volatile int*>(abort_flag)) ok = false;
           }
-          ok = __shfl_sync(0xffffffffu, int(ok), 0) != 0;
+          lok = lok && *reinterpret_cast<volatile int*>(abort_flag) == 0;
+          ok = __all_sync(0xffffffffu, lok) != 0;
+          if (!ok && lane == 0) {
+            report(p.err, KVATTN_DEVERR_TIMEOUT);
+            *reinterpret_cast<volatile int*>(abort_flag) = 1;
+          }
         }
+        it += uint32_t(nchunk);
       }
     }
     if (!ok && lane == 0) {
