@@ -135,47 +135,67 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Merge the partial results of every split unit.  grid.x = unit; each thread
-// owns a float4 of one row.  skip_single leaves units with one split alone
-// (the decode kernel already wrote their final rows).
+// Merge the partial results of every split unit:
+//   M = max_w lse_w,  o = sum_w e^(lse_w - M) o_w / sum_w e^(lse_w - M),
+//   lse = M + log sum_w e^(lse_w - M).
+// One warp per (unit, row): the lanes reduce M and the normaliser over the
+// splits together, then each lane streams float4 columns of the partial rows
+// (independent loads across splits).  skip_single leaves units with one split
+// alone (the decode kernel already wrote their final rows).
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
                                                       const float* __restrict__ part_lse,
                                                       const int32_t* __restrict__ first,
                                                       const int32_t* __restrict__ count,
-                                                      int rows, int dv, float* __restrict__ out,
+                                                      int n_units, int rows, int dv,
+                                                      float* __restrict__ out,
                                                       float* __restrict__ lse, int skip_single) {
-  const int u = blockIdx.x;
-  const int cnt = count[u];
-  if (cnt == 1 && skip_single) return;
-  const int f = first[u];
+  const int lane = threadIdx.x & 31;
+  const int64_t n_pairs = int64_t(n_units) * rows;
   const int v4 = dv >> 2;
-  for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < rows * v4;
-       idx += gridDim.y * blockDim.x) {
-    const int r = idx / v4, c = idx - r * v4;
-    float4* o4 = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv) + c;
+  for (int64_t pr = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; pr < n_pairs;
+       pr += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+    const int u = int(pr / rows), r = int(pr % rows);
+    const int cnt = count[u];
+    if (cnt == 1 && skip_single) continue;  // warp-uniform
+    const int f = first[u];
+    const float* lrow = part_lse + size_t(f) * rows + r;  // split w at lrow[w * rows]
     float M = -INFINITY;
-    for (int w = 0; w < cnt; ++w) M = fmaxf(M, part_lse[size_t(f + w) * rows + r]);
+    for (int w = lane; w < cnt; w += 32) M = fmaxf(M, lrow[size_t(w) * rows]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
     if (M == -INFINITY) {
-      *o4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (c == 0) lse[size_t(u) * rows + r] = -INFINITY;
+      for (int c = lane; c < v4; c += 32) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane == 0) lse[size_t(u) * rows + r] = -INFINITY;
       continue;
     }
     float den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < cnt; ++w) {
-      const float lw = part_lse[size_t(f + w) * rows + r];
-      if (lw == -INFINITY) continue;
-      const float e = exp2_approx((lw - M) * kLog2e);
-      den += e;
-      const float4 p = reinterpret_cast<const float4*>(part_out + (size_t(f + w) * rows + r) * dv)[c];
-      acc.x += e * p.x;
-      acc.y += e * p.y;
-      acc.z += e * p.z;
-      acc.w += e * p.w;
+    for (int w = lane; w < cnt; w += 32) {
+      const float lw = lrow[size_t(w) * rows];
+      if (lw != -INFINITY) den += exp2_approx((lw - M) * kLog2e);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
     const float inv = 1.f / den;
-    *o4 = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (c == 0) lse[size_t(u) * rows + r] = M + log2_approx(den) * kLn2;
+    const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
+    const size_t wstride = size_t(rows) * v4;  // float4s between splits
+    for (int c = lane; c < v4; c += 32) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int w = 0; w < cnt; ++w) {
+        const float lw = lrow[size_t(w) * rows];
+        const float e = lw == -INFINITY ? 0.f : exp2_approx((lw - M) * kLog2e);
+        const float4 p = prow[size_t(w) * wstride + c];
+        if (e != 0.f) {  // a split with no valid row holds zeros, never NaN, but skip it
+          acc.x += e * p.x;
+          acc.y += e * p.y;
+          acc.z += e * p.z;
+          acc.w += e * p.w;
+        }
+      }
+      orow[c] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (lane == 0) lse[size_t(u) * rows + r] = M + log2_approx(den) * kLn2;
   }
 }
 
@@ -184,11 +204,12 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
                            float* lse, bool skip_single, cudaStream_t s) {
   if (n_units <= 0) return cudaSuccess;
   const int threads = 256;
-  const int work = rows * (dv / 4);
-  const int gy = (work + threads - 1) / threads;
-  dim3 grid(n_units, gy > 0 ? gy : 1);
-  combine_kernel<<<grid, threads, 0, s>>>(part_out, part_lse, first, count, rows, dv, out, lse,
-                                          skip_single ? 1 : 0);
+  const int64_t warps = int64_t(n_units) * rows;
+  int64_t blocks = (warps + threads / 32 - 1) / (threads / 32);
+  const int cap = device_sm_count() > 0 ? 8 * device_sm_count() : 1184;
+  if (blocks > cap) blocks = cap;
+  combine_kernel<<<int(blocks), threads, 0, s>>>(part_out, part_lse, first, count, n_units, rows,
+                                                 dv, out, lse, skip_single ? 1 : 0);
   return cudaGetLastError();
 }
 
