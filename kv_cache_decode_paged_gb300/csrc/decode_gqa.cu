@@ -71,16 +71,26 @@ struct GqaCfg {
   static_assert(NC % MT == 0, "m-tiles must divide the consumer warps");
 };
 
-// Two E4M3 codes -> f16x2 holding code * 2^-8, exactly: an E4M3 value
-// (-1)^s 2^(e-7) (1 + m/8) has the bit pattern s.eeee.mmm; placed into an f16
-// as s.0eeee.mmm0000000 it reads (-1)^s 2^(e-15) (1 + m/8), and subnormals map
-// to subnormals the same way.  `sel` picks which two bytes of w (a byte_perm
-// selector that puts them in bytes 1 and 3); the 2^8 goes into the scales.
-KV_DEVI uint32_t e4m3x2_to_f16x2_lo8(uint32_t w, uint32_t sel) {
-  const uint32_t y = __byte_perm(w, 0u, sel);
-  return (y & 0x80008000u) | ((y >> 1) & 0x3f803f80u);
+// Rescale O only when a row's running max grows by more than 2^8.
+constexpr float kRescaleLog2 = 8.f;
+
+// Two E4M3 codes -> an f16 pair, exactly (every E4M3 value, subnormals and
+// NaN included, is representable in f16): the hardware conversion of a packed
+// byte pair, low byte to the low half.
+KV_DEVI uint32_t e4m3x2_to_f16x2(uint16_t pair) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
 }
-constexpr uint32_t kSelB01 = 0x1404, kSelB23 = 0x3424, kSelB02 = 0x2404, kSelB13 = 0x3414;
+// codes 0,1 and 2,3 of w
+KV_DEVI uint32_t e4m3_b01(uint32_t w) { return e4m3x2_to_f16x2(uint16_t(w & 0xffffu)); }
+KV_DEVI uint32_t e4m3_b23(uint32_t w) { return e4m3x2_to_f16x2(uint16_t(w >> 16)); }
+// codes 0,2 and 1,3 of w (one byte permutation serves both)
+KV_DEVI void e4m3_b02_b13(uint32_t w, uint32_t& b02, uint32_t& b13) {
+  const uint32_t y = __byte_perm(w, 0u, 0x3120);
+  b02 = e4m3x2_to_f16x2(uint16_t(y & 0xffffu));
+  b13 = e4m3x2_to_f16x2(uint16_t(y >> 16));
+}
 
 // Byte offset of (token r, 16-byte chunk c) inside a 128B-swizzled tile.
 template <int BOX_BYTES>
@@ -285,10 +295,10 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
             const int ch = 2 * cp + (lmat >> 1);
             uint32_t r0, r1, r2, r3;
             ldsm_x4(kb + swz<C::BOX_BYTES>(tok, ch), r0, r1, r2, r3);
-            mma_f16(acc[0], qa[2 * cp], e4m3x2_to_f16x2_lo8(r0, kSelB01), e4m3x2_to_f16x2_lo8(r0, kSelB23));
-            mma_f16(acc[1], qa[2 * cp], e4m3x2_to_f16x2_lo8(r1, kSelB01), e4m3x2_to_f16x2_lo8(r1, kSelB23));
-            mma_f16(acc[0], qa[2 * cp + 1], e4m3x2_to_f16x2_lo8(r2, kSelB01), e4m3x2_to_f16x2_lo8(r2, kSelB23));
-            mma_f16(acc[1], qa[2 * cp + 1], e4m3x2_to_f16x2_lo8(r3, kSelB01), e4m3x2_to_f16x2_lo8(r3, kSelB23));
+            mma_f16(acc[0], qa[2 * cp], e4m3_b01(r0), e4m3_b23(r0));
+            mma_f16(acc[1], qa[2 * cp], e4m3_b01(r1), e4m3_b23(r1));
+            mma_f16(acc[0], qa[2 * cp + 1], e4m3_b01(r2), e4m3_b23(r2));
+            mma_f16(acc[1], qa[2 * cp + 1], e4m3_b01(r3), e4m3_b23(r3));
           }
         }
         float sc[2][4];
@@ -305,27 +315,36 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float c0 = exp2_approx(m0 - mn0), c1 = exp2_approx(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
+        // Lazy rescaling: O and l keep their reference max until a row's
+        // chunk max exceeds it by kRescaleLog2; P then stays below 2^8.  The
+        // first chunk always takes this branch (the reference starts at -inf).
+        const bool grow0 = mx0 > m0 + kRescaleLog2, grow1 = mx1 > m1 + kRescaleLog2;
+        if (__any_sync(0xffffffffu, grow0 || grow1)) {
+          const float mn0 = grow0 ? mx0 : m0, mn1 = grow1 ? mx1 : m1;
+          const float c0 = grow0 ? exp2_approx(m0 - mn0) : 1.f;
+          const float c1 = grow1 ? exp2_approx(m1 - mn1) : 1.f;
+          m0 = mn0;
+          m1 = mn1;
+          l0 *= c0;
+          l1 *= c1;
+#pragma unroll
+          for (int i = 0; i < NNT; ++i) {
+            o[i][0] *= c0;
+            o[i][1] *= c0;
+            o[i][2] *= c1;
+            o[i][3] *= c1;
+          }
+        }
         float pr[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          pr[nt][0] = exp2_approx(sc[nt][0] - mn0);
-          pr[nt][1] = exp2_approx(sc[nt][1] - mn0);
-          pr[nt][2] = exp2_approx(sc[nt][2] - mn1);
-          pr[nt][3] = exp2_approx(sc[nt][3] - mn1);
+          pr[nt][0] = exp2_approx(sc[nt][0] - m0);
+          pr[nt][1] = exp2_approx(sc[nt][1] - m0);
+          pr[nt][2] = exp2_approx(sc[nt][2] - m1);
+          pr[nt][3] = exp2_approx(sc[nt][3] - m1);
         }
-        l0 = l0 * c0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-        l1 = l1 * c1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-#pragma unroll
-        for (int i = 0; i < NNT; ++i) {
-          o[i][0] *= c0;
-          o[i][1] *= c0;
-          o[i][2] *= c1;
-          o[i][3] *= c1;
-        }
+        l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+        l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
         uint32_t pa[4];
         if constexpr (!FP8) {
           pa[0] = pack_bf16(pr[0][0], pr[0][1]);
@@ -368,14 +387,15 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
             uint32_t r0, r1, r2, r3;
             ldsm_x4_t(vb + swz<C::BOX_BYTES>(tok, ch), r0, r1, r2, r3);
             const int c0 = 2 * cp, c1 = 2 * cp + 1;
-            mma_f16(o[2 * c0], pa, e4m3x2_to_f16x2_lo8(r0, kSelB02) & mlo,
-                    e4m3x2_to_f16x2_lo8(r1, kSelB02) & mhi);
-            mma_f16(o[2 * c0 + 1], pa, e4m3x2_to_f16x2_lo8(r0, kSelB13) & mlo,
-                    e4m3x2_to_f16x2_lo8(r1, kSelB13) & mhi);
-            mma_f16(o[2 * c1], pa, e4m3x2_to_f16x2_lo8(r2, kSelB02) & mlo,
-                    e4m3x2_to_f16x2_lo8(r3, kSelB02) & mhi);
-            mma_f16(o[2 * c1 + 1], pa, e4m3x2_to_f16x2_lo8(r2, kSelB13) & mlo,
-                    e4m3x2_to_f16x2_lo8(r3, kSelB13) & mhi);
+            uint32_t a02, a13, b02, b13, x02, x13, y02, y13;
+            e4m3_b02_b13(r0, a02, a13);
+            e4m3_b02_b13(r1, b02, b13);
+            e4m3_b02_b13(r2, x02, x13);
+            e4m3_b02_b13(r3, y02, y13);
+            mma_f16(o[2 * c0], pa, a02 & mlo, b02 & mhi);
+            mma_f16(o[2 * c0 + 1], pa, a13 & mlo, b13 & mhi);
+            mma_f16(o[2 * c1], pa, x02 & mlo, y02 & mhi);
+            mma_f16(o[2 * c1 + 1], pa, x13 & mlo, y13 & mhi);
           }
         }
       }
@@ -595,9 +615,9 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   prm.bs = cc->block_size;
   prm.max_blocks = a.max_blocks;
   prm.num_blocks = cc->num_blocks;
-  // FP8 codes are widened as code * 2^-8; the 2^8 returns through the scales
-  prm.qk_scale_log2 = a.scale * kLog2e * (fp8 ? cc->k_scale * 256.f : 1.f);
-  prm.v_mult = fp8 ? cc->v_scale * 256.f : 1.f;
+  // FP8 codes are widened exactly; the per-tensor scales enter here
+  prm.qk_scale_log2 = a.scale * kLog2e * (fp8 ? cc->k_scale : 1.f);
+  prm.v_mult = fp8 ? cc->v_scale : 1.f;
   prm.err = a.err;
   kvattn_status st;
   if (fp8)
