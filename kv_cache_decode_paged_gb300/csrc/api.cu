@@ -198,7 +198,9 @@ extern "C" kvattn_status kvattn_combine(const float* part_out, const float* part
   if (!part_out || !part_lse || !split_first || !split_count || !out || !lse)
     return KVATTN_ERR_INVALID_ARG;
   if (!aligned(part_out, 16) || !aligned(out, 16)) return KVATTN_ERR_INVALID_ARG;
-  if (int64_t(rows_per_unit) * (dv / 4) >= INT_MAX) return KVATTN_ERR_UNSUPPORTED;
+  if (int64_t(rows_per_unit) * (dv / 4) >= INT_MAX ||
+      int64_t(n_units) * rows_per_unit >= INT_MAX)  // one block per (unit, row)
+    return KVATTN_ERR_UNSUPPORTED;
   return launch_combine(part_out, part_lse, split_first, split_count, n_units, rows_per_unit, dv,
                         out, lse, false, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVATTN_OK

@@ -138,78 +138,106 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
 // Merge the partial results of every split unit:
 //   M = max_w lse_w,  o = sum_w e^(lse_w - M) o_w / sum_w e^(lse_w - M),
 //   lse = M + log sum_w e^(lse_w - M).
-// One warp per (unit, row): the lanes reduce M and the normaliser over the
-// splits together, then each lane streams float4 columns of the partial rows
-// (independent loads across splits).  skip_single leaves units with one split
-// alone (the decode kernel already wrote their final rows).
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_out,
-                                                      const float* __restrict__ part_lse,
-                                                      const int32_t* __restrict__ first,
-                                                      const int32_t* __restrict__ count,
-                                                      int n_units, int rows, int dv,
-                                                      float* __restrict__ out,
-                                                      float* __restrict__ lse, int skip_single) {
-  const int lane = threadIdx.x & 31;
-  const int64_t n_pairs = int64_t(n_units) * rows;
+// One block per (unit, row): the threads reduce M and the normaliser over the
+// splits together; for the weighted sum, warp i takes splits i, i+8, ... and
+// each lane a float4 column, and the eight partial sums meet in shared memory.
+// A unit can have hundreds of splits (a long sequence over many CTAs), so the
+// splits, not only the columns, are spread over threads.  skip_single leaves
+// units with one split alone (the decode kernel already wrote their rows).
+constexpr int kCombineThreads = 256;
+constexpr int kCombineWarps = kCombineThreads / 32;
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse,
+                   const int32_t* __restrict__ first, const int32_t* __restrict__ count,
+                   int rows, int dv, float* __restrict__ out, float* __restrict__ lse,
+                   int skip_single) {
+  __shared__ float red[kCombineWarps];
+  __shared__ float4 part[kCombineWarps][32];
+  const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
+  const int u = blockIdx.x / rows, r = blockIdx.x % rows;
+  const int cnt = count[u];
+  if (cnt == 1 && skip_single) return;
+  const int f = first[u];
   const int v4 = dv >> 2;
-  for (int64_t pr = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; pr < n_pairs;
-       pr += (int64_t(gridDim.x) * blockDim.x) >> 5) {
-    const int u = int(pr / rows), r = int(pr % rows);
-    const int cnt = count[u];
-    if (cnt == 1 && skip_single) continue;  // warp-uniform
-    const int f = first[u];
-    const float* lrow = part_lse + size_t(f) * rows + r;  // split w at lrow[w * rows]
-    float M = -INFINITY;
-    for (int w = lane; w < cnt; w += 32) M = fmaxf(M, lrow[size_t(w) * rows]);
+  const float* lrow = part_lse + size_t(f) * rows + r;  // split w at lrow[w * rows]
+  float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
+
+  float M = -INFINITY;
+  for (int w = tid; w < cnt; w += kCombineThreads) M = fmaxf(M, lrow[size_t(w) * rows]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
-    if (M == -INFINITY) {
-      for (int c = lane; c < v4; c += 32) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (lane == 0) lse[size_t(u) * rows + r] = -INFINITY;
-      continue;
-    }
-    float den = 0.f;
-    for (int w = lane; w < cnt; w += 32) {
-      const float lw = lrow[size_t(w) * rows];
-      if (lw != -INFINITY) den += exp2_approx((lw - M) * kLog2e);
-    }
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red[wi] = M;
+  __syncthreads();
+  M = red[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    const float inv = 1.f / den;
-    const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
-    const size_t wstride = size_t(rows) * v4;  // float4s between splits
-    for (int c = lane; c < v4; c += 32) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int w = 0; w < cnt; ++w) {
-        const float lw = lrow[size_t(w) * rows];
-        const float e = lw == -INFINITY ? 0.f : exp2_approx((lw - M) * kLog2e);
-        const float4 p = prow[size_t(w) * wstride + c];
-        if (e != 0.f) {  // a split with no valid row holds zeros, never NaN, but skip it
-          acc.x += e * p.x;
-          acc.y += e * p.y;
-          acc.z += e * p.z;
-          acc.w += e * p.w;
-        }
-      }
-      orow[c] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
-    if (lane == 0) lse[size_t(u) * rows + r] = M + log2_approx(den) * kLn2;
+  for (int i = 1; i < kCombineWarps; ++i) M = fmaxf(M, red[i]);
+  __syncthreads();  // red is reused below
+  if (M == -INFINITY) {  // no split saw a valid token for this row
+    for (int c = tid; c < v4; c += kCombineThreads) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0) lse[size_t(u) * rows + r] = -INFINITY;
+    return;
   }
+  float den = 0.f;
+  for (int w = tid; w < cnt; w += kCombineThreads) {
+    const float lw = lrow[size_t(w) * rows];
+    if (lw != -INFINITY) den += exp2_approx((lw - M) * kLog2e);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane == 0) red[wi] = den;
+  __syncthreads();
+  den = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCombineWarps; ++i) den += red[i];
+  const float inv = 1.f / den;
+
+  const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
+  const size_t wstride = size_t(rows) * v4;  // float4s between splits
+  for (int c0 = 0; c0 < v4; c0 += 32) {
+    const int c = c0 + lane;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < v4) {
+#pragma unroll 4
+      for (int w = wi; w < cnt; w += kCombineWarps) {
+        const float lw = lrow[size_t(w) * rows];
+        if (lw == -INFINITY) continue;  // a split with no valid token for this row
+        const float e = exp2_approx((lw - M) * kLog2e);
+        const float4 p = prow[size_t(w) * wstride + c];
+        acc.x += e * p.x;
+        acc.y += e * p.y;
+        acc.z += e * p.z;
+        acc.w += e * p.w;
+      }
+    }
+    part[wi][lane] = acc;
+    __syncthreads();
+    if (wi == 0 && c < v4) {
+      float4 t = part[0][lane];
+#pragma unroll
+      for (int i = 1; i < kCombineWarps; ++i) {
+        const float4 q = part[i][lane];
+        t.x += q.x;
+        t.y += q.y;
+        t.z += q.z;
+        t.w += q.w;
+      }
+      orow[c] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
+    }
+    __syncthreads();
+  }
+  if (tid == 0) lse[size_t(u) * rows + r] = M + log2_approx(den) * kLn2;
 }
 
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
                            const int32_t* count, int n_units, int rows, int dv, float* out,
                            float* lse, bool skip_single, cudaStream_t s) {
-  if (n_units <= 0) return cudaSuccess;
-  const int threads = 256;
-  const int64_t warps = int64_t(n_units) * rows;
-  int64_t blocks = (warps + threads / 32 - 1) / (threads / 32);
-  const int cap = device_sm_count() > 0 ? 8 * device_sm_count() : 1184;
-  if (blocks > cap) blocks = cap;
-  combine_kernel<<<int(blocks), threads, 0, s>>>(part_out, part_lse, first, count, n_units, rows,
-                                                 dv, out, lse, skip_single ? 1 : 0);
+  if (n_units <= 0 || rows <= 0) return cudaSuccess;
+  const int64_t blocks = int64_t(n_units) * rows;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  combine_kernel<<<unsigned(blocks), kCombineThreads, 0, s>>>(part_out, part_lse, first, count,
+                                                              rows, dv, out, lse,
+                                                              skip_single ? 1 : 0);
   return cudaGetLastError();
 }
 
