@@ -67,6 +67,14 @@ KV_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream runs;
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible (a no-op without the launch attribute); pdl_launch_dependents()
+// lets the next such kernel start early.
+KV_DEVI void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+KV_DEVI void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Non-blocking test: has the phase with the given parity completed?
 KV_DEVI bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

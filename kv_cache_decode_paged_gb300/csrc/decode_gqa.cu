@@ -116,6 +116,10 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
+  // Launched right behind the planner: wait for its plan, and let the combine
+  // that follows get scheduled while this grid runs.
+  pdl_wait();
+  pdl_launch_dependents();
   const int4 st = p.cta_start[c], en = p.cta_start[c + 1];
   if (!pos_less(st, en)) return;
 
@@ -545,8 +549,10 @@ static kvattn_status launch_variant(const GqaArgs& a, const GqaParams& prm, int 
   if (!encode_tensor_map_3d(&tmK, dt, cc->k, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_3d(&tmV, dt, cc->v, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return KVATTN_ERR_CUDA;
-  gqa_decode_kernel<D, MT, FP8><<<G, C::THREADS, C::SMEM, a.stream>>>(tmK, tmV, prm);
-  return cudaGetLastError() == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA;
+  return launch_pdl(gqa_decode_kernel<D, MT, FP8>, dim3(G), dim3(C::THREADS), C::SMEM, a.stream,
+                    tmK, tmV, prm) == cudaSuccess
+             ? KVATTN_OK
+             : KVATTN_ERR_CUDA;
 }
 
 template <int D, bool FP8>

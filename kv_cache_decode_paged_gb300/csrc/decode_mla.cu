@@ -159,6 +159,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
+  // Launched right behind the planner: wait for its plan, and let the combine
+  // that follows get scheduled while this grid runs.
+  pdl_wait();
+  pdl_launch_dependents();
   const int4 st = p.cta_start[pair], en = p.cta_start[pair + 1];
   if (!pos_less(st, en)) return;  // both ranks of the pair take the same exit
 
@@ -764,8 +768,10 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   prm.num_blocks = cc->num_blocks;
   prm.scale_log2 = a.scale * kLog2e;
   prm.err = a.err;
-  mla_decode_kernel<<<2 * G, mla::THREADS, mla::SMEM, a.stream>>>(tmQF, tmQH, tmLF, tmLH, prm);
-  if (cudaGetLastError() != cudaSuccess) return KVATTN_ERR_CUDA;
+  // the kernel fixes its cluster shape (a CTA pair) at compile time
+  if (launch_pdl(mla_decode_kernel, dim3(2 * G), dim3(mla::THREADS), mla::SMEM, a.stream, tmQF,
+                 tmQH, tmLF, tmLH, prm) != cudaSuccess)
+    return KVATTN_ERR_CUDA;
   if (launch_combine(prm.part_out, prm.part_lse, pa.split_first, pa.split_count, a.B, a.h,
                      mla::DC, a.out, a.lse, true, a.stream) != cudaSuccess)
     return KVATTN_ERR_CUDA;

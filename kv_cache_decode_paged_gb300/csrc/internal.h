@@ -1,6 +1,8 @@
 // internal.h -- host-side plumbing shared by the translation units of libkvattn.
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -63,6 +65,25 @@ struct PlanArgs {
 };
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s);
+
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous kernel of the stream finishes and must call pdl_wait() before it
+// reads that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
                            const int32_t* count, int n_units, int rows, int dv, float* out,
                            float* lse, bool skip_single, cudaStream_t s);

@@ -24,15 +24,26 @@ namespace kv {
 // counts are 1 (0 for empty units) and no partial slot is used.  It wins when
 // the split would save little: a CTA that crosses a unit boundary drains its
 // pipeline, and every split unit costs a combine pass over its partials.
+// cum[] is also kept in shared memory when it fits (B < kPlanSmemSeqs), so the
+// searches below do not chase global memory.
+constexpr int kPlanSmemSeqs = 4096;  // 32 KB, inside the default dynamic limit
+
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
   __shared__ int64_t warp_tot[32];
   __shared__ int64_t carry_s;
   __shared__ unsigned long long maxn_s;
+  extern __shared__ int64_t cum_s[];  // [B + 1] when B < kPlanSmemSeqs
+  // Launched with programmatic serialisation: wait for whatever kernel wrote
+  // seq_lens, then let the decode kernel that follows get scheduled.
+  pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  const bool smem_cum = a.B < kPlanSmemSeqs;
   if (tid == 0) {
     carry_s = 0;
     maxn_s = 0;
     a.cum[0] = 0;
+    if (smem_cum) cum_s[0] = 0;
   }
   __syncthreads();
   for (int base = 0; base < a.B; base += blockDim.x) {
@@ -70,12 +81,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     }
     __syncthreads();
     const int64_t carry = carry_s;
-    if (i < a.B) a.cum[i + 1] = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + x;
+    if (i < a.B) {
+      const int64_t v = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + x;
+      a.cum[i + 1] = v;
+      if (smem_cum) cum_s[i + 1] = v;
+    }
     __syncthreads();
     if (tid == 0) carry_s = carry + warp_tot[nw - 1];
     __syncthreads();
   }
-  const int64_t* cum = a.cum;
+  __syncthreads();
+  const int64_t* cum = smem_cum ? cum_s : a.cum;
   const int64_t U = a.units_per_seq;
   const int64_t T = U * cum[a.B];
   // With more CTAs than pages, only the first T CTAs get work (one page or
@@ -131,8 +147,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(a);
-  return cudaGetLastError();
+  const size_t smem = a.B < kPlanSmemSeqs ? size_t(a.B + 1) * sizeof(int64_t) : 0;
+  return launch_pdl(plan_kernel, dim3(1), dim3(1024), smem, s, a);
 }
 
 // Merge the partial results of every split unit:
@@ -154,6 +170,7 @@ __global__ void __launch_bounds__(kCombineThreads)
                    int skip_single) {
   __shared__ float red[kCombineWarps];
   __shared__ float4 part[kCombineWarps][32];
+  pdl_wait();  // the partials come from the kernel launched just before
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int u = blockIdx.x / rows, r = blockIdx.x % rows;
   const int cnt = count[u];
@@ -235,10 +252,8 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
   if (n_units <= 0 || rows <= 0) return cudaSuccess;
   const int64_t blocks = int64_t(n_units) * rows;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  combine_kernel<<<unsigned(blocks), kCombineThreads, 0, s>>>(part_out, part_lse, first, count,
-                                                              rows, dv, out, lse,
-                                                              skip_single ? 1 : 0);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(unsigned(blocks)), dim3(kCombineThreads), 0, s, part_out,
+                    part_lse, first, count, rows, dv, out, lse, skip_single ? 1 : 0);
 }
 
 // ---- device queries -----------------------------------------------------------
