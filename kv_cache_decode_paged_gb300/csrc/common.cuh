@@ -88,8 +88,11 @@ KV_DEVI bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
+// Bounded wait for the phase with the given parity to complete.  A phase that
+// has already completed is seen by the non-blocking test, which is cheaper
+// than a try_wait.
 KV_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
   for (uint32_t i = 0; i < KV_MAX_SPIN; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;

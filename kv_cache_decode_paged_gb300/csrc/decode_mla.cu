@@ -173,7 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kSFull0 + i], 1);
       mbar_init(&bars[kSRead0 + i], (NSW + NSEND) / 32);  // one arrival per reading warp
-      mbar_init(&bars[kPFull0 + i], NSW);
+      mbar_init(&bars[kPFull0 + i], NSW / 32);  // one arrival per softmax warp
       mbar_init(&bars[kPVDone0 + i], 1);
       mbar_init(&bars[kXFull0 + i], 1);    // one local expect_tx arrival + the peer's bytes
       mbar_init(&bars[kXEmpty0 + i], 1);   // one arrival from the peer's softmax warps
@@ -408,7 +408,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       ++seg;
       for (int k = sg.j0; k < sg.j1; ++k, ++u) {
         const uint32_t slot = u & 1;
-        bool good = qgood && wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
+        // Staging is free once the peer has received the previous partial; the
+        // peer's receive slot once it has read the partial sent two tiles ago.
+        // Both concern earlier tiles, so they are waited for before S(u): the
+        // path from S(u) landing to its push then holds no wait.  Both signals
+        // only say that reads have finished, so waits at CTA scope suffice.
+        bool good = qgood && (u == 0 || wait_all(&bars[kXSent], (u - 1) & 1));
+        good = good && (u < 2 || wait_all(&bars[kXEmpty0 + slot], ((u - 2) >> 1) & 1));
+        good = good && wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
         uint32_t hx[32];
         if (good) {
           tc_fence_after();
@@ -425,12 +432,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             hx[16 + j] = partial_pair(v1[2 * j], v1[2 * j + 1], p.scale_log2);
           }
         }
-        // Staging is free once the peer has received the previous partial; the
-        // peer's receive slot once it has read the partial sent two tiles ago.
-        // Both signals only say that reads have finished, so waits at CTA
-        // scope suffice.
-        good = good && (u == 0 || wait_all(&bars[kXSent], (u - 1) & 1));
-        good = good && (u < 2 || wait_all(&bars[kXEmpty0 + slot], ((u - 2) >> 1) & 1));
         // the abort flag is read by every lane but decided for the warp
         good = good && !__any_sync(0xffffffffu, *abort_flag != 0);
         if (!good) { ok = false; break; }
@@ -602,7 +603,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           }
           tc_fence_before();
-          mbar_arrive(&bars[kPFull0 + slot]);
+          __syncwarp();  // good is warp-uniform: the whole warp is here
+          if (lane == 0) mbar_arrive(&bars[kPFull0 + slot]);
         }
       }
       // ---- epilogue: O / l for this segment's rows (each thread: 128 columns)
