@@ -281,6 +281,17 @@ KV_DEVI void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
 
 // Bounded wait that acquires at cluster scope (sees the peer's released writes).
 KV_DEVI bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
   for (uint32_t i = 0; i < KV_MAX_SPIN; ++i) {
     uint32_t ok;
     asm volatile(

@@ -19,18 +19,22 @@
 // its half of the output O[:, 256r : 256r + 256] += P . c[:, 256r : 256r + 256]
 // (the c_KV part of D_r is exactly the value columns it needs).
 // The two partial scores meet through distributed shared memory: each rank
-// scales its partial to log2 units, rounds it to f16 and pushes it to the
-// other with one bulk copy; both ranks add the same two f16 partials, so their
-// softmax inputs and P are bit-identical.
+// rounds its raw partial to f16 and pushes it into the peer's receive slot
+// with bulk copies; both ranks add the same two f16 partials, so their softmax
+// inputs and P are bit-identical.
 //
 // Measured on GB300: a K = 16 MMA with M = 128 reading both operands from
 // shared memory costs ~78 cycles for any N <= 128 (and 128 cycles at N = 256);
 // with A in tensor memory ~123 cycles for N <= 128 and ~136 at N = 256.  A
-// distributed-shared-memory push has ~1000 cycles of latency.  The kernel is
-// therefore organised so that the exchange of tile t+1 overlaps the softmax of
-// tile t, and so that four value stages fit: the first 128 c_KV dims of this
-// rank's Q sit in TMEM (score K steps 0..7 read A from TMEM), the other 128
-// and the 32 rope dims in shared memory.
+// bulk copy into the peer's shared memory takes ~0.6 us to land, while loads
+// from the peer's shared memory and release-ordered remote arrives each cost
+// about as much again, so partials are pushed, never pulled.  The exchange of
+// tile t+1 overlaps the softmax of tile t: two staging slots keep a push
+// in flight while the next one is staged, and each softmax warp hands its
+// share of the receive slot back as soon as it holds the values in registers.
+// Four value stages fit because the first 128 c_KV dims of this rank's Q sit
+// in TMEM (score K steps 2..9 read A from TMEM), the other 128 and the 32 rope
+// dims in shared memory.
 //   warp 0      TMA producer: per sequence the shared-memory part of Q; per
 //               tile 4 value boxes (4-stage ring) and one rope box (2-slot
 //               ring, freed once S is computed)
@@ -77,9 +81,9 @@ constexpr int NROPE = 2;                                  // rope ring
 constexpr int OFF_R = OFF_V + NSTAGE * VSTAGE;
 constexpr int XROW = BS * 2;                              // a row of a partial tile, f16
 constexpr int XBYTES = 128 * XROW;                        // 16 KB
-constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // 2 receive slots (peer writes)
-constexpr int OFF_XS = OFF_X + 2 * XBYTES;                // send staging
-constexpr int OFF_MX = OFF_XS + XBYTES;                   // row max / row sum exchange
+constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // receive slot (the peer writes)
+constexpr int OFF_XS = OFF_X + XBYTES;                    // 2 send staging slots
+constexpr int OFF_MX = OFF_XS + 2 * XBYTES;               // row max / row sum exchange
 constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
 constexpr int NBARS = 32;
 constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
@@ -124,12 +128,12 @@ enum : int {
   kSRead0 = 5,      // 2: the senders and the softmax warps have read S slot t % 2
   kPFull0 = 7,      // 2: P(t) written to P slot t % 2
   kPVDone0 = 9,     // 2: P.V of tile t finished
-  kXFull0 = 11,     // 2: the peer's partial of tile t is in receive slot t % 2 (tx bytes)
-  kXEmpty0 = 13,    // 2: the peer has read this rank's partial from its receive slot t % 2
-  kXSent = 15,      // the peer has received this rank's last partial: staging is free
-  kQTmem = 16,      // the sender warps have written this sequence's Q columns to TMEM
-  kMmaDrain = 17,   // 2: each MMA issuer's last operations completed (exit path)
-  kKVFull0 = 19,                          // NSTAGE: value boxes (and rope box) landed
+  kXFull = 11,      // the peer's partial of tile t is in the receive slot (tx bytes)
+  kXEmpty = 12,     // the peer has read this rank's partial of tile t from its receive slot
+  kXSent0 = 13,     // 2: the peer has received this rank's partial from staging slot t % 2
+  kQTmem = 15,      // the sender warps have written this sequence's Q columns to TMEM
+  kMmaDrain = 16,   // 2: each MMA issuer's last operations completed (exit path)
+  kKVFull0 = 18,                          // NSTAGE: value boxes (and rope box) landed
   kKVEmpty0 = kKVFull0 + mla::NSTAGE,     // NSTAGE: P.V finished with the value stage
   kRopeEmpty0 = kKVEmpty0 + mla::NSTAGE,  // 2: S finished with the rope slot
   kAbort = kRopeEmpty0 + 2,               // an int flag in this slot
@@ -137,10 +141,20 @@ enum : int {
 };
 static_assert(kNumBars <= mla::NBARS, "barrier slots");
 
-// One f16 pair of scaled partial scores: senders and softmax warps round the
-// same fp32 values the same way.
-KV_DEVI uint32_t partial_pair(uint32_t a, uint32_t b, float scale_log2) {
-  return pack_f16(__uint_as_float(a) * scale_log2, __uint_as_float(b) * scale_log2);
+// One f16 pair of partial scores (raw dot products, unscaled): the senders
+// and the softmax warps round the same fp32 values the same way, and both
+// ranks add the same two f16 pairs (f16 addition is commutative), so their
+// softmax inputs are bit-identical.
+KV_DEVI uint32_t partial_pair(uint32_t a, uint32_t b) {
+  return pack_f16(__uint_as_float(a), __uint_as_float(b));
+}
+KV_DEVI uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hadd2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+KV_DEVI uint32_t hmax2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
@@ -175,11 +189,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       mbar_init(&bars[kSRead0 + i], (NSW + NSEND) / 32);  // one arrival per reading warp
       mbar_init(&bars[kPFull0 + i], NSW / 32);  // one arrival per softmax warp
       mbar_init(&bars[kPVDone0 + i], 1);
-      mbar_init(&bars[kXFull0 + i], 1);    // one local expect_tx arrival + the peer's bytes
-      mbar_init(&bars[kXEmpty0 + i], 1);   // one arrival from the peer's softmax warps
+      mbar_init(&bars[kXSent0 + i], 1);    // one arrival from the peer's softmax warps
       mbar_init(&bars[kRopeEmpty0 + i], 1);
     }
-    mbar_init(&bars[kXSent], 1);           // one arrival from the peer's softmax warps
+    mbar_init(&bars[kXFull], 1);           // one local expect_tx arrival + the peer's bytes
+    mbar_init(&bars[kXEmpty], NSW / 32);   // one arrival per softmax warp of the peer
     mbar_init(&bars[kQTmem], NSEND / 32);
     mbar_init(&bars[kMmaDrain], 1);
     mbar_init(&bars[kMmaDrain + 1], 1);
@@ -189,8 +203,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bars[kXFull0], XBYTES);      // the peer's tiles 0 and 1
-    mbar_arrive_expect_tx(&bars[kXFull0 + 1], XBYTES);
+    mbar_arrive_expect_tx(&bars[kXFull], XBYTES);       // the peer's tile 0
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -371,7 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
     uint8_t* xstage = smem + OFF_XS;
     const uint32_t xbuf_peer = map_peer(smem_u32(smem + OFF_X), peer);
-    const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull0]), peer);
+    const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull]), peer);
     auto wait_all = [](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
     };
@@ -407,14 +420,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       }
       ++seg;
       for (int k = sg.j0; k < sg.j1; ++k, ++u) {
-        const uint32_t slot = u & 1;
-        // Staging is free once the peer has received the previous partial; the
-        // peer's receive slot once it has read the partial sent two tiles ago.
-        // Both concern earlier tiles, so they are waited for before S(u): the
-        // path from S(u) landing to its push then holds no wait.  Both signals
-        // only say that reads have finished, so waits at CTA scope suffice.
-        bool good = qgood && (u == 0 || wait_all(&bars[kXSent], (u - 1) & 1));
-        good = good && (u < 2 || wait_all(&bars[kXEmpty0 + slot], ((u - 2) >> 1) & 1));
+        const uint32_t slot = u & 1;   // S slot and staging slot
+        // Staging slot u % 2 is free once the peer has received the partial
+        // pushed from it two tiles ago (long before S(u) lands), so S(u) is
+        // read and staged at once; the push itself then waits only until the
+        // peer has read the previous partial out of its receive slot.  Both
+        // signals only say that reads have finished, so waits at CTA scope
+        // suffice.
+        bool good = qgood && (u < 2 || wait_all(&bars[kXSent0 + slot], ((u - 2) >> 1) & 1));
         good = good && wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
         uint32_t hx[32];
         if (good) {
@@ -428,8 +441,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            hx[j] = partial_pair(v0[2 * j], v0[2 * j + 1], p.scale_log2);
-            hx[16 + j] = partial_pair(v1[2 * j], v1[2 * j + 1], p.scale_log2);
+            hx[j] = partial_pair(v0[2 * j], v0[2 * j + 1]);
+            hx[16 + j] = partial_pair(v1[2 * j], v1[2 * j + 1]);
           }
         }
         // the abort flag is read by every lane but decided for the warp
@@ -437,16 +450,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         if (!good) { ok = false; break; }
         // Each warp stages and pushes its own 32 rows (4 KB): no barrier across
         // the sender warps; the peer's barrier counts the bytes of all four.
-        uint4* srow = reinterpret_cast<uint4*>(xstage + r * XROW);
+        uint8_t* sbuf = xstage + slot * XBYTES;
+        uint4* srow = reinterpret_cast<uint4*>(sbuf + r * XROW);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           srow[c ^ (r & 7)] = make_uint4(hx[4 * c], hx[4 * c + 1], hx[4 * c + 2], hx[4 * c + 3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (u > 0 && !wait_all(&bars[kXEmpty], (u - 1) & 1)) { ok = false; break; }
         __syncwarp();
         if (lane == 0) {
           const uint32_t off = uint32_t(32 * (warp & 3)) * XROW;
-          bulk_copy_to_peer(xbuf_peer + slot * XBYTES + off, xstage + off, 32 * XROW,
-                            xfull_peer + 8 * slot);
+          bulk_copy_to_peer(xbuf_peer + off, sbuf + off, 32 * XROW, xfull_peer);
         }
       }
     }
@@ -455,11 +469,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       *abort_flag = 1;
     }
     // Drain: the peer's last arrivals on this CTA's barriers (received / read)
-    if (u > 0) {
-      mbar_wait_cluster(&bars[kXSent], (u - 1) & 1);
-      mbar_wait_cluster(&bars[kXEmpty0 + ((u - 1) & 1)], ((u - 1) >> 1) & 1);
-      if (u > 1) mbar_wait_cluster(&bars[kXEmpty0 + (u & 1)], ((u - 2) >> 1) & 1);
-    }
+    for (uint32_t k = u > 2 ? u - 2 : 0; k < u; ++k)
+      mbar_wait_cluster(&bars[kXSent0 + (k & 1)], (k >> 1) & 1);
+    if (u > 0) mbar_wait_cluster(&bars[kXEmpty], (u - 1) & 1);
   } else {
     // ------------------------------------------ softmax / epilogue warps (2..9)
     const int r = 32 * (warp & 3) + lane;          // head row = TMEM lane
@@ -468,8 +480,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     const int tid = threadIdx.x - SW0;             // 0..255
     const uint8_t* xbuf = smem + OFF_X;
     float* mx_s = reinterpret_cast<float*>(smem + OFF_MX);   // [2][128]
-    const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty0]), peer);
-    const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent]), peer);
+    const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty]), peer);
+    const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent0]), peer);
     Walker w{p.cum, 1, st, en};
     Seg sg;
     uint32_t it = 0, received = 0;
@@ -500,40 +512,52 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) own[j] = partial_pair(v[2 * j], v[2 * j + 1], p.scale_log2);
+          for (int j = 0; j < 16; ++j) own[j] = partial_pair(v[2 * j], v[2 * j + 1]);
         }
         // The peer's bulk copy writes this CTA's shared memory and completes on
         // this CTA's barrier: observing the phase makes the bytes visible.
-        good = good && wait_all(&bars[kXFull0 + slot], (t >> 1) & 1);
+        good = good && wait_all(&bars[kXFull], t & 1);
         received += good ? 1u : 0u;
         if (good && tid == 0) {
-          // the bulk copy has landed, so it has read the peer's staging buffer
-          mbar_arrive_remote_relaxed(xsent_peer);
-          mbar_arrive_expect_tx(&bars[kXFull0 + slot], XBYTES);    // arm for tile t + 2
+          // the bulk copy has landed, so it has read the peer's staging slot t % 2
+          mbar_arrive_remote_relaxed(xsent_peer + 8 * slot);
+          // arm for tile t + 1: the peer pushes it only after this rank's
+          // receive slot is released below, after every thread saw this phase
+          mbar_arrive_expect_tx(&bars[kXFull], XBYTES);
         }
-        float sc[32];
+        // hs: f16 pairs of full raw scores, tokens 32hh + 2j and + 2j + 1
+        uint32_t hs[16];
         float mx = -INFINITY;
         if (good) {
           const int valid = len - (sg.j0 + int(k)) * BS - 32 * hh;
-          const uint4* xr = reinterpret_cast<const uint4*>(xbuf + slot * XBYTES + r * XROW);
+          const uint4* xr = reinterpret_cast<const uint4*>(xbuf + r * XROW);
+          uint4 pv[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) pv[c] = xr[(4 * hh + c) ^ (r & 7)];
+          // Once every lane's loads have been performed the warp releases its
+          // share of the receive slot, so that the peer can push the next
+          // partial while this tile's softmax goes on.
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 pv4 = xr[(4 * hh + c) ^ (r & 7)];
-            const uint32_t pw[4] = {pv4.x, pv4.y, pv4.z, pv4.w};
+            hs[4 * c] = hadd2_u32(own[4 * c], pv[c].x);
+            hs[4 * c + 1] = hadd2_u32(own[4 * c + 1], pv[c].y);
+            hs[4 * c + 2] = hadd2_u32(own[4 * c + 2], pv[c].z);
+            hs[4 * c + 3] = hadd2_u32(own[4 * c + 3], pv[c].w);
+          }
+          if (valid < 32) {   // tokens past the end of the sequence score -inf
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int j = 8 * c + 2 * q;
-              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&own[4 * c + q]));
-              const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&pw[q]));
-              sc[j] = a.x + b.x;
-              sc[j + 1] = a.y + b.y;
+            for (int j = 0; j < 16; ++j) {
+              if (2 * j >= valid) hs[j] = (hs[j] & 0xffff0000u) | 0xfc00u;
+              if (2 * j + 1 >= valid) hs[j] = (hs[j] & 0x0000ffffu) | 0xfc000000u;
             }
           }
+          uint32_t hm = hs[0];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            sc[j] = j < valid ? sc[j] : -INFINITY;
-            mx = fmaxf(mx, sc[j]);
-          }
+          for (int j = 1; j < 16; ++j) hm = hmax2_u32(hm, hs[j]);
+          const float2 m2 = __half22float2(*reinterpret_cast<const __half2*>(&hm));
+          mx = fmaxf(m2.x, m2.y) * p.scale_log2;   // log2 units (scale > 0 keeps the order)
         }
         // One barrier per tile in the common case: every thread has read the
         // receive slot, and no row's max has outgrown its reference by the
@@ -572,8 +596,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             m_ref = m_new;
           }
         }
-        // receive slot read: every thread's loads from it returned before the barrier
-        if (good && tid == 32) mbar_arrive_remote_relaxed(xempty_peer + 8 * slot);
         // P slot t % 2 was last read by P.V(t - 2)
         good = good && (t < 2 || wait_all(&bars[kPVDone0 + slot], ((t - 2) >> 1) & 1));
         if (good) {
@@ -582,7 +604,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           float lsum = 0.f;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float p0 = exp2_approx(sc[2 * j] - m_ref), p1 = exp2_approx(sc[2 * j + 1] - m_ref);
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hs[j]));
+            const float p0 = exp2_approx(fmaf(f.x, p.scale_log2, -m_ref));
+            const float p1 = exp2_approx(fmaf(f.y, p.scale_log2, -m_ref));
             lsum += p0 + p1;
             pk[j] = pack_bf16(p0, p1);
           }
@@ -654,14 +678,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     if (!ok) {
       report(p.err, KVATTN_DEVERR_TIMEOUT);
       *abort_flag = 1;
-      // The peer may have pushed up to two partials that were not consumed;
-      // they land before this CTA's shared memory goes away.
+      // The peer may have pushed one partial that was not consumed (it pushes
+      // the next only after this rank released the receive slot); it lands
+      // before this CTA's shared memory goes away.
       uint32_t total = 0;
       Walker w2{p.cum, 1, st, en};
       Seg s2;
       while (w2.next(s2)) total += uint32_t(s2.j1 - s2.j0);
-      for (uint32_t k = received; k < total && k < received + 2; ++k)
-        mbar_wait_cluster(&bars[kXFull0 + (k & 1)], (k >> 1) & 1);
+      if (received < total) mbar_wait_cluster(&bars[kXFull], received & 1);
     }
   }
   tc_fence_before();
