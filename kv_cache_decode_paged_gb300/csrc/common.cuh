@@ -125,6 +125,19 @@ KV_DEVI void tma_load_3d_nohint(void* smem_dst, const CUtensorMap* map, int c0, 
       : "memory");
 }
 
+// 3-D tiled store of one box from shared memory (bulk async group).  The box
+// is clipped at the tensor's bounds.
+KV_DEVI void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+KV_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every bulk store this thread committed has completed.
+KV_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // L2 policy for data read exactly once per step (the KV stream).
 KV_DEVI uint64_t policy_evict_first() {
   uint64_t p;

@@ -103,6 +103,7 @@ static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
                   OFF_XS % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM <= 232448, "shared memory");
+static_assert((NSW / 32) * 4 * 32 * 128 <= NSTAGE * VSTAGE, "epilogue staging fits the value ring");
 }  // namespace mla
 
 struct MlaParams {
@@ -161,7 +162,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmQF,
                       const __grid_constant__ CUtensorMap tmQH,
                       const __grid_constant__ CUtensorMap tmLF,
-                      const __grid_constant__ CUtensorMap tmLH, const MlaParams p) {
+                      const __grid_constant__ CUtensorMap tmLH,
+                      const __grid_constant__ CUtensorMap tmO,
+                      const __grid_constant__ CUtensorMap tmPO, const MlaParams p) {
   using namespace mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -654,17 +657,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         dl = p.part_lse + slot_idx * p.h + r;
       }
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      Walker wn = w;
+      Seg sn;
+      if (!wn.next(sn)) {
+        // The CTA's last segment: the value ring is idle (every load was
+        // consumed by a P.V that has completed), so each warp stages its 32 rows
+        // x 128 columns there in four 128-byte swizzled boxes and one lane
+        // stores them with TMA (whole lines, instead of one 16-byte piece of
+        // 32 rows per store instruction).  Rows past h fall outside the
+        // tensor and are clipped.
+        uint8_t* ob = smem + OFF_V + (warp - 2) * (4 * 32 * 128);
 #pragma unroll 1
-      for (int cb = 0; cb < 128; cb += 32) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_off + TM_O + 128 * hh + cb, o);
-        tmem_ld_wait();
-        if (row_ok) {
-          float4* d4 = reinterpret_cast<float4*>(dst + cb);
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + TM_O + 128 * hh + 32 * cb, o);
+          tmem_ld_wait();
+          uint8_t* brow = ob + cb * (32 * 128) + lane * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            d4[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                                __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+            *reinterpret_cast<float4*>(brow + ((j ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                            __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          const int z = sg.full ? sg.b : sg.b + pair;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb)
+            tma_store_3d(sg.full ? &tmO : &tmPO, ob + cb * (32 * 128),
+                         256 * int(rank) + 128 * hh + 32 * cb, 32 * (warp & 3), z);
+          bulk_commit();
+          bulk_wait_all();
+        }
+        __syncwarp();
+      } else {
+#pragma unroll 1
+        for (int cb = 0; cb < 128; cb += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + TM_O + 128 * hh + cb, o);
+          tmem_ld_wait();
+          if (row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dst + cb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d4[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                  __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+          }
         }
       }
       if (row_ok && rank == 0 && hh == 0)
@@ -757,7 +796,7 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   pa.err = a.err;
   if (launch_plan(pa, a.stream) != cudaSuccess) return KVATTN_ERR_CUDA;
 
-  alignas(64) CUtensorMap tmQF, tmQH, tmLF, tmLH;
+  alignas(64) CUtensorMap tmQF, tmQH, tmLF, tmLH, tmO, tmPO;
   {
     const uint64_t dims[3] = {uint64_t(mla::ROWW), uint64_t(a.h), uint64_t(a.B)};
     const uint64_t strides[2] = {uint64_t(mla::ROWW) * 2, uint64_t(mla::ROWW) * 2 * a.h};
@@ -778,6 +817,18 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
                               boxh, CU_TENSOR_MAP_SWIZZLE_64B))
       return KVATTN_ERR_CUDA;
   }
+  {
+    // outputs as [slots][h][512] fp32, stored in 32 x 32 boxes (128-byte swizzle)
+    const uint64_t so[2] = {uint64_t(mla::DC) * 4, uint64_t(mla::DC) * 4 * a.h};
+    const uint32_t box[3] = {32u, 32u, 1u};
+    const uint64_t dims_o[3] = {uint64_t(mla::DC), uint64_t(a.h), uint64_t(a.B)};
+    const uint64_t dims_p[3] = {uint64_t(mla::DC), uint64_t(a.h), uint64_t(a.B) + uint64_t(G)};
+    if (!encode_tensor_map_3d(&tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.out, dims_o, so, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_3d(&tmPO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + L.part_out, dims_p, so,
+                              box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return KVATTN_ERR_CUDA;
+  }
   MlaParams prm;
   prm.q = static_cast<const uint16_t*>(a.q);
   prm.bt = a.block_table;
@@ -796,7 +847,7 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   prm.err = a.err;
   // the kernel fixes its cluster shape (a CTA pair) at compile time
   if (launch_pdl(mla_decode_kernel, dim3(2 * G), dim3(mla::THREADS), mla::SMEM, a.stream, tmQF,
-                 tmQH, tmLF, tmLH, prm) != cudaSuccess)
+                 tmQH, tmLF, tmLH, tmO, tmPO, prm) != cudaSuccess)
     return KVATTN_ERR_CUDA;
   if (launch_combine(prm.part_out, prm.part_lse, pa.split_first, pa.split_count, a.B, a.h,
                      mla::DC, a.out, a.lse, true, a.stream) != cudaSuccess)
