@@ -208,6 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     fence_barrier_init();
     mbar_arrive_expect_tx(&bars[kXFull], XBYTES);       // the peer's tile 0
   }
+  __syncwarp();  // warp 0 reconverges before the warp-aligned instructions below
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
@@ -727,6 +728,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       if (received < total) mbar_wait_cluster(&bars[kXFull], received & 1);
     }
   }
+  // Role code diverges within warps (single-lane producers and issuers); the
+  // CTA barrier and the cluster barrier below are warp-aligned, so every warp
+  // reconverges first.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
