@@ -29,18 +29,18 @@
 // bulk copy into the peer's shared memory takes ~0.6 us to land, while loads
 // from the peer's shared memory and release-ordered remote arrives each cost
 // about as much again, so partials are pushed, never pulled.  The exchange of
-// tile t+1 overlaps the softmax of tile t: two staging slots keep a push
-// in flight while the next one is staged, and each softmax warp hands its
-// share of the receive slot back as soon as it holds the values in registers.
-// Four value stages fit because the first 128 c_KV dims of this rank's Q sit
-// in TMEM (score K steps 2..9 read A from TMEM), the other 128 and the 32 rope
-// dims in shared memory.
+// tile t+1 overlaps the softmax of tile t: a push lands well within a tile, so
+// one staging buffer suffices, and each softmax warp hands its share of the
+// receive slot back as soon as it holds the values in registers.  Four value
+// stages fit because the first 64 c_KV dims of this rank's Q sit in TMEM
+// (score K steps 2..5 read A from TMEM), the other 192 and the 32 rope dims in
+// shared memory.
 //   warp 0      TMA producer: per sequence the shared-memory part of Q; per
 //               tile 4 value boxes (4-stage ring) and one rope box (2-slot
 //               ring, freed once S is computed)
 //   warp 1      TMEM owner and S issuer: S(t) into one of two S slots
 //   warp 14     P.V issuer: P.V(t) with P from one of two P slots
-//   warps 10-13 senders: per sequence Q[:, 256r : 256r + 128] into TMEM; per
+//   warps 10-13 senders: per sequence Q[:, 256r : 256r + 64] into TMEM; per
 //               tile S(t) partial -> f16 -> staging -> bulk copy to the peer
 //               (one thread per head row)
 //   warps 2-9   softmax: peer partial + own partial, online softmax with lazy
@@ -67,9 +67,11 @@ constexpr int QF_BYTES = 128 * 128;    // Q box [128 heads x 64 dims], 128-byte 
 constexpr int QH_BYTES = 128 * 64;     // Q box [128 heads x 32 rope dims], 64-byte swizzle
 constexpr int VF_BYTES = BS * 128;     // latent box [64 rows x 64 dims]
 constexpr int RH_BYTES = BS * 64;      // latent box [64 rows x 32 rope dims]
-constexpr int OFF_QF = 0;                                 // Q dims 256r+128 .. 256r+255
-constexpr int OFF_QH = 2 * QF_BYTES;                      // Q rope dims
-constexpr int Q_BYTES = 2 * QF_BYTES + QH_BYTES;          // 40 KB
+constexpr int NQT = 4;                                    // score K steps with Q in TMEM
+constexpr int NQF = 4 - NQT / 4;                          // Q boxes in shared memory
+constexpr int OFF_QF = 0;                                 // Q dims 256r+16*NQT .. 256r+255
+constexpr int OFF_QH = NQF * QF_BYTES;                    // Q rope dims
+constexpr int Q_BYTES = NQF * QF_BYTES + QH_BYTES;        // 56 KB
 constexpr int NSTAGE = 4;                                 // value ring
 constexpr int VSTAGE = 4 * VF_BYTES;                      // 32 KB
 // The value ring is laid out box-major: box i (dims 64i .. 64i+63 of this
@@ -82,8 +84,8 @@ constexpr int OFF_R = OFF_V + NSTAGE * VSTAGE;
 constexpr int XROW = BS * 2;                              // a row of a partial tile, f16
 constexpr int XBYTES = 128 * XROW;                        // 16 KB
 constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // receive slot (the peer writes)
-constexpr int OFF_XS = OFF_X + XBYTES;                    // 2 send staging slots
-constexpr int OFF_MX = OFF_XS + 2 * XBYTES;               // row max / row sum exchange
+constexpr int OFF_XS = OFF_X + XBYTES;                    // send staging
+constexpr int OFF_MX = OFF_XS + XBYTES;                   // row max / row sum exchange
 constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
 constexpr int NBARS = 32;
 constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
@@ -96,7 +98,7 @@ constexpr int KSTEPS = 18;             // 288 score dims per rank / 16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;           // two S slots of 64 columns
 constexpr uint32_t TM_P = 128;         // two P slots of 32 columns (bf16 pairs)
-constexpr uint32_t TM_Q = 192;         // Q dims 256r .. 256r+127 (bf16 pairs)
+constexpr uint32_t TM_Q = 192;         // Q dims 256r .. 256r+16*NQT-1 (bf16 pairs)
 constexpr uint32_t TM_O = 256;         // O half: columns 256..511
 constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the max grows by 2^8
 static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
@@ -131,7 +133,7 @@ enum : int {
   kPVDone0 = 9,     // 2: P.V of tile t finished
   kXFull = 11,      // the peer's partial of tile t is in the receive slot (tx bytes)
   kXEmpty = 12,     // the peer has read this rank's partial of tile t from its receive slot
-  kXSent0 = 13,     // 2: the peer has received this rank's partial from staging slot t % 2
+  kXSent = 13,      // the peer has received this rank's partial of tile t: staging is free
   kQTmem = 15,      // the sender warps have written this sequence's Q columns to TMEM
   kMmaDrain = 16,   // 2: each MMA issuer's last operations completed (exit path)
   kKVFull0 = 18,                          // NSTAGE: value boxes (and rope box) landed
@@ -192,10 +194,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       mbar_init(&bars[kSRead0 + i], (NSW + NSEND) / 32);  // one arrival per reading warp
       mbar_init(&bars[kPFull0 + i], NSW / 32);  // one arrival per softmax warp
       mbar_init(&bars[kPVDone0 + i], 1);
-      mbar_init(&bars[kXSent0 + i], 1);    // one arrival from the peer's softmax warps
       mbar_init(&bars[kRopeEmpty0 + i], 1);
     }
     mbar_init(&bars[kXFull], 1);           // one local expect_tx arrival + the peer's bytes
+    mbar_init(&bars[kXSent], 1);           // one arrival from the peer's softmax warps
     mbar_init(&bars[kXEmpty], NSW / 32);   // one arrival per softmax warp of the peer
     mbar_init(&bars[kQTmem], NSEND / 32);
     mbar_init(&bars[kMmaDrain], 1);
@@ -237,8 +239,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       while (ok && w.next(sg)) {
         if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
-        for (int i = 0; i < 2; ++i)
-          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 128 + 64 * i, 0, sg.b,
+        for (int i = 0; i < NQF; ++i)
+          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 16 * NQT + 64 * i, 0, sg.b,
                              &bars[kQFull]);
         tma_load_3d_nohint(smem + OFF_QH, &tmQH, rx, 0, sg.b, &bars[kQFull]);
         const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
@@ -309,10 +311,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             } else {
               const int m = j - 2;  // c_KV dims 16m .. 16m+15 of this rank
               const uint64_t b = vb0 + uint64_t(((m >> 2) * VBOX + (m & 3) * 32) >> 4);
-              if (m < 8)
+              if (m < NQT)
                 umma_ts(d, tmem + TM_Q + 8 * m, b, id_s, 1u);
               else
-                umma_ss(d, qa0 + uint64_t((((m - 8) >> 2) * QF_BYTES + (m & 3) * 32) >> 4), b,
+                umma_ss(d, qa0 + uint64_t((((m - NQT) >> 2) * QF_BYTES + (m & 3) * 32) >> 4), b,
                         id_s, 1u);
             }
           }
@@ -397,7 +399,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     uint32_t u = 0, seg = 0;
     bool ok = true;
     while (ok && w.next(sg)) {
-      // This sequence's Q[:, 256r : 256r + 128] into TMEM, once the previous
+      // This sequence's Q[:, 256r : 256r + 16 NQT] into TMEM, once the previous
       // sequence's score MMAs (which read it) have completed.  Rows past h are 0.
       bool qgood = seg == 0 || wait_all(&bars[kQEmpty], (seg - 1) & 1);
       if (qgood) {
@@ -405,7 +407,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         const uint4* src =
             reinterpret_cast<const uint4*>(p.q + (int64_t(sg.b) * p.h + r) * ROWW + 256 * rank);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < NQT / 4; ++half) {
           uint32_t qv[32];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -424,15 +426,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       }
       ++seg;
       for (int k = sg.j0; k < sg.j1; ++k, ++u) {
-        const uint32_t slot = u & 1;   // S slot and staging slot
-        // Staging slot u % 2 is free once the peer has received the partial
-        // pushed from it two tiles ago (long before S(u) lands), so S(u) is
-        // read and staged at once; the push itself then waits only until the
-        // peer has read the previous partial out of its receive slot.  Both
-        // signals only say that reads have finished, so waits at CTA scope
-        // suffice.
-        bool good = qgood && (u < 2 || wait_all(&bars[kXSent0 + slot], ((u - 2) >> 1) & 1));
-        good = good && wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
+        const uint32_t slot = u & 1;   // S slot
+        bool good = qgood && wait_all(&bars[kSFull0 + slot], (u >> 1) & 1);
         uint32_t hx[32];
         if (good) {
           tc_fence_after();
@@ -452,9 +447,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         // the abort flag is read by every lane but decided for the warp
         good = good && !__any_sync(0xffffffffu, *abort_flag != 0);
         if (!good) { ok = false; break; }
-        // Each warp stages and pushes its own 32 rows (4 KB): no barrier across
-        // the sender warps; the peer's barrier counts the bytes of all four.
-        uint8_t* sbuf = xstage + slot * XBYTES;
+        // Staging is free once the peer has received the previous partial (it
+        // lands ~0.6 us after its push, well within a tile); the push then waits
+        // until the peer has read the previous partial out of its receive slot.
+        // Both signals only say that reads have finished, so waits at CTA scope
+        // suffice.  Each warp stages and pushes its own 32 rows (4 KB): no
+        // barrier across the sender warps; the peer's barrier counts the bytes
+        // of all four.
+        if (u > 0 && !wait_all(&bars[kXSent], (u - 1) & 1)) { ok = false; break; }
+        uint8_t* sbuf = xstage;
         uint4* srow = reinterpret_cast<uint4*>(sbuf + r * XROW);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -473,9 +474,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       *abort_flag = 1;
     }
     // Drain: the peer's last arrivals on this CTA's barriers (received / read)
-    for (uint32_t k = u > 2 ? u - 2 : 0; k < u; ++k)
-      mbar_wait_cluster(&bars[kXSent0 + (k & 1)], (k >> 1) & 1);
-    if (u > 0) mbar_wait_cluster(&bars[kXEmpty], (u - 1) & 1);
+    if (u > 0) {
+      mbar_wait_cluster(&bars[kXSent], (u - 1) & 1);
+      mbar_wait_cluster(&bars[kXEmpty], (u - 1) & 1);
+    }
   } else {
     // ------------------------------------------ softmax / epilogue warps (2..9)
     const int r = 32 * (warp & 3) + lane;          // head row = TMEM lane
@@ -485,7 +487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     const uint8_t* xbuf = smem + OFF_X;
     float* mx_s = reinterpret_cast<float*>(smem + OFF_MX);   // [2][128]
     const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty]), peer);
-    const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent0]), peer);
+    const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent]), peer);
     Walker w{p.cum, 1, st, en};
     Seg sg;
     uint32_t it = 0, received = 0;
@@ -523,8 +525,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         good = good && wait_all(&bars[kXFull], t & 1);
         received += good ? 1u : 0u;
         if (good && tid == 0) {
-          // the bulk copy has landed, so it has read the peer's staging slot t % 2
-          mbar_arrive_remote_relaxed(xsent_peer + 8 * slot);
+          // the bulk copy has landed, so it has read the peer's staging buffer
+          mbar_arrive_remote_relaxed(xsent_peer);
           // arm for tile t + 1: the peer pushes it only after this rank's
           // receive slot is released below, after every thread saw this phase
           mbar_arrive_expect_tx(&bars[kXFull], XBYTES);
