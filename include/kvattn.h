@@ -208,7 +208,8 @@ KVATTN_API kvattn_status kvattn_decode_mla(const void* q_absorbed, const kvattn_
  *   weight.  out [n_units][rows_per_unit][dv], lse [n_units][rows_per_unit].
  *   All pointers are device pointers; dv must be a multiple of 4 and
  *   part_out / out 16-byte aligned (KVATTN_ERR_INVALID_ARG otherwise);
- *   n_units * rows_per_unit must stay below 2^31 (KVATTN_ERR_UNSUPPORTED). */
+ *   n_units * rows_per_unit must stay below 2^31 and dv at most 512
+ *   (KVATTN_ERR_UNSUPPORTED otherwise). */
 KVATTN_API kvattn_status kvattn_combine(const float* part_out, const float* part_lse,
                              const int32_t* split_first, const int32_t* split_count, int n_units,
                              int rows_per_unit, int dv, float* out, float* lse, void* stream);

@@ -195,6 +195,7 @@ extern "C" kvattn_status kvattn_combine(const float* part_out, const float* part
                                         float* lse, void* stream) {
   if (n_units < 0 || rows_per_unit <= 0 || dv <= 0 || dv % 4) return KVATTN_ERR_INVALID_ARG;
   if (n_units == 0) return KVATTN_OK;
+  if (dv > 512) return KVATTN_ERR_UNSUPPORTED;  // row widths of the decode paths: 64, 128, 512
   if (!part_out || !part_lse || !split_first || !split_count || !out || !lse)
     return KVATTN_ERR_INVALID_ARG;
   if (!aligned(part_out, 16) || !aligned(out, 16)) return KVATTN_ERR_INVALID_ARG;

@@ -154,22 +154,25 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
 // Merge the partial results of every split unit:
 //   M = max_w lse_w,  o = sum_w e^(lse_w - M) o_w / sum_w e^(lse_w - M),
 //   lse = M + log sum_w e^(lse_w - M).
-// One block per (unit, row): the threads reduce M and the normaliser over the
-// splits together; for the weighted sum, warp i takes splits i, i+8, ... and
-// each lane a float4 column, and the eight partial sums meet in shared memory.
-// A unit can have hundreds of splits (a long sequence over many CTAs), so the
-// splits, not only the columns, are spread over threads.  skip_single leaves
-// units with one split alone (the decode kernel already wrote their rows).
+// One block per (unit, row).  Warp i takes splits i, i+8, ... and keeps a
+// running (max, normaliser, weighted sum) over them -- the online form of the
+// same merge, so each split's lse and output row are loaded together in one
+// pass -- and lane l the float4 columns l, l+32, ...; the eight warp states
+// meet in shared memory.  A unit can have hundreds of splits (a long sequence
+// over many CTAs), so the splits, not only the columns, are spread over warps.
+// skip_single leaves units with one split alone (the decode kernel already
+// wrote their rows).
 constexpr int kCombineThreads = 256;
 constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kCombineMaxCols = 4;   // float4 columns per lane: dv <= 512
 
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse,
                    const int32_t* __restrict__ first, const int32_t* __restrict__ count,
                    int rows, int dv, float* __restrict__ out, float* __restrict__ lse,
                    int skip_single) {
-  __shared__ float red[kCombineWarps];
-  __shared__ float4 part[kCombineWarps][32];
+  __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+  __shared__ float4 s_acc[kCombineWarps][kCombineMaxCols * 32];
   pdl_wait();  // the partials come from the kernel launched just before
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int u = blockIdx.x / rows, r = blockIdx.x % rows;
@@ -178,78 +181,78 @@ __global__ void __launch_bounds__(kCombineThreads)
   const int f = first[u];
   const int v4 = dv >> 2;
   const float* lrow = part_lse + size_t(f) * rows + r;  // split w at lrow[w * rows]
-  float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
-
-  float M = -INFINITY;
-  for (int w = tid; w < cnt; w += kCombineThreads) M = fmaxf(M, lrow[size_t(w) * rows]);
+  const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
+  const size_t wstride = size_t(rows) * v4;             // float4s between splits
+  float m = -INFINITY, l = 0.f;                         // log2 units
+  float4 acc[kCombineMaxCols];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) red[wi] = M;
+  for (int j = 0; j < kCombineMaxCols; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+  for (int w = wi; w < cnt; w += kCombineWarps) {
+    const float lw = lrow[size_t(w) * rows] * kLog2e;
+    float4 v[kCombineMaxCols];
+#pragma unroll
+    for (int j = 0; j < kCombineMaxCols; ++j)
+      v[j] = (lane + 32 * j < v4) ? prow[size_t(w) * wstride + lane + 32 * j]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lw == -INFINITY) continue;  // a split with no valid token for this row
+    const float mn = fmaxf(m, lw);
+    const float a = exp2_approx(m - mn), e = exp2_approx(lw - mn);  // a = 0 while m = -inf
+    l = l * a + e;
+#pragma unroll
+    for (int j = 0; j < kCombineMaxCols; ++j) {
+      acc[j].x = acc[j].x * a + e * v[j].x;
+      acc[j].y = acc[j].y * a + e * v[j].y;
+      acc[j].z = acc[j].z * a + e * v[j].z;
+      acc[j].w = acc[j].w * a + e * v[j].w;
+    }
+    m = mn;
+  }
+  if (lane == 0) {
+    s_m[wi] = m;
+    s_l[wi] = l;
+  }
+#pragma unroll
+  for (int j = 0; j < kCombineMaxCols; ++j)
+    if (lane + 32 * j < v4) s_acc[wi][lane + 32 * j] = acc[j];
   __syncthreads();
-  M = red[0];
+  float M = -INFINITY;
 #pragma unroll
-  for (int i = 1; i < kCombineWarps; ++i) M = fmaxf(M, red[i]);
-  __syncthreads();  // red is reused below
+  for (int i = 0; i < kCombineWarps; ++i) M = fmaxf(M, s_m[i]);
+  float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
   if (M == -INFINITY) {  // no split saw a valid token for this row
     for (int c = tid; c < v4; c += kCombineThreads) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid == 0) lse[size_t(u) * rows + r] = -INFINITY;
     return;
   }
-  float den = 0.f;
-  for (int w = tid; w < cnt; w += kCombineThreads) {
-    const float lw = lrow[size_t(w) * rows];
-    if (lw != -INFINITY) den += exp2_approx((lw - M) * kLog2e);
+  float sc[kCombineWarps];
+  float L = 0.f;
+#pragma unroll
+  for (int i = 0; i < kCombineWarps; ++i) {
+    sc[i] = s_m[i] == -INFINITY ? 0.f : exp2_approx(s_m[i] - M);
+    L += s_l[i] * sc[i];
   }
+  const float inv = 1.f / L;
+  for (int c = tid; c < v4; c += kCombineThreads) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  if (lane == 0) red[wi] = den;
-  __syncthreads();
-  den = 0.f;
-#pragma unroll
-  for (int i = 0; i < kCombineWarps; ++i) den += red[i];
-  const float inv = 1.f / den;
-
-  const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
-  const size_t wstride = size_t(rows) * v4;  // float4s between splits
-  for (int c0 = 0; c0 < v4; c0 += 32) {
-    const int c = c0 + lane;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (c < v4) {
-#pragma unroll 4
-      for (int w = wi; w < cnt; w += kCombineWarps) {
-        const float lw = lrow[size_t(w) * rows];
-        if (lw == -INFINITY) continue;  // a split with no valid token for this row
-        const float e = exp2_approx((lw - M) * kLog2e);
-        const float4 p = prow[size_t(w) * wstride + c];
-        acc.x += e * p.x;
-        acc.y += e * p.y;
-        acc.z += e * p.z;
-        acc.w += e * p.w;
-      }
+    for (int i = 0; i < kCombineWarps; ++i) {
+      const float4 q = s_acc[i][c];
+      t.x += sc[i] * q.x;
+      t.y += sc[i] * q.y;
+      t.z += sc[i] * q.z;
+      t.w += sc[i] * q.w;
     }
-    part[wi][lane] = acc;
-    __syncthreads();
-    if (wi == 0 && c < v4) {
-      float4 t = part[0][lane];
-#pragma unroll
-      for (int i = 1; i < kCombineWarps; ++i) {
-        const float4 q = part[i][lane];
-        t.x += q.x;
-        t.y += q.y;
-        t.z += q.z;
-        t.w += q.w;
-      }
-      orow[c] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
-    }
-    __syncthreads();
+    orow[c] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
   }
-  if (tid == 0) lse[size_t(u) * rows + r] = M + log2_approx(den) * kLn2;
+  if (tid == 0) lse[size_t(u) * rows + r] = (M + log2_approx(L)) * kLn2;
 }
 
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
                            const int32_t* count, int n_units, int rows, int dv, float* out,
                            float* lse, bool skip_single, cudaStream_t s) {
   if (n_units <= 0 || rows <= 0) return cudaSuccess;
+  if (dv > 4 * 32 * kCombineMaxCols) return cudaErrorInvalidValue;
   const int64_t blocks = int64_t(n_units) * rows;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   return launch_pdl(combine_kernel, dim3(unsigned(blocks)), dim3(kCombineThreads), 0, s, part_out,

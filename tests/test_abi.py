@@ -137,3 +137,4 @@ def test_append_and_combine_validation(lib):
     assert lib.kvattn_append(ctypes.byref(c), FAKE, FAKE, 5, FAKE, FAKE, FAKE, 2, 4, None, None) == 1
     assert lib.kvattn_combine(FAKE, FAKE, FAKE, FAKE, 3, 4, 6, FAKE, FAKE, None) == 1   # dv % 4
     assert lib.kvattn_combine(FAKE, FAKE, FAKE, FAKE, 0, 4, 8, FAKE, FAKE, None) == 0
+    assert lib.kvattn_combine(FAKE, FAKE, FAKE, FAKE, 3, 4, 516, FAKE, FAKE, None) == 2  # dv > 512
