@@ -601,6 +601,11 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   pa.cta_start = reinterpret_cast<int4*>(ws + L.cta);
   pa.split_first = reinterpret_cast<int32_t*>(ws + L.split_first);
   pa.split_count = reinterpret_cast<int32_t*>(ws + L.split_count);
+  pa.arrive = nullptr;   // merged by the combine kernel
+  pa.out = nullptr;
+  pa.lse = nullptr;
+  pa.rows = g;
+  pa.dv = a.d;
   pa.err = a.err;
   if (launch_plan(pa, a.stream) != cudaSuccess) return KVATTN_ERR_CUDA;
 

@@ -54,6 +54,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "merge.cuh"
 #include "tcgen05.cuh"
 #include "walk.cuh"
 
@@ -117,8 +118,11 @@ struct MlaParams {
   float* out;
   float* lse;
   float* part_out;
-  float* part_lse;
-  int B, h, max_blocks;
+  float* part_lse;              // [slots][2][h]: one copy per rank
+  const int32_t* split_first;  // per sequence: first partial slot and number of splits
+  const int32_t* split_count;
+  int32_t* arrive;             // merge counters, per rank: [B] units, then [B + G] slots
+  int B, h, max_blocks, G;
   int64_t num_blocks;
   float scale_log2;
   int32_t* err;
@@ -140,7 +144,8 @@ enum : int {
   kKVEmpty0 = kKVFull0 + mla::NSTAGE,     // NSTAGE: P.V finished with the value stage
   kRopeEmpty0 = kKVEmpty0 + mla::NSTAGE,  // 2: S finished with the rope slot
   kAbort = kRopeEmpty0 + 2,               // an int flag in this slot
-  kNumBars = kAbort + 1
+  kMergeFlags = kAbort + 1,               // 2 slots: 3 ints for the in-kernel merge
+  kNumBars = kMergeFlags + 2
 };
 static_assert(kNumBars <= mla::NBARS, "barrier slots");
 
@@ -165,8 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
                       const __grid_constant__ CUtensorMap tmQH,
                       const __grid_constant__ CUtensorMap tmLF,
                       const __grid_constant__ CUtensorMap tmLH,
-                      const __grid_constant__ CUtensorMap tmO,
-                      const __grid_constant__ CUtensorMap tmPO, const MlaParams p) {
+                      const __grid_constant__ CUtensorMap tmO, const MlaParams p) {
   using namespace mla;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -492,6 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     Seg sg;
     uint32_t it = 0, received = 0;
     bool ok = true;
+    int nseg = 0, seg_unit[2] = {0, 0}, seg_slot[2] = {0, 0};   // this CTA's partials
     // Every wait result is made warp-uniform: the warp-collective TMEM
     // instructions that follow must be executed by all 32 lanes or none.
     auto wait_all = [](uint64_t* bar, uint32_t parity) {
@@ -657,13 +662,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       } else {
         const int64_t slot_idx = int64_t(sg.b) + pair;
         dst = p.part_out + (slot_idx * p.h + r) * DC + 256 * rank + 128 * hh;
-        dl = p.part_lse + slot_idx * p.h + r;
+        dl = p.part_lse + (slot_idx * 2 + rank) * p.h + r;   // each rank merges with its own copy
+        if (nseg < 2) {   // only the first and the last segment of a range can be parts
+          seg_unit[nseg] = sg.b;
+          seg_slot[nseg] = int(slot_idx);
+          ++nseg;
+        }
       }
       const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
       Walker wn = w;
       Seg sn;
-      if (!wn.next(sn)) {
-        // The CTA's last segment: the value ring is idle (every load was
+      if (sg.full && !wn.next(sn)) {
+        // The CTA's last segment, final rows: the value ring is idle (every load was
         // consumed by a P.V that has completed), so each warp stages its 32 rows
         // x 128 columns there in four 128-byte swizzled boxes and one lane
         // stores them with TMA (whole lines, instead of one 16-byte piece of
@@ -685,11 +695,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          const int z = sg.full ? sg.b : sg.b + pair;
 #pragma unroll 1
           for (int cb = 0; cb < 4; ++cb)
-            tma_store_3d(sg.full ? &tmO : &tmPO, ob + cb * (32 * 128),
-                         256 * int(rank) + 128 * hh + 32 * cb, 32 * (warp & 3), z);
+            tma_store_3d(&tmO, ob + cb * (32 * 128), 256 * int(rank) + 128 * hh + 32 * cb,
+                         32 * (warp & 3), sg.b);
           bulk_commit();
           bulk_wait_all();
         }
@@ -709,7 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           }
         }
       }
-      if (row_ok && rank == 0 && hh == 0)
+      if (row_ok && (rank == 0 || !sg.full) && hh == 0)
         *dl = (lrow > 0.f) ? (m_ref + log2_approx(lrow)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&bars[kOFree]);
@@ -728,6 +737,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       Seg s2;
       while (w2.next(s2)) total += uint32_t(s2.j1 - s2.j0);
       if (received < total) mbar_wait_cluster(&bars[kXFull], received & 1);
+    } else {
+      // Publish this rank's halves of the partials it wrote and merge the
+      // groups and sequences they complete (merge.cuh): each rank merges its
+      // own 256 output columns, so no combine pass is launched.  The value
+      // ring is not touched; mx_s is free after the last epilogue.
+      MergeArgs m;
+      m.part_out = p.part_out + 256 * rank;
+      m.part_lse = p.part_lse + int(rank) * p.h;
+      m.split_first = p.split_first;
+      m.split_count = p.split_count;
+      m.arrive_unit = p.arrive + int64_t(rank) * (2 * p.B + p.G);
+      m.arrive_slot = m.arrive_unit + p.B;
+      m.out = p.out + 256 * rank;
+      m.lse = p.lse;
+      m.rows = p.h;
+      m.dv = 256;
+      m.ld = DC;
+      m.lse_stride = 2 * p.h;
+      m.write_lse = rank == 0;
+      finish_splits<NSW>(m, nseg, seg_unit, seg_slot, reinterpret_cast<int*>(&bars[kMergeFlags]),
+                         mx_s, tid, 2);
     }
   }
   // Role code diverges within warps (single-lane producers and issuers); the
@@ -793,17 +823,23 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   pa.max_blocks = a.max_blocks;
   pa.G = G;
   // A pair that crosses a sequence boundary drains its pipeline (epilogue,
-  // Q reload: about as long as 7 tiles) and a split sequence costs a combine
-  // pass; below this many extra tiles one pair per sequence is faster.
+  // Q reload: about as long as 7 tiles) and a split sequence costs a merge of
+  // 256 KB partials; below this many extra tiles one pair per sequence is
+  // faster.
   pa.whole_unit_slack = 12;
   pa.cum = reinterpret_cast<int64_t*>(ws + L.cum);
   pa.cta_start = reinterpret_cast<int4*>(ws + L.cta);
   pa.split_first = reinterpret_cast<int32_t*>(ws + L.split_first);
   pa.split_count = reinterpret_cast<int32_t*>(ws + L.split_count);
+  pa.arrive = reinterpret_cast<int32_t*>(ws + L.arrive);
+  pa.out = a.out;
+  pa.lse = a.lse;
+  pa.rows = a.h;
+  pa.dv = mla::DC;
   pa.err = a.err;
   if (launch_plan(pa, a.stream) != cudaSuccess) return KVATTN_ERR_CUDA;
 
-  alignas(64) CUtensorMap tmQF, tmQH, tmLF, tmLH, tmO, tmPO;
+  alignas(64) CUtensorMap tmQF, tmQH, tmLF, tmLH, tmO;
   {
     const uint64_t dims[3] = {uint64_t(mla::ROWW), uint64_t(a.h), uint64_t(a.B)};
     const uint64_t strides[2] = {uint64_t(mla::ROWW) * 2, uint64_t(mla::ROWW) * 2 * a.h};
@@ -825,15 +861,12 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
       return KVATTN_ERR_CUDA;
   }
   {
-    // outputs as [slots][h][512] fp32, stored in 32 x 32 boxes (128-byte swizzle)
+    // final outputs as [B][h][512] fp32, stored in 32 x 32 boxes (128-byte swizzle)
     const uint64_t so[2] = {uint64_t(mla::DC) * 4, uint64_t(mla::DC) * 4 * a.h};
     const uint32_t box[3] = {32u, 32u, 1u};
     const uint64_t dims_o[3] = {uint64_t(mla::DC), uint64_t(a.h), uint64_t(a.B)};
-    const uint64_t dims_p[3] = {uint64_t(mla::DC), uint64_t(a.h), uint64_t(a.B) + uint64_t(G)};
     if (!encode_tensor_map_3d(&tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.out, dims_o, so, box,
-                              CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_3d(&tmPO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + L.part_out, dims_p, so,
-                              box, CU_TENSOR_MAP_SWIZZLE_128B))
+                              CU_TENSOR_MAP_SWIZZLE_128B))
       return KVATTN_ERR_CUDA;
   }
   MlaParams prm;
@@ -846,6 +879,10 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   prm.lse = a.lse;
   prm.part_out = reinterpret_cast<float*>(ws + L.part_out);
   prm.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
+  prm.split_first = pa.split_first;
+  prm.split_count = pa.split_count;
+  prm.arrive = pa.arrive;
+  prm.G = G;
   prm.B = a.B;
   prm.h = a.h;
   prm.max_blocks = a.max_blocks;
@@ -854,11 +891,9 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   prm.err = a.err;
   // the kernel fixes its cluster shape (a CTA pair) at compile time
   if (launch_pdl(mla_decode_kernel, dim3(2 * G), dim3(mla::THREADS), mla::SMEM, a.stream, tmQF,
-                 tmQH, tmLF, tmLH, tmO, tmPO, prm) != cudaSuccess)
+                 tmQH, tmLF, tmLH, tmO, prm) != cudaSuccess)
     return KVATTN_ERR_CUDA;
-  if (launch_combine(prm.part_out, prm.part_lse, pa.split_first, pa.split_count, a.B, a.h,
-                     mla::DC, a.out, a.lse, true, a.stream) != cudaSuccess)
-    return KVATTN_ERR_CUDA;
+
   return KVATTN_OK;
 }
 

@@ -20,9 +20,14 @@ namespace kv {
 //   cta_start[G+1]   (b, kvh, page) where CTA c's range starts
 //   split_first[U]   first partial slot of unit u (slot = u + c for CTA c)
 //   split_count[U]   how many CTAs touched unit u (0, 1 or more)
-// and the decode kernel writes partial outputs for units it did not finish.
+//   arrive[2(U+U+G)] zeroed: arrival counters of the in-kernel merge (MLA),
+//                    for its two column parts (merge.cuh): per part, U unit
+//                    counters, then U+G slot counters
+// and the decode kernel writes partial outputs (and their lse, one copy per
+// column part) for units it did not finish.  GQA merges them with the combine
+// kernel; MLA merges them inside the decode kernel.
 struct WsLayout {
-  size_t cum, cta, split_first, split_count, part_lse, part_out, total;
+  size_t cum, cta, split_first, split_count, arrive, part_lse, part_out, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -38,8 +43,10 @@ inline WsLayout ws_layout(int B, int units, int G, int rows, int dv) {
   off = align256(off + size_t(units) * 4);
   L.split_count = off;
   off = align256(off + size_t(units) * 4);
+  L.arrive = off;
+  off = align256(off + size_t(2 * (units + units + G)) * 4);
   L.part_lse = off;
-  off = align256(off + size_t(units + G) * rows * 4);
+  off = align256(off + size_t(units + G) * 2 * rows * 4);
   L.part_out = off;
   off = align256(off + size_t(units + G) * rows * size_t(dv) * 4);
   L.total = off;
@@ -61,6 +68,13 @@ struct PlanArgs {
   int4* cta_start;
   int32_t* split_first;
   int32_t* split_count;
+  // In-kernel merge only (null otherwise): 2 * (units + units + G) arrival
+  // counters, zeroed here; the rows of units with no token are final at once
+  // and written here (out = 0, lse = -inf).
+  int32_t* arrive;
+  float* out;      // [units][rows][dv]
+  float* lse;      // [units][rows]
+  int rows, dv;
   int32_t* err;
 };
 

@@ -28,6 +28,22 @@ namespace kv {
 // searches below do not chase global memory.
 constexpr int kPlanSmemSeqs = 4096;  // 32 KB, inside the default dynamic limit
 
+// In-kernel merge set-up: zero the arrival counters, and write the rows of
+// units of sequences with no token (no CTA visits them): out = 0, lse = -inf.
+__device__ void merge_setup(const PlanArgs& a, const int64_t* cum) {
+  if (!a.arrive) return;
+  const int64_t U = a.units_per_seq, units = int64_t(a.B) * U;
+  for (int64_t i = threadIdx.x; i < 2 * (units + units + a.G); i += blockDim.x) a.arrive[i] = 0;
+  const int v4 = a.dv >> 2;
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+    if (cum[b + 1] != cum[b]) continue;   // empty sequences are rare: one thread each
+    const int64_t row0 = int64_t(b) * U * a.rows, nrows = U * a.rows;
+    float4* o = reinterpret_cast<float4*>(a.out + row0 * a.dv);
+    for (int64_t i = 0; i < nrows * v4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = 0; i < nrows; ++i) a.lse[row0 + i] = -INFINITY;
+  }
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
   __shared__ int64_t warp_tot[32];
   __shared__ int64_t carry_s;
@@ -110,6 +126,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
       a.split_first[u] = int32_t(2 * u);
       a.split_count[u] = cum[b + 1] > cum[b] ? 1 : 0;
     }
+    merge_setup(a, cum);
     return;
   }
   for (int c = tid; c <= a.G; c += blockDim.x) {
@@ -144,6 +161,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PlanArgs a) {
     a.split_first[u] = int32_t(u + c0);
     a.split_count[u] = int32_t(c1 - c0 + 1);
   }
+  merge_setup(a, cum);
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
