@@ -638,8 +638,11 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   else
     st = dispatch_mt<128, false>(a, prm, G);
   if (st != KVATTN_OK) return st;
+  // With at most a few CTAs per unit on average (G + units <= 4 units), each
+  // split unit's merge is a handful of loads: one warp per row suffices.
+  const bool few = int64_t(G) + units <= 4 * int64_t(units);
   if (launch_combine(prm.part_out, prm.part_lse, pa.split_first, pa.split_count, units, g, a.d,
-                     a.out, a.lse, true, a.stream) != cudaSuccess)
+                     a.out, a.lse, true, a.stream, few) != cudaSuccess)
     return KVATTN_ERR_CUDA;
   return KVATTN_OK;
 }

@@ -98,9 +98,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+// Merge split units' partials.  few_splits picks one warp per (unit, row)
+// (units split a handful of ways); otherwise a block per (unit, row) spreads
+// the splits over its warps.
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
                            const int32_t* count, int n_units, int rows, int dv, float* out,
-                           float* lse, bool skip_single, cudaStream_t s);
+                           float* lse, bool skip_single, cudaStream_t s, bool few_splits = false);
 
 // Number of SMs of the current device (cached per device), or -1.
 int device_sm_count();

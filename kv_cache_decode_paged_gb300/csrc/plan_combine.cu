@@ -266,14 +266,64 @@ __global__ void __launch_bounds__(kCombineThreads)
   if (tid == 0) lse[size_t(u) * rows + r] = (M + log2_approx(L)) * kLn2;
 }
 
+// The same merge with one warp per (unit, row) and eight rows per block, for
+// decodes whose units have few splits each (a handful of loads per warp):
+// a quarter as many blocks as rows, so they start in one wave.  dv <= 128.
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_rows_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse,
+                        const int32_t* __restrict__ first, const int32_t* __restrict__ count,
+                        int64_t n_items, int rows, int dv, float* __restrict__ out,
+                        float* __restrict__ lse, int skip_single) {
+  pdl_wait();  // the partials come from the kernel launched just before
+  const int lane = threadIdx.x & 31;
+  const int64_t item = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+  if (item >= n_items) return;
+  const int u = int(item / rows), r = int(item % rows);
+  const int cnt = count[u];
+  if (cnt == 1 && skip_single) return;
+  const int f = first[u];
+  const int v4 = dv >> 2;
+  const bool col = lane < v4;
+  const float* lrow = part_lse + size_t(f) * rows + r;
+  const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
+  const size_t wstride = size_t(rows) * v4;
+  float m = -INFINITY, l = 0.f;                 // log2 units
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int w = 0; w < cnt; ++w) {
+    const float lw = lrow[size_t(w) * rows] * kLog2e;
+    const float4 v = col ? prow[size_t(w) * wstride + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lw == -INFINITY) continue;  // a split with no valid token for this row
+    const float mn = fmaxf(m, lw);
+    const float a = exp2_approx(m - mn), e = exp2_approx(lw - mn);
+    l = l * a + e;
+    acc.x = acc.x * a + e * v.x;
+    acc.y = acc.y * a + e * v.y;
+    acc.z = acc.z * a + e * v.z;
+    acc.w = acc.w * a + e * v.w;
+    m = mn;
+  }
+  float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
+  const float inv = m == -INFINITY ? 0.f : 1.f / l;   // no valid token: zeros, lse -inf
+  if (col) orow[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (lane == 0) lse[size_t(u) * rows + r] = m == -INFINITY ? -INFINITY : (m + log2_approx(l)) * kLn2;
+}
+
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
                            const int32_t* count, int n_units, int rows, int dv, float* out,
-                           float* lse, bool skip_single, cudaStream_t s) {
+                           float* lse, bool skip_single, cudaStream_t s, bool few_splits) {
   if (n_units <= 0 || rows <= 0) return cudaSuccess;
   if (dv > 4 * 32 * kCombineMaxCols) return cudaErrorInvalidValue;
-  const int64_t blocks = int64_t(n_units) * rows;
-  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  return launch_pdl(combine_kernel, dim3(unsigned(blocks)), dim3(kCombineThreads), 0, s, part_out,
+  const int64_t items = int64_t(n_units) * rows;
+  if (few_splits && dv <= 128) {
+    const int64_t blocks = (items + kCombineWarps - 1) / kCombineWarps;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    return launch_pdl(combine_rows_kernel, dim3(unsigned(blocks)), dim3(kCombineThreads), 0, s,
+                      part_out, part_lse, first, count, items, rows, dv, out, lse,
+                      skip_single ? 1 : 0);
+  }
+  if (items > 0x7fffffff) return cudaErrorInvalidValue;
+  return launch_pdl(combine_kernel, dim3(unsigned(items)), dim3(kCombineThreads), 0, s, part_out,
                     part_lse, first, count, rows, dv, out, lse, skip_single ? 1 : 0);
 }
 
