@@ -107,6 +107,7 @@ static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
               "swizzled tiles need 1024-byte alignment");
 static_assert(SMEM <= 232448, "shared memory");
 static_assert((NSW / 32) * 4 * 32 * 128 <= NSTAGE * VSTAGE, "epilogue staging fits the value ring");
+static_assert(merge_scratch_floats(128) * 4 <= NSTAGE * VSTAGE, "merge scratch fits the value ring");
 }  // namespace mla
 
 struct MlaParams {
@@ -741,7 +742,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       // Publish this rank's halves of the partials it wrote and merge the
       // groups and sequences they complete (merge.cuh): each rank merges its
       // own 256 output columns, so no combine pass is launched.  The value
-      // ring is not touched; mx_s is free after the last epilogue.
+      // ring is idle by now (every load consumed, every P.V and TMA store
+      // complete) and holds the merge's scratch.
       MergeArgs m;
       m.part_out = p.part_out + 256 * rank;
       m.part_lse = p.part_lse + int(rank) * p.h;
@@ -757,7 +759,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       m.lse_stride = 2 * p.h;
       m.write_lse = rank == 0;
       finish_splits<NSW>(m, nseg, seg_unit, seg_slot, reinterpret_cast<int*>(&bars[kMergeFlags]),
-                         mx_s, tid, 2);
+                         reinterpret_cast<float*>(smem + OFF_V), tid, 2);
     }
   }
   // Role code diverges within warps (single-lane producers and issuers); the

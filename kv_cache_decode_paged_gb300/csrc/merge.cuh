@@ -43,9 +43,19 @@ struct MergeArgs {
   bool write_lse;
 };
 
+constexpr int kMergeMaxW = 16;   // inputs whose weights are staged in shared memory
+constexpr int kMergeIPT = 4;     // output float4s per thread per batch
+
+// Shared-memory scratch merge_slots needs for `rows` rows.
+__host__ __device__ constexpr int merge_scratch_floats(int rows) { return (kMergeMaxW + 2) * rows; }
+
 // Merge n inputs, slots s0, s0 + stride, ..., into dst / dst_lse (which may
-// be slot s0 itself).  Every one of the NT threads calls it; sm holds 2 * rows
-// floats of scratch; bar_id is a named barrier over exactly these threads.
+// be slot s0 itself).  Every one of the NT threads calls it; sm holds
+// merge_scratch_floats(rows) floats; bar_id is a named barrier over exactly
+// these threads.  The rows' weights e^(lse_w - M) / sum are computed once;
+// each thread then sums kMergeIPT output float4s at a time, so that the loads
+// of a whole batch are in flight together (a merge is latency-bound: it
+// touches each partial once).
 template <int NT>
 __device__ void merge_slots(const MergeArgs& m, int s0, int stride, int n, float* dst,
                             float* dst_lse, float* sm, int tid, int bar_id) {
@@ -53,6 +63,8 @@ __device__ void merge_slots(const MergeArgs& m, int s0, int stride, int n, float
   const int64_t ls = m.lse_stride;
   float* s_max = sm;
   float* s_inv = sm + rows;
+  float* s_w = sm + 2 * rows;   // [kMergeMaxW][rows], used when n <= kMergeMaxW
+  const bool staged = n <= kMergeMaxW;
   for (int row = tid; row < rows; row += NT) {
     float M = -INFINITY;
     for (int k = 0; k < n; ++k)
@@ -61,32 +73,59 @@ __device__ void merge_slots(const MergeArgs& m, int s0, int stride, int n, float
     if (M != -INFINITY)
       for (int k = 0; k < n; ++k) {
         const float lw = __ldcg(m.part_lse + (s0 + k * stride) * ls + row);
-        if (lw != -INFINITY) den += exp2_approx((lw - M) * kLog2e);
+        const float e = lw != -INFINITY ? exp2_approx((lw - M) * kLog2e) : 0.f;
+        den += e;
+        if (staged) s_w[k * rows + row] = e;
       }
+    const float inv = (M != -INFINITY && den > 0.f) ? 1.f / den : 0.f;
     s_max[row] = M;
-    s_inv[row] = (M != -INFINITY && den > 0.f) ? 1.f / den : 0.f;
+    s_inv[row] = inv;
+    if (staged)
+      for (int k = 0; k < n; ++k) s_w[k * rows + row] = M != -INFINITY ? s_w[k * rows + row] * inv : 0.f;
   }
   named_bar_sync(bar_id, NT);
-  for (int idx = tid; idx < rows * v4; idx += NT) {
-    const int row = idx / v4, c4 = idx - row * v4;
-    const float M = s_max[row], inv = s_inv[row];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (inv > 0.f) {
-#pragma unroll 4
-      for (int k = 0; k < n; ++k) {
-        const int64_t slot = s0 + k * stride;
-        const float lw = __ldcg(m.part_lse + slot * ls + row);
-        if (lw == -INFINITY) continue;   // a split with no valid token for this row
-        const float e = exp2_approx((lw - M) * kLog2e) * inv;
-        const float4 v =
-            __ldcg(reinterpret_cast<const float4*>(m.part_out + (slot * rows + row) * m.ld) + c4);
-        acc.x += e * v.x;
-        acc.y += e * v.y;
-        acc.z += e * v.z;
-        acc.w += e * v.w;
+  const int total = rows * v4;
+  for (int base = tid; base < total; base += NT * kMergeIPT) {
+    float4 acc[kMergeIPT];
+#pragma unroll
+    for (int i = 0; i < kMergeIPT; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < n; ++k) {
+      const int64_t slot = s0 + k * stride;
+      float4 v[kMergeIPT];
+      float e[kMergeIPT];
+#pragma unroll
+      for (int i = 0; i < kMergeIPT; ++i) {
+        const int idx = base + i * NT;
+        const int row = idx / v4, c4 = idx - row * v4;
+        e[i] = 0.f;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < total) {
+          if (staged) {
+            e[i] = s_w[k * rows + row];
+          } else if (s_inv[row] > 0.f) {
+            const float lw = __ldcg(m.part_lse + slot * ls + row);
+            e[i] = lw != -INFINITY ? exp2_approx((lw - s_max[row]) * kLog2e) * s_inv[row] : 0.f;
+          }
+          if (e[i] != 0.f)   // a split with no valid token for this row adds nothing
+            v[i] = __ldcg(reinterpret_cast<const float4*>(m.part_out + (slot * rows + row) * m.ld) + c4);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kMergeIPT; ++i) {
+        acc[i].x += e[i] * v[i].x;
+        acc[i].y += e[i] * v[i].y;
+        acc[i].z += e[i] * v[i].z;
+        acc[i].w += e[i] * v[i].w;
       }
     }
-    reinterpret_cast<float4*>(dst + int64_t(row) * m.ld)[c4] = acc;
+#pragma unroll
+    for (int i = 0; i < kMergeIPT; ++i) {
+      const int idx = base + i * NT;
+      if (idx < total) {
+        const int row = idx / v4, c4 = idx - row * v4;
+        reinterpret_cast<float4*>(dst + int64_t(row) * m.ld)[c4] = acc[i];
+      }
+    }
   }
   // every lse read above is done before dst_lse (possibly slot s0's) changes
   named_bar_sync(bar_id, NT);
@@ -100,7 +139,7 @@ __device__ void merge_slots(const MergeArgs& m, int s0, int stride, int n, float
 // End of a CTA's work: publish its nseg (<= 2) partials, given as (unit,
 // slot) pairs, and merge what their arrivals complete.  Every one of the NT
 // threads calls it with the same arguments; flags points to 3 ints of shared
-// memory, sm to 2 * rows floats.
+// memory, sm to merge_scratch_floats(rows) floats.
 template <int NT>
 __device__ void finish_splits(const MergeArgs& m, int nseg, const int* seg_unit,
                               const int* seg_slot, int* flags, float* sm, int tid, int bar_id) {
