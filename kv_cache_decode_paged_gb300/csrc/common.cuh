@@ -138,6 +138,13 @@ KV_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "mem
 // Wait until every bulk store this thread committed has completed.
 KV_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// 32-byte store of eight 32-bit values (address 32-byte aligned).
+KV_DEVI void st_global_v8(float* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // L2 policy for data read exactly once per step (the KV stream).
 KV_DEVI uint64_t policy_evict_first() {
   uint64_t p;

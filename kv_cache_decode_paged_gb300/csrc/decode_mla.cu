@@ -705,17 +705,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         }
         __syncwarp();
       } else {
+        // Each lane writes its own row: 32-byte stores where the row is 32-byte
+        // aligned (the workspace always is), halving the store transactions of
+        // these scattered rows.
+        const bool v8 = (reinterpret_cast<uintptr_t>(dst) & 31) == 0;
 #pragma unroll 1
         for (int cb = 0; cb < 128; cb += 32) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_off + TM_O + 128 * hh + cb, o);
           tmem_ld_wait();
-          if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
+          if (row_ok && v8) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) st_global_v8(dst + cb + 8 * j, o + 8 * j);
+          } else if (row_ok) {
             float4* d4 = reinterpret_cast<float4*>(dst + cb);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              d4[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                                  __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+              d4[j] = make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                                  __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
           }
         }
       }
