@@ -189,14 +189,20 @@ __global__ void __launch_bounds__(kCombineThreads)
                    const int32_t* __restrict__ first, const int32_t* __restrict__ count,
                    int rows, int dv, float* __restrict__ out, float* __restrict__ lse,
                    int skip_single) {
+  // skip_single is set only behind this library's decode kernels, whose split
+  // counts were written before the decode started (its own dependency wait
+  // precedes its trigger): then they are read before waiting for the decode,
+  // and units with one split leave at once.  Otherwise (the public call, after
+  // arbitrary kernels) everything is read after the wait.
+  if (!skip_single) pdl_wait();
   __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
   __shared__ float4 s_acc[kCombineWarps][kCombineMaxCols * 32];
-  pdl_wait();  // the partials come from the kernel launched just before
   const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5;
   const int u = blockIdx.x / rows, r = blockIdx.x % rows;
   const int cnt = count[u];
   if (cnt == 1 && skip_single) return;
   const int f = first[u];
+  if (skip_single) pdl_wait();  // the partials come from the decode kernel
   const int v4 = dv >> 2;
   const float* lrow = part_lse + size_t(f) * rows + r;  // split w at lrow[w * rows]
   const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
@@ -274,14 +280,17 @@ __global__ void __launch_bounds__(kCombineThreads)
                         const int32_t* __restrict__ first, const int32_t* __restrict__ count,
                         int64_t n_items, int rows, int dv, float* __restrict__ out,
                         float* __restrict__ lse, int skip_single) {
-  pdl_wait();  // the partials come from the kernel launched just before
   const int lane = threadIdx.x & 31;
   const int64_t item = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+  // as in combine_kernel: behind a decode kernel the split counts are read
+  // before waiting for it
+  if (!skip_single) pdl_wait();
   if (item >= n_items) return;
   const int u = int(item / rows), r = int(item % rows);
   const int cnt = count[u];
   if (cnt == 1 && skip_single) return;
   const int f = first[u];
+  if (skip_single) pdl_wait();  // the partials come from the decode kernel
   const int v4 = dv >> 2;
   const bool col = lane < v4;
   const float* lrow = part_lse + size_t(f) * rows + r;
