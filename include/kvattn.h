@@ -160,7 +160,8 @@ KVATTN_API int kvattn_default_num_ctas(int kind, int dtype, int h, int h_kv, int
  *   seq_lens:    device, [batch] int32, tokens cached per sequence (the
  *                current token included).
  *   h % h_kv == 0, g = h / h_kv <= 64; d_h in {64, 128} (FP8: 128);
- *   block_size in {16, 32, 64}.
+ *   block_size a multiple of 16, at most 256 (vLLM's 16 up to one block of
+ *   a short sequence).
  *   scale:       softmax scale (1/sqrt(d_h) in the pages' formula).
  *   out:         device, [batch][h][d_h] float32.
  *   lse:         device, [batch][h] float32, natural log; -inf for empty rows.

@@ -120,8 +120,8 @@ extern "C" kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* ca
   if (g > 64) return KVATTN_ERR_UNSUPPORTED;
   if (d_h != 64 && d_h != 128) return KVATTN_ERR_UNSUPPORTED;
   if (cache->dtype == KVATTN_FP8_E4M3 && d_h != 128) return KVATTN_ERR_UNSUPPORTED;
-  if (cache->block_size != 16 && cache->block_size != 32 && cache->block_size != 64)
-    return KVATTN_ERR_UNSUPPORTED;
+  // whole 16-token TMA chunks per block, at most 16 of them
+  if (cache->block_size % 16 != 0 || cache->block_size > 256) return KVATTN_ERR_UNSUPPORTED;
   if (cache->num_blocks * int64_t(h_kv) >= INT_MAX) return KVATTN_ERR_UNSUPPORTED;
   if (int64_t(batch) * h_kv >= INT_MAX / 2 || int64_t(batch) * h >= INT_MAX) return KVATTN_ERR_UNSUPPORTED;
   if (num_ctas > 65535) return KVATTN_ERR_INVALID_ARG;

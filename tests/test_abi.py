@@ -100,6 +100,8 @@ def _gqa_cache(**kw):
     (dict(d=96), dict(d_h=96), kv.KVATTN_ERR_UNSUPPORTED),              # head dim not built
     (dict(h=130, h_kv=1), dict(h_kv=1), kv.KVATTN_ERR_UNSUPPORTED),     # g > 64
     ({}, dict(block_size=8), kv.KVATTN_ERR_UNSUPPORTED),
+    ({}, dict(block_size=40), kv.KVATTN_ERR_UNSUPPORTED),             # not whole 16-token chunks
+    ({}, dict(block_size=512), kv.KVATTN_ERR_UNSUPPORTED),            # more than 16 chunks
     ({}, dict(dtype=7), kv.KVATTN_ERR_UNSUPPORTED),
     ({}, dict(dtype=kv.KVATTN_FP8_E4M3, k_scale=0.0), kv.KVATTN_ERR_INVALID_ARG),
     ({}, dict(kind=kv.KVATTN_MLA), kv.KVATTN_ERR_INVALID_ARG),

@@ -25,9 +25,23 @@ def test_tiny_config(oracle):
     _check(oracle, wl)
 
 
-@pytest.mark.parametrize("bs", [16, 32, 64])
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
 def test_tiny_block_sizes(oracle, bs):
     _check(oracle, inputs.make_workload("tiny", block_size=bs, table="permuted"))
+
+
+def test_tiny_one_block_per_sequence(oracle):
+    # config 1's contiguous cache read as one 128-token block per sequence
+    wl = inputs.make_workload("tiny", block_size=128)
+    assert wl.block_table.shape[1] == 1
+    _check(oracle, wl)
+
+
+@pytest.mark.parametrize("bs", [128, 256])
+def test_large_blocks_fp8_and_split(oracle, bs):
+    # many 16-token chunks per block, an FP8 cache, and a forced split
+    _check(oracle, inputs.make_workload("llama3_70b_fp8", lens=[700, 2049, 1], block_size=bs))
+    _check(oracle, inputs.make_workload("llama3_8b", lens=[3000, 129], block_size=bs), num_ctas=7)
 
 
 @pytest.mark.parametrize("name,lens", [
