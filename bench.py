@@ -9,10 +9,16 @@ larger than L2, so every step streams the KV cache from HBM.
 
   python bench.py [--config llama3_8b] [--steps K] [--warmup W]
   python bench.py --impl reference      # the float64 CPU oracle on a bounded sample
+  python bench.py --config llama3_70b --q-len 4   # 4 new tokens per sequence (GQA)
   torchrun --nproc-per-node N bench.py --gpus N   # N independent replicas
 
 Metric: decode-attention KV-read GB/s (algorithmic KV bytes of a step / step
 time); also microseconds per layer-step and the fraction of ~8 TB/s.
+
+With --q-len L > 1 (GQA only) a step appends the last L tokens of every
+sequence and runs the multi-token decode: L queries per sequence, causal among
+the new tokens (speculative verification).  The KV bytes read are the same as
+for one token; the work per byte is L times larger.
 """
 from __future__ import annotations
 
@@ -49,6 +55,8 @@ def parse():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="new tokens per sequence (GQA; > 1 runs the multi-token decode)")
     return ap.parse_args()
 
 
@@ -160,14 +168,27 @@ def config_dict(wl, args):
          "parallelism": f"replicas x{args.gpus}"}
     if wl.kind == "gqa":
         d.update({"h_kv": wl.h_kv, "d_h": wl.d})
+    if args.q_len > 1:
+        d["workload"] = f"{wl.name}, {args.q_len} new tokens per sequence"
+        d["q_len"] = args.q_len
     else:
         d.update({"d_c": wl.d_c, "d_rope": wl.d_rope})
     return d
 
 
+def multi_queries(args, wl):
+    """[B][q_len][h][d] bf16 bits for a multi-token run, else None."""
+    if args.q_len <= 1:
+        return None
+    if wl.kind != "gqa":
+        raise SystemExit("--q-len > 1 needs a GQA config")
+    from kv_cache_decode_paged_gb300 import inputs
+    return inputs.multi_token_queries(wl, args.q_len, args.seed)
+
+
 # ----------------------------------------------------------------------- oracle
 
-def oracle_sample_rate(wl, budget_s, oracle):
+def oracle_sample_rate(wl, budget_s, oracle, qm=None):
     """Run the oracle over whole sequences until the time budget is spent.
     Returns (GB/s of KV read, seconds, sample description)."""
     done_bytes, t_total, seqs = 0, 0.0, []
@@ -184,10 +205,16 @@ def oracle_sample_rate(wl, budget_s, oracle):
             kc = oracle.quantize_e4m3(wl.k[sl], wl.k_scale)
             vc = oracle.quantize_e4m3(wl.v[sl], wl.v_scale)
             t0 = time.perf_counter()
-            oracle.gqa_decode(wl.q[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
-                              k_scale=wl.k_scale, v_scale=wl.v_scale)
-        else:
+            if qm is None:
+                oracle.gqa_decode(wl.q[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
+                                  k_scale=wl.k_scale, v_scale=wl.v_scale)
+            else:
+                oracle.gqa_decode_multi(qm[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
+                                        k_scale=wl.k_scale, v_scale=wl.v_scale)
+        elif qm is None:
             oracle.gqa_decode(wl.q[b], wl.k[sl], wl.v[sl], wl.scale)
+        else:
+            oracle.gqa_decode_multi(qm[b], wl.k[sl], wl.v[sl], wl.scale)
         t_total += time.perf_counter() - t0
         done_bytes += int(wl.seq_lens[b]) * per_tok
         seqs.append(int(b))
@@ -207,6 +234,7 @@ def run_reference(args, wl, rank):
     # size one step (a few KV heads of one sequence) so the whole run ends in ~2 minutes
     budget_per_step = min(0.5, 120.0 / max(1, steps + warm))
     order = list(np.argsort(wl.seq_lens))[len(wl.seq_lens) // 2:] or [0]
+    qm = multi_queries(args, wl)
 
     def one(i, heads):
         b = int(order[i % len(order)])
@@ -217,13 +245,16 @@ def run_reference(args, wl, rank):
             oracle.mla_decode(wl.q[b, :hq], rows, wl.d_c, wl.scale)
             return int(wl.seq_lens[b]) * per_tok * hq / wl.h
         g = wl.g
+        kw = {}
+        k, v = wl.k[sl, :heads], wl.v[sl, :heads]
         if wl.kv_dtype == "fp8":
-            kc = oracle.quantize_e4m3(wl.k[sl, :heads], wl.k_scale)
-            vc = oracle.quantize_e4m3(wl.v[sl, :heads], wl.v_scale)
-            oracle.gqa_decode(wl.q[b, :heads * g], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
-                              k_scale=wl.k_scale, v_scale=wl.v_scale)
+            k = oracle.quantize_e4m3(k, wl.k_scale)
+            v = oracle.quantize_e4m3(v, wl.v_scale)
+            kw = dict(fmt=oracle.FMT_E4M3, k_scale=wl.k_scale, v_scale=wl.v_scale)
+        if qm is None:
+            oracle.gqa_decode(wl.q[b, :heads * g], k, v, wl.scale, **kw)
         else:
-            oracle.gqa_decode(wl.q[b, :heads * g], wl.k[sl, :heads], wl.v[sl, :heads], wl.scale)
+            oracle.gqa_decode_multi(qm[b, :, :heads * g], k, v, wl.scale, **kw)
         return int(wl.seq_lens[b]) * per_tok * heads / wl.h_kv
 
     units = wl.h if wl.kind == "mla" else wl.h_kv
@@ -277,25 +308,41 @@ def run_ours(args, wl, rank, world, local):
     g = GpuWorkload(wl, poison=False, device=dev)     # pools filled by kvattn_append (untimed)
     torch.cuda.synchronize()
 
-    # the current token of every non-empty sequence: position s_b - 1
-    live = np.nonzero(wl.seq_lens > 0)[0]
-    last = (wl.cu_seqlens[1:] - 1)[live]
+    # the new tokens of every non-empty sequence: positions s_b - L .. s_b - 1
+    # (L = 1 for plain decode; clipped at 0 for sequences shorter than L)
+    L = args.q_len
+    qm = multi_queries(args, wl)
+    idx = [(b, t) for b in np.nonzero(wl.seq_lens > 0)[0]
+           for t in range(max(0, int(wl.seq_lens[b]) - L), int(wl.seq_lens[b]))]
+    live = np.array([b for b, _ in idx], dtype=np.int64)
+    tpos = np.array([t for _, t in idx], dtype=np.int64)
+    last = wl.cu_seqlens[live] + tpos
     seq_idx = torch.from_numpy(live.astype(np.int32)).to(dev)
-    pos = torch.from_numpy((wl.seq_lens[live] - 1).astype(np.int32)).to(dev)
+    pos = torch.from_numpy(tpos.astype(np.int32)).to(dev)
     if wl.kind == "gqa":
         new0, new1 = dev_bits(wl.k[last], dev), dev_bits(wl.v[last], dev)
         dv = wl.d
     else:
         new0, new1 = dev_bits(wl.c_kv[last], dev), dev_bits(wl.k_r[last], dev)
         dv = wl.d_c
-    ws = g.workspace()
-    out = torch.empty((wl.B, wl.h, dv), dtype=torch.float32, device=dev)
-    lse = torch.empty((wl.B, wl.h), dtype=torch.float32, device=dev)
+    if qm is None:
+        ws = g.workspace()
+        out = torch.empty((wl.B, wl.h, dv), dtype=torch.float32, device=dev)
+        lse = torch.empty((wl.B, wl.h), dtype=torch.float32, device=dev)
+        q_dev = g.q
+    else:
+        ws = kv.workspace_for(kv.KVATTN_GQA, wl.B, wl.h * L, wl.h_kv, wl.d, 0, dev)
+        out = torch.empty((wl.B, L, wl.h, dv), dtype=torch.float32, device=dev)
+        lse = torch.empty((wl.B, L, wl.h), dtype=torch.float32, device=dev)
+        q_dev = dev_bits(qm, dev)
     desc = g.cache.descriptor()
     stream = torch.cuda.current_stream()
 
     def decode():
-        if wl.kind == "gqa":
+        if qm is not None:
+            kv.kvattn_decode_gqa_multi(q_dev, desc, g.bt, g.seq_lens, L, wl.h, wl.h_kv, wl.d,
+                                       wl.scale, out, lse, ws, err=g.err, stream=stream)
+        elif wl.kind == "gqa":
             kv.kvattn_decode_gqa(g.q, desc, g.bt, g.seq_lens, wl.h, wl.h_kv, wl.d, wl.scale,
                                  out, lse, ws, err=g.err, stream=stream)
         else:
@@ -345,7 +392,7 @@ def run_ours(args, wl, rank, world, local):
 
     # ---- end to end: host buffers in, result out, every step
     e2e_steps = args.e2e_steps or args.steps
-    h_q = torch.from_numpy(np.ascontiguousarray(wl.q).view(np.int16)).pin_memory()
+    h_q = torch.from_numpy(np.ascontiguousarray(wl.q if qm is None else qm).view(np.int16)).pin_memory()
     h_new0 = new0.cpu().pin_memory()
     h_new1 = new1.cpu().pin_memory()
     h_pos = pos.cpu().pin_memory()
@@ -356,7 +403,7 @@ def run_ours(args, wl, rank, world, local):
     d2h = h_out.numel() * 4 + h_lse.numel() * 4
 
     def e2e_step():
-        g.q.copy_(h_q, non_blocking=True)
+        q_dev.copy_(h_q, non_blocking=True)
         new0.copy_(h_new0, non_blocking=True)
         new1.copy_(h_new1, non_blocking=True)
         pos.copy_(h_pos, non_blocking=True)
@@ -419,7 +466,7 @@ def run_ours(args, wl, rank, world, local):
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        gbs, secs, sample = oracle_sample_rate(wl, args.cpu_budget_s, oracle)
+        gbs, secs, sample = oracle_sample_rate(wl, args.cpu_budget_s, oracle, qm)
         line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": oracle.num_threads(),
                                 "kind": "oracle", "sample": sample, "seconds": secs}
     print(json.dumps(line), flush=True)

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define KVATTN_ABI_VERSION 1
+#define KVATTN_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define KVATTN_API __attribute__((visibility("default")))
@@ -178,6 +178,30 @@ KVATTN_API kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* ca
                                 float* out, float* lse, void* workspace, size_t workspace_bytes,
                                 int num_ctas, int32_t* err, void* stream);
 
+/* Multi-token GQA decode: q_len new tokens per sequence, all already in the
+ * cache (speculative decoding verifies several draft tokens in one pass: "MLA：
+ * 为什么一份 Latent 可以代替多头 KV Cache", section "Prefill 为什么未必使用与
+ * Decode 相同的吸收方式" lists the tokens one verification checks among the
+ * inputs of kernel selection, and section "正确性验证应该从两种实现互证" item 5
+ * asks the kernel to be checked with speculative tokens).  Token j of sequence
+ * b sits at position s_b - q_len + j and attends causally to positions
+ * [0, s_b - q_len + j]; a token whose position would be negative (s_b < q_len)
+ * sees nothing: out 0, lse -inf.  One K/V read serves all q_len * g rows of a
+ * KV head.
+ *   q:    device, [batch][q_len][h][d_h] bf16.
+ *   out:  device, [batch][q_len][h][d_h] float32;  lse: [batch][q_len][h].
+ *   q_len >= 1 (KVATTN_ERR_INVALID_ARG otherwise), q_len * g <= 64
+ *   (KVATTN_ERR_UNSUPPORTED otherwise).
+ *   workspace: >= kvattn_decode_workspace_bytes(KVATTN_GQA, batch, h * q_len,
+ *   h_kv, d_h, num_ctas) bytes.
+ * Other arguments, and the three launches, as for kvattn_decode_gqa, which is
+ * this call with q_len = 1. */
+KVATTN_API kvattn_status kvattn_decode_gqa_multi(const void* q, const kvattn_cache* cache,
+                                const int32_t* block_table, const int32_t* seq_lens, int batch,
+                                int max_blocks_per_seq, int q_len, int h, int h_kv, int d_h,
+                                float scale, float* out, float* lse, void* workspace,
+                                size_t workspace_bytes, int num_ctas, int32_t* err, void* stream);
+
 /* MLA absorbed decode.
  *   q_absorbed:  device, [batch][h][d_c + d_rope] bf16: [W_UK^T q^C | q^R] per
  *                head ("Let us define the absorbed query vector").
@@ -189,7 +213,9 @@ KVATTN_API kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* ca
  *   lse:         device, [batch][h] float32.
  *   workspace:   >= kvattn_decode_workspace_bytes(KVATTN_MLA, batch, h, 1, d_c,
  *                num_ctas) bytes.
- * Other arguments as for kvattn_decode_gqa. */
+ * Launches two kernels on `stream`: the split planner and the decode kernel,
+ * which also merges the partials of sequences it split over several CTA
+ * pairs.  Other arguments as for kvattn_decode_gqa. */
 KVATTN_API kvattn_status kvattn_decode_mla(const void* q_absorbed, const kvattn_cache* cache,
                                 const int32_t* block_table, const int32_t* seq_lens, int batch,
                                 int max_blocks_per_seq, int h, int d_c, int d_rope, float scale,

@@ -37,6 +37,7 @@ EXPORTED = [
     "kvattn_status_string", "kvattn_abi_version", "kvattn_page_bytes", "kvattn_cell_bytes",
     "kvattn_append", "kvattn_decode_workspace_bytes", "kvattn_default_num_ctas",
     "kvattn_decode_gqa", "kvattn_decode_mla", "kvattn_combine", "kvattn_decode_gqa_noalloc",
+    "kvattn_decode_gqa_multi",
 ]
 
 KVATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -96,6 +97,8 @@ def load_library(build: bool = True) -> ctypes.CDLL:
             "kvattn_combine": (i32, [P, P, P, P, i32, i32, i32, P, P, P]),
             "kvattn_decode_gqa_noalloc": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P,
                                                 i32, P, P]),
+            "kvattn_decode_gqa_multi": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, i32, f32, P,
+                                              P, P, sz, i32, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -165,6 +168,19 @@ def kvattn_decode_gqa(q, cache: kvattn_cache, block_table, seq_lens, h, h_kv, d_
         _ptr(q), ctypes.byref(cache), _ptr(block_table), _ptr(seq_lens), int(batch),
         int(max_blocks), int(h), int(h_kv), int(d_h), float(scale), _ptr(out), _ptr(lse),
         _ptr(workspace), int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
+        int(num_ctas), _ptr(err), _stream(stream)))
+
+
+def kvattn_decode_gqa_multi(q, cache: kvattn_cache, block_table, seq_lens, q_len, h, h_kv, d_h,
+                            scale, out, lse, workspace, num_ctas=0, err=None, stream=None):
+    """q_len new tokens per sequence ([batch][q_len][h][d_h] q, out and lse
+    rows [batch][q_len][h]), causal among the new tokens."""
+    batch, max_blocks = block_table.shape
+    _check("kvattn_decode_gqa_multi", load_library().kvattn_decode_gqa_multi(
+        _ptr(q), ctypes.byref(cache), _ptr(block_table), _ptr(seq_lens), int(batch),
+        int(max_blocks), int(q_len), int(h), int(h_kv), int(d_h), float(scale), _ptr(out),
+        _ptr(lse), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
         int(num_ctas), _ptr(err), _stream(stream)))
 
 

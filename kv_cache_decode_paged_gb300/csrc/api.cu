@@ -94,14 +94,17 @@ extern "C" size_t kvattn_decode_workspace_bytes(int kind, int batch, int h, int 
   return ws_layout(batch, units, G, rows, dv).total;
 }
 
-extern "C" kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* cache,
-                                           const int32_t* block_table, const int32_t* seq_lens,
-                                           int batch, int max_blocks_per_seq, int h, int h_kv,
-                                           int d_h, float scale, float* out, float* lse,
-                                           void* workspace, size_t workspace_bytes, int num_ctas,
-                                           int32_t* err, void* stream) {
+extern "C" kvattn_status kvattn_decode_gqa_multi(const void* q, const kvattn_cache* cache,
+                                                 const int32_t* block_table,
+                                                 const int32_t* seq_lens, int batch,
+                                                 int max_blocks_per_seq, int q_len, int h,
+                                                 int h_kv, int d_h, float scale, float* out,
+                                                 float* lse, void* workspace,
+                                                 size_t workspace_bytes, int num_ctas,
+                                                 int32_t* err, void* stream) {
   if (!cache || cache->kind != KVATTN_GQA) return KVATTN_ERR_INVALID_ARG;
-  if (batch < 0 || max_blocks_per_seq <= 0 || h <= 0 || h_kv <= 0 || d_h <= 0 || num_ctas < 0)
+  if (batch < 0 || max_blocks_per_seq <= 0 || h <= 0 || h_kv <= 0 || d_h <= 0 || num_ctas < 0 ||
+      q_len <= 0)
     return KVATTN_ERR_INVALID_ARG;
   if (h % h_kv != 0) return KVATTN_ERR_INVALID_ARG;  // "num_heads % num_kv_heads == 0"
   if (cache->h_kv != h_kv || cache->d_h != d_h || cache->reserved != 0) return KVATTN_ERR_INVALID_ARG;
@@ -117,13 +120,14 @@ extern "C" kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* ca
   if (cache->dtype == KVATTN_FP8_E4M3 && !(cache->k_scale > 0.f && cache->v_scale > 0.f))
     return KVATTN_ERR_INVALID_ARG;
   const int g = h / h_kv;
-  if (g > 64) return KVATTN_ERR_UNSUPPORTED;
+  if (int64_t(g) * q_len > 64) return KVATTN_ERR_UNSUPPORTED;   // rows per KV head: 4 m-tiles
   if (d_h != 64 && d_h != 128) return KVATTN_ERR_UNSUPPORTED;
   if (cache->dtype == KVATTN_FP8_E4M3 && d_h != 128) return KVATTN_ERR_UNSUPPORTED;
   // whole 16-token TMA chunks per block, at most 16 of them
   if (cache->block_size % 16 != 0 || cache->block_size > 256) return KVATTN_ERR_UNSUPPORTED;
   if (cache->num_blocks * int64_t(h_kv) >= INT_MAX) return KVATTN_ERR_UNSUPPORTED;
-  if (int64_t(batch) * h_kv >= INT_MAX / 2 || int64_t(batch) * h >= INT_MAX) return KVATTN_ERR_UNSUPPORTED;
+  if (int64_t(batch) * h_kv >= INT_MAX / 2 || int64_t(batch) * q_len * h >= INT_MAX)
+    return KVATTN_ERR_UNSUPPORTED;
   if (num_ctas > 65535) return KVATTN_ERR_INVALID_ARG;
   GqaArgs a;
   a.q = q;
@@ -135,6 +139,7 @@ extern "C" kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* ca
   a.h = h;
   a.h_kv = h_kv;
   a.d = d_h;
+  a.qlen = q_len;
   a.scale = scale;
   a.out = out;
   a.lse = lse;
@@ -144,6 +149,17 @@ extern "C" kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* ca
   a.err = err;
   a.stream = static_cast<cudaStream_t>(stream);
   return run_decode_gqa(a);
+}
+
+extern "C" kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* cache,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           int batch, int max_blocks_per_seq, int h, int h_kv,
+                                           int d_h, float scale, float* out, float* lse,
+                                           void* workspace, size_t workspace_bytes, int num_ctas,
+                                           int32_t* err, void* stream) {
+  return kvattn_decode_gqa_multi(q, cache, block_table, seq_lens, batch, max_blocks_per_seq, 1, h,
+                                 h_kv, d_h, scale, out, lse, workspace, workspace_bytes, num_ctas,
+                                 err, stream);
 }
 
 extern "C" kvattn_status kvattn_decode_mla(const void* q_absorbed, const kvattn_cache* cache,

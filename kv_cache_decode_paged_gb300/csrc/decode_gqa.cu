@@ -41,6 +41,8 @@ struct GqaParams {
   float* part_out;
   float* part_lse;
   int B, h, hkv, g, bs, max_blocks;
+  int qlen;   // new tokens per sequence (1: plain decode)
+  int rows;   // rows per unit: qlen * g, ordered (token j, head in group)
   int64_t num_blocks;
   float qk_scale_log2;  // softmax scale * log2(e), times k_scale for FP8
   float v_mult;         // 1, or v_scale for FP8
@@ -96,6 +98,13 @@ KV_DEVI void e4m3_b02_b13(uint32_t w, uint32_t& b02, uint32_t& b13) {
 template <int BOX_BYTES>
 KV_DEVI uint32_t swz(int r, int c) {
   return (c >> 3) * BOX_BYTES + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// Row r of unit (b, kvh) is query token j = r / g (at position s_b - qlen + j)
+// and head kvh * g + r % g; its index among the [B][qlen][h] q, out and lse rows.
+KV_DEVI int64_t unit_row(const GqaParams& p, int b, int kvh, int r) {
+  const int j = r / p.g, i = r - j * p.g;
+  return (int64_t(b) * p.qlen + j) * p.h + kvh * p.g + i;
 }
 
 template <int D, int MT, bool FP8>
@@ -220,15 +229,18 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
   uint32_t it = 0;
   bool ok = true;
   while (w.next(sg)) {
-    const int hbase = sg.kvh * p.g;
     const int hl0 = 16 * mt + r0, hl1 = hl0 + 8;
+    // Causal limit among the new tokens: row hl's token sees the first
+    // len - (qlen - 1 - j) cached tokens (all of them when qlen = 1).
+    const int back0 = p.qlen - 1 - min(hl0, p.rows - 1) / p.g;
+    const int back1 = p.qlen - 1 - min(hl1, p.rows - 1) / p.g;
     uint32_t qa[NKS][4];
     {
       const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-          p.q + (int64_t(sg.b) * p.h + hbase + min(hl0, p.g - 1)) * D);
+          p.q + unit_row(p, sg.b, sg.kvh, min(hl0, p.rows - 1)) * D);
       const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-          p.q + (int64_t(sg.b) * p.h + hbase + min(hl1, p.g - 1)) * D);
-      const bool v0 = hl0 < p.g, v1 = hl1 < p.g;
+          p.q + unit_row(p, sg.b, sg.kvh, min(hl1, p.rows - 1)) * D);
+      const bool v0 = hl0 < p.rows, v1 = hl1 < p.rows;
       if constexpr (!FP8) {
 #pragma unroll
         for (int ks = 0; ks < NKS; ++ks) {
@@ -311,7 +323,8 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int tok = nt * 8 + 2 * tig + (i & 1);
-            sc[nt][i] = tok < valid ? acc[nt][i] * p.qk_scale_log2 : -INFINITY;
+            sc[nt][i] = tok < valid - (i < 2 ? back0 : back1) ? acc[nt][i] * p.qk_scale_log2
+                                                              : -INFINITY;
           }
         float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
         float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
@@ -339,13 +352,17 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
             o[i][3] *= c1;
           }
         }
+        // a row that has seen no token yet (possible only for an early new
+        // token in a later part of its sequence) keeps m = -inf: its scores
+        // here are all -inf too, and must give p = 0, not exp2(NaN)
+        const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
         float pr[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          pr[nt][0] = exp2_approx(sc[nt][0] - m0);
-          pr[nt][1] = exp2_approx(sc[nt][1] - m0);
-          pr[nt][2] = exp2_approx(sc[nt][2] - m1);
-          pr[nt][3] = exp2_approx(sc[nt][3] - m1);
+          pr[nt][0] = exp2_approx(sc[nt][0] - mu0);
+          pr[nt][1] = exp2_approx(sc[nt][1] - mu0);
+          pr[nt][2] = exp2_approx(sc[nt][2] - mu1);
+          pr[nt][3] = exp2_approx(sc[nt][3] - mu1);
         }
         l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
         l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
@@ -457,24 +474,21 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
     }
     named_bar_sync(1, C::NC * 32);
     {
-      const int64_t unit = int64_t(sg.b) * p.hkv + sg.kvh;
-      float* dst_o;
-      float* dst_l;
-      if (sg.full) {
-        dst_o = p.out + (int64_t(sg.b) * p.h + hbase) * D;
-        dst_l = p.lse + int64_t(sg.b) * p.h + hbase;
-      } else {
-        const int64_t slot = unit + c;
-        dst_o = p.part_out + slot * p.g * D;
-        dst_l = p.part_lse + slot * p.g;
-      }
+      // Row hl goes to its [B][qlen][h] row when the segment is the whole
+      // unit, else to row hl of this CTA's partial slot (slot u + c).
+      const int64_t slot = int64_t(sg.b) * p.hkv + sg.kvh + c;
+      auto out_row = [&](int hl) {
+        return sg.full ? unit_row(p, sg.b, sg.kvh, hl) : slot * p.rows + hl;
+      };
+      float* dst_o = sg.full ? p.out : p.part_out;
+      float* dst_l = sg.full ? p.lse : p.part_lse;
       constexpr int V4 = D / 4;
       for (int idx = ctid; idx < MT * 16 * V4; idx += C::NC * 32) {
         const int mt2 = idx / (16 * V4);
         const int rem = idx - mt2 * 16 * V4;
         const int row = rem / V4, c4 = rem - row * V4;
         const int hl = 16 * mt2 + row;
-        if (hl >= p.g) continue;
+        if (hl >= p.rows) continue;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int sidx = 0; sidx < C::NSTREAM; ++sidx) {
@@ -491,19 +505,19 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
           acc.z *= p.v_mult;
           acc.w *= p.v_mult;
         }
-        reinterpret_cast<float4*>(dst_o + int64_t(hl) * D)[c4] = acc;
+        reinterpret_cast<float4*>(dst_o + out_row(hl) * D)[c4] = acc;
       }
       if (ctid < MT * 16) {
         const int mt2 = ctid >> 4, row = ctid & 15;
         const int hl = 16 * mt2 + row;
-        if (hl < p.g) {
+        if (hl < p.rows) {
           float M = -INFINITY, L = 0.f;
           for (int sidx = 0; sidx < C::NSTREAM; ++sidx) M = fmaxf(M, ms[(sidx * MT + mt2) * 16 + row]);
           for (int sidx = 0; sidx < C::NSTREAM; ++sidx) {
             const float a = ms[(sidx * MT + mt2) * 16 + row];
             if (a != -INFINITY) L += ls[(sidx * MT + mt2) * 16 + row] * exp2_approx(a - M);
           }
-          dst_l[hl] = (M == -INFINITY || !(L > 0.f)) ? -INFINITY : (M + log2_approx(L)) * kLn2;
+          dst_l[out_row(hl)] = (M == -INFINITY || !(L > 0.f)) ? -INFINITY : (M + log2_approx(L)) * kLn2;
         }
       }
     }
@@ -555,11 +569,12 @@ static kvattn_status launch_variant(const GqaArgs& a, const GqaParams& prm, int 
              : KVATTN_ERR_CUDA;
 }
 
+// m-tiles of 16 rows: a unit's rows are q_len tokens x g heads (<= 64)
 template <int D, bool FP8>
 static kvattn_status dispatch_mt(const GqaArgs& a, const GqaParams& prm, int G) {
-  const int g = a.h / a.h_kv;
-  if (g <= 16) return launch_variant<D, 1, FP8>(a, prm, G);
-  if (g <= 32) return launch_variant<D, 2, FP8>(a, prm, G);
+  const int rows = prm.rows;
+  if (rows <= 16) return launch_variant<D, 1, FP8>(a, prm, G);
+  if (rows <= 32) return launch_variant<D, 2, FP8>(a, prm, G);
   return launch_variant<D, 4, FP8>(a, prm, G);
 }
 
@@ -581,11 +596,13 @@ int gqa_default_ctas(int dtype, int h, int h_kv, int d) {
 kvattn_status run_decode_gqa(const GqaArgs& a) {
   const kvattn_cache* cc = a.cache;
   const bool fp8 = cc->dtype == KVATTN_FP8_E4M3;
-  int G = a.G > 0 ? a.G : gqa_default_ctas(cc->dtype, a.h, a.h_kv, a.d);
+  const int qlen = a.qlen > 0 ? a.qlen : 1;
+  int G = a.G > 0 ? a.G : gqa_default_ctas(cc->dtype, a.h * qlen, a.h_kv, a.d);
   if (G <= 0) return KVATTN_ERR_CUDA;
   const int units = a.B * a.h_kv;
   const int g = a.h / a.h_kv;
-  const WsLayout L = ws_layout(a.B, units, G, g, a.d);
+  const int rows = qlen * g;
+  const WsLayout L = ws_layout(a.B, units, G, rows, a.d);
   if (!a.workspace || a.ws_bytes < L.total || (reinterpret_cast<uintptr_t>(a.workspace) & 255))
     return KVATTN_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -604,7 +621,7 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   pa.arrive = nullptr;   // merged by the combine kernel
   pa.out = nullptr;
   pa.lse = nullptr;
-  pa.rows = g;
+  pa.rows = rows;
   pa.dv = a.d;
   pa.err = a.err;
   if (launch_plan(pa, a.stream) != cudaSuccess) return KVATTN_ERR_CUDA;
@@ -623,6 +640,8 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   prm.h = a.h;
   prm.hkv = a.h_kv;
   prm.g = g;
+  prm.qlen = qlen;
+  prm.rows = rows;
   prm.bs = cc->block_size;
   prm.max_blocks = a.max_blocks;
   prm.num_blocks = cc->num_blocks;
@@ -641,8 +660,8 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   // With at most a few CTAs per unit on average (G + units <= 4 units), each
   // split unit's merge is a handful of loads: one warp per row suffices.
   const bool few = int64_t(G) + units <= 4 * int64_t(units);
-  if (launch_combine(prm.part_out, prm.part_lse, pa.split_first, pa.split_count, units, g, a.d,
-                     a.out, a.lse, true, a.stream, few) != cudaSuccess)
+  if (launch_combine(prm.part_out, prm.part_lse, pa.split_first, pa.split_count, units, rows, a.d,
+                     a.out, a.lse, true, a.stream, few, g, a.h_kv, qlen) != cudaSuccess)
     return KVATTN_ERR_CUDA;
   return KVATTN_OK;
 }

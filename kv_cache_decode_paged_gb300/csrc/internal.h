@@ -100,10 +100,13 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 // Merge split units' partials.  few_splits picks one warp per (unit, row)
 // (units split a handful of ways); otherwise a block per (unit, row) spreads
-// the splits over its warps.
+// the splits over its warps.  A unit's rows are qlen tokens x g heads of one
+// of hkv KV heads of a sequence; the final rows are [sequence][token][hkv * g]
+// (g = 0: g = rows, hkv = qlen = 1, unit-major rows).
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
                            const int32_t* count, int n_units, int rows, int dv, float* out,
-                           float* lse, bool skip_single, cudaStream_t s, bool few_splits = false);
+                           float* lse, bool skip_single, cudaStream_t s, bool few_splits = false,
+                           int g = 0, int hkv = 1, int qlen = 1);
 
 // Number of SMs of the current device (cached per device), or -1.
 int device_sm_count();
@@ -120,6 +123,7 @@ struct GqaArgs {
   const int32_t* block_table;
   const int32_t* seq_lens;
   int B, max_blocks, h, h_kv, d;
+  int qlen;   // new tokens per sequence (1: plain decode)
   float scale;
   float* out;
   float* lse;

@@ -181,6 +181,18 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t s) {
 // skip_single leaves units with one split alone (the decode kernel already
 // wrote their rows).
 constexpr int kCombineThreads = 256;
+
+// Where row r of unit u goes.  Units are (sequence, KV head) pairs with hkv
+// per sequence; a unit's rows are (new token j, head in group): q_len tokens x
+// g heads.  The final rows are laid out [sequence][token][hkv * g heads], so
+// with q_len = 1 (or hkv = 1, g = rows) this is simply u * rows + r.
+struct RowMap {
+  int g, hkv, qlen;
+  __device__ __forceinline__ int64_t operator()(int u, int r) const {
+    const int b = u / hkv, kvh = u - b * hkv, j = r / g, i = r - j * g;
+    return (int64_t(b) * qlen + j) * (int64_t(hkv) * g) + int64_t(kvh) * g + i;
+  }
+};
 constexpr int kCombineWarps = kCombineThreads / 32;
 constexpr int kCombineMaxCols = 4;   // float4 columns per lane: dv <= 512
 
@@ -188,7 +200,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse,
                    const int32_t* __restrict__ first, const int32_t* __restrict__ count,
                    int rows, int dv, float* __restrict__ out, float* __restrict__ lse,
-                   int skip_single) {
+                   int skip_single, RowMap map) {
   // skip_single is set only behind this library's decode kernels, whose split
   // counts were written before the decode started (its own dependency wait
   // precedes its trigger): then they are read before waiting for the decode,
@@ -243,10 +255,11 @@ __global__ void __launch_bounds__(kCombineThreads)
   float M = -INFINITY;
 #pragma unroll
   for (int i = 0; i < kCombineWarps; ++i) M = fmaxf(M, s_m[i]);
-  float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
+  const int64_t orow_i = map(u, r);
+  float4* orow = reinterpret_cast<float4*>(out + orow_i * dv);
   if (M == -INFINITY) {  // no split saw a valid token for this row
     for (int c = tid; c < v4; c += kCombineThreads) orow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (tid == 0) lse[size_t(u) * rows + r] = -INFINITY;
+    if (tid == 0) lse[orow_i] = -INFINITY;
     return;
   }
   float sc[kCombineWarps];
@@ -269,7 +282,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     }
     orow[c] = make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv);
   }
-  if (tid == 0) lse[size_t(u) * rows + r] = (M + log2_approx(L)) * kLn2;
+  if (tid == 0) lse[orow_i] = (M + log2_approx(L)) * kLn2;
 }
 
 // The same merge with one warp per (unit, row) and eight rows per block, for
@@ -279,7 +292,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     combine_rows_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse,
                         const int32_t* __restrict__ first, const int32_t* __restrict__ count,
                         int64_t n_items, int rows, int dv, float* __restrict__ out,
-                        float* __restrict__ lse, int skip_single) {
+                        float* __restrict__ lse, int skip_single, RowMap map) {
   const int lane = threadIdx.x & 31;
   const int64_t item = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
   // as in combine_kernel: behind a decode kernel the split counts are read
@@ -312,16 +325,20 @@ __global__ void __launch_bounds__(kCombineThreads)
     acc.w = acc.w * a + e * v.w;
     m = mn;
   }
-  float4* orow = reinterpret_cast<float4*>(out + (size_t(u) * rows + r) * dv);
+  const int64_t orow_i = map(u, r);
+  float4* orow = reinterpret_cast<float4*>(out + orow_i * dv);
   const float inv = m == -INFINITY ? 0.f : 1.f / l;   // no valid token: zeros, lse -inf
   if (col) orow[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lane == 0) lse[size_t(u) * rows + r] = m == -INFINITY ? -INFINITY : (m + log2_approx(l)) * kLn2;
+  if (lane == 0) lse[orow_i] = m == -INFINITY ? -INFINITY : (m + log2_approx(l)) * kLn2;
 }
 
 cudaError_t launch_combine(const float* part_out, const float* part_lse, const int32_t* first,
                            const int32_t* count, int n_units, int rows, int dv, float* out,
-                           float* lse, bool skip_single, cudaStream_t s, bool few_splits) {
+                           float* lse, bool skip_single, cudaStream_t s, bool few_splits,
+                           int g, int hkv, int qlen) {
   if (n_units <= 0 || rows <= 0) return cudaSuccess;
+  RowMap map{g > 0 ? g : rows, hkv > 0 ? hkv : 1, qlen > 0 ? qlen : 1};
+  if (int64_t(map.g) * map.qlen != rows) return cudaErrorInvalidValue;
   if (dv > 4 * 32 * kCombineMaxCols) return cudaErrorInvalidValue;
   const int64_t items = int64_t(n_units) * rows;
   if (few_splits && dv <= 128) {
@@ -329,11 +346,11 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     return launch_pdl(combine_rows_kernel, dim3(unsigned(blocks)), dim3(kCombineThreads), 0, s,
                       part_out, part_lse, first, count, items, rows, dv, out, lse,
-                      skip_single ? 1 : 0);
+                      skip_single ? 1 : 0, map);
   }
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
   return launch_pdl(combine_kernel, dim3(unsigned(items)), dim3(kCombineThreads), 0, s, part_out,
-                    part_lse, first, count, rows, dv, out, lse, skip_single ? 1 : 0);
+                    part_lse, first, count, rows, dv, out, lse, skip_single ? 1 : 0, map);
 }
 
 // ---- device queries -----------------------------------------------------------

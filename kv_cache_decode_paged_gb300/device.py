@@ -88,6 +88,24 @@ class GpuWorkload:
         torch.cuda.synchronize()
         return out.cpu().numpy(), lse.cpu().numpy()
 
+    def decode_multi(self, q_multi, num_ctas=0, ws=None):
+        """Multi-token decode of q_multi [B][q_len][h][d] (bf16 bits or a device
+        tensor): returns out [B][q_len][h][d], lse [B][q_len][h]."""
+        import torch
+        from . import kvattn_decode_gqa_multi
+        wl = self.wl
+        q = q_multi if isinstance(q_multi, torch.Tensor) else dev_bits(q_multi, self.device)
+        q_len = int(q.shape[1])
+        if ws is None:
+            ws = workspace_for(KVATTN_GQA, wl.B, wl.h * q_len, wl.h_kv, wl.d, num_ctas, self.device)
+        out = torch.empty((wl.B, q_len, wl.h, wl.d), dtype=torch.float32, device=self.device)
+        lse = torch.empty((wl.B, q_len, wl.h), dtype=torch.float32, device=self.device)
+        kvattn_decode_gqa_multi(q, self.cache.descriptor(), self.bt, self.seq_lens, q_len, wl.h,
+                                wl.h_kv, wl.d, wl.scale, out, lse, ws, num_ctas=num_ctas,
+                                err=self.err)
+        torch.cuda.synchronize()
+        return out.cpu().numpy(), lse.cpu().numpy()
+
     def err_bits(self) -> int:
         return int(self.err.item())
 

@@ -250,6 +250,17 @@ def make_workload(name: str, seed: int = 0, batch: Optional[int] = None,
     return wl
 
 
+def multi_token_queries(wl: Workload, q_len: int, seed: int = 0) -> np.ndarray:
+    """Queries of q_len new tokens per sequence for a GQA workload (speculative
+    verification): [B][q_len][h][d] bf16 bits, drawn like the single-token q.
+    The new tokens are the last q_len cached tokens of each sequence."""
+    assert wl.kind == "gqa"
+    r = WORKLOADS[wl.name]
+    n = wl.B * q_len * wl.h * wl.d
+    return normal_bf16(rng_for(seed, f"q_multi{q_len}"), n, r["q_std"]).reshape(
+        wl.B, q_len, wl.h, wl.d)
+
+
 def plant_needle(wl: Workload, b: int, head: int, t: int, strength: float = 30.0):
     """Overwrite K[t] of sequence b (the KV head that ``head`` reads) with
     ``strength * q/|q|`` so that one key dominates the softmax of that head."""

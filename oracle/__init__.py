@@ -201,6 +201,28 @@ def gqa_decode(q_bf16, k, v, scale, fmt=FMT_BF16, k_scale=1.0, v_scale=1.0):
     return out, lse
 
 
+def gqa_decode_multi(q_bf16, k, v, scale, fmt=FMT_BF16, k_scale=1.0, v_scale=1.0):
+    """q_len new tokens of one sequence, causal among themselves (speculative
+    verification: "MLA：为什么一份 Latent 可以代替多头 KV Cache", section
+    "正确性验证应该从两种实现互证", item 5).  q [q_len, h, d] bf16 bits; k, v
+    [s, h_kv, d] hold every cached token, the new ones last.  Token j sits at
+    position s - q_len + j and attends to positions [0, s - q_len + j]: its row
+    is the single-token decode over that prefix.  A token whose position would
+    be negative sees nothing (out 0, lse -inf).  Returns (out [q_len, h, d],
+    lse [q_len, h]) float64."""
+    q = np.asarray(q_bf16)
+    q_len, h, d = q.shape
+    s = np.asarray(k).shape[0]
+    out = np.zeros((q_len, h, d), dtype=np.float64)
+    lse = np.full((q_len, h), -np.inf, dtype=np.float64)
+    for j in range(q_len):
+        n = s - q_len + j + 1
+        if n > 0:
+            out[j], lse[j] = gqa_decode(q[j], np.asarray(k)[:n], np.asarray(v)[:n], scale, fmt,
+                                        k_scale, v_scale)
+    return out, lse
+
+
 def mla_decode(q, rows, d_c, scale, fmt=FMT_BF16):
     """One sequence: q [h, d_c + d_rope], rows [s, d_c + d_rope] (bf16 bits or
     float64).  Returns (out [h, d_c], lse [h]) float64."""

@@ -63,3 +63,19 @@ def assert_parity(out, lse, ref_out: dict, ref_lse: dict, fp8=False):
     if fin.any():
         assert np.abs(gl[fin] - rl[fin]).max() <= TOL_LSE
     return max_abs, rel
+
+
+def oracle_multi(oracle, wl: inputs.Workload, qm: np.ndarray, seqs=None):
+    """Oracle rows of a multi-token decode: qm [B][q_len][h][d] bf16 bits."""
+    seqs = range(wl.B) if seqs is None else seqs
+    outs, lses = {}, {}
+    for b in seqs:
+        sl = wl.seq_slice(b)
+        if wl.kv_dtype == "fp8":
+            kc = oracle.quantize_e4m3(wl.k[sl], wl.k_scale)
+            vc = oracle.quantize_e4m3(wl.v[sl], wl.v_scale)
+            outs[b], lses[b] = oracle.gqa_decode_multi(qm[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
+                                                       k_scale=wl.k_scale, v_scale=wl.v_scale)
+        else:
+            outs[b], lses[b] = oracle.gqa_decode_multi(qm[b], wl.k[sl], wl.v[sl], wl.scale)
+    return outs, lses

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert kv.kvattn_abi_version() == 1
+    assert kv.kvattn_abi_version() == 2
 
 
 def test_struct_layout():

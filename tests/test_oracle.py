@@ -165,6 +165,38 @@ def test_gqa_decode_matches_torch_sdpa(oracle, h, h_kv, d, s):
     np.testing.assert_allclose(lse, ref_l, rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("h,h_kv,d,s,q_len", [(4, 2, 16, 9, 3), (8, 1, 8, 5, 5), (2, 2, 32, 3, 4)])
+def test_gqa_multi_token_matches_causal_sdpa(oracle, h, h_kv, d, s, q_len):
+    # q_len new tokens, the last q_len of s cached: torch SDPA over all s keys
+    # with the causal mask of the new tokens (token j sees positions
+    # <= s - q_len + j) -- one matrix call, not the oracle's per-token prefixes.
+    # (2, 2, 32, 3, 4): the first new token's position is negative -> empty row.
+    rng = np.random.default_rng(h * 1000 + s * 10 + q_len)
+    q = inputs.bf16_bits(rng.standard_normal((q_len, h, d)).astype(np.float32))
+    k = inputs.bf16_bits(rng.standard_normal((s, h_kv, d)).astype(np.float32))
+    v = inputs.bf16_bits(rng.standard_normal((s, h_kv, d)).astype(np.float32))
+    scale = 1 / math.sqrt(d)
+    out, lse = oracle.gqa_decode_multi(q, k, v, scale)
+    f = lambda a: torch.from_numpy(inputs.bf16_to_f32(a).astype(np.float64))
+    qt = f(q).permute(1, 0, 2)[None]                        # [1, h, q_len, d]
+    kt = f(k).permute(1, 0, 2)[None].repeat_interleave(h // h_kv, dim=1)   # [1, h, s, d]
+    vt = f(v).permute(1, 0, 2)[None].repeat_interleave(h // h_kv, dim=1)
+    pos = torch.arange(s)[None, :]
+    limit = (s - q_len + torch.arange(q_len))[:, None]
+    mask = pos <= limit                                      # [q_len, s]
+    logits = torch.einsum("bhqd,bhsd->bhqs", qt, kt) * scale
+    logits = logits.masked_fill(~mask, float("-inf"))
+    for j in range(q_len):
+        if limit[j, 0] < 0:
+            assert (out[j] == 0).all() and np.isneginf(lse[j]).all()
+            continue
+        p = torch.softmax(logits[0, :, j], dim=-1)          # [h, s]
+        ref = torch.einsum("hs,hsd->hd", p, vt[0]).numpy()
+        np.testing.assert_allclose(out[j], ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse[j], torch.logsumexp(logits[0, :, j], dim=-1).numpy(),
+                                   rtol=1e-12, atol=1e-13)
+
+
 def test_gqa_g1_is_mha_head_by_head(oracle):
     # g = 1: each head is its own single-head attention
     rng = np.random.default_rng(7)
