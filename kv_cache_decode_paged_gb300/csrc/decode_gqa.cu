@@ -102,12 +102,17 @@ KV_DEVI uint32_t swz(int r, int c) {
 
 // Row r of unit (b, kvh) is query token j = r / g (at position s_b - qlen + j)
 // and head kvh * g + r % g; its index among the [B][qlen][h] q, out and lse rows.
+// MQ = false is the single-token form (qlen = 1, r < g).
+template <bool MQ>
 KV_DEVI int64_t unit_row(const GqaParams& p, int b, int kvh, int r) {
+  if constexpr (!MQ) return int64_t(b) * p.h + kvh * p.g + r;
   const int j = r / p.g, i = r - j * p.g;
   return (int64_t(b) * p.qlen + j) * p.h + kvh * p.g + i;
 }
 
-template <int D, int MT, bool FP8>
+// MQ: several new tokens per sequence (qlen > 1), causal among themselves.
+// The single-token instantiation carries none of the causal-limit work.
+template <int D, int MT, bool FP8, bool MQ>
 __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
@@ -232,14 +237,14 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
     const int hl0 = 16 * mt + r0, hl1 = hl0 + 8;
     // Causal limit among the new tokens: row hl's token sees the first
     // len - (qlen - 1 - j) cached tokens (all of them when qlen = 1).
-    const int back0 = p.qlen - 1 - min(hl0, p.rows - 1) / p.g;
-    const int back1 = p.qlen - 1 - min(hl1, p.rows - 1) / p.g;
+    const int back0 = MQ ? p.qlen - 1 - min(hl0, p.rows - 1) / p.g : 0;
+    const int back1 = MQ ? p.qlen - 1 - min(hl1, p.rows - 1) / p.g : 0;
     uint32_t qa[NKS][4];
     {
       const uint32_t* q0 = reinterpret_cast<const uint32_t*>(
-          p.q + unit_row(p, sg.b, sg.kvh, min(hl0, p.rows - 1)) * D);
+          p.q + unit_row<MQ>(p, sg.b, sg.kvh, min(hl0, p.rows - 1)) * D);
       const uint32_t* q1 = reinterpret_cast<const uint32_t*>(
-          p.q + unit_row(p, sg.b, sg.kvh, min(hl1, p.rows - 1)) * D);
+          p.q + unit_row<MQ>(p, sg.b, sg.kvh, min(hl1, p.rows - 1)) * D);
       const bool v0 = hl0 < p.rows, v1 = hl1 < p.rows;
       if constexpr (!FP8) {
 #pragma unroll
@@ -355,7 +360,8 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
         // a row that has seen no token yet (possible only for an early new
         // token in a later part of its sequence) keeps m = -inf: its scores
         // here are all -inf too, and must give p = 0, not exp2(NaN)
-        const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+        const float mu0 = MQ && m0 == -INFINITY ? 0.f : m0;
+        const float mu1 = MQ && m1 == -INFINITY ? 0.f : m1;
         float pr[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -478,7 +484,7 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
       // unit, else to row hl of this CTA's partial slot (slot u + c).
       const int64_t slot = int64_t(sg.b) * p.hkv + sg.kvh + c;
       auto out_row = [&](int hl) {
-        return sg.full ? unit_row(p, sg.b, sg.kvh, hl) : slot * p.rows + hl;
+        return sg.full ? unit_row<MQ>(p, sg.b, sg.kvh, hl) : slot * p.rows + hl;
       };
       float* dst_o = sg.full ? p.out : p.part_out;
       float* dst_l = sg.full ? p.lse : p.part_lse;
@@ -538,10 +544,13 @@ static int occupancy_ctas() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   std::call_once(flags[dev], [dev] {
     int n = 0;
-    cudaFuncSetAttribute(gqa_decode_kernel<D, MT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         C::SMEM);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<D, MT, FP8>, C::THREADS,
-                                                      C::SMEM) != cudaSuccess)
+    // both forms share the configuration; the attribute is set on each
+    cudaFuncSetAttribute(gqa_decode_kernel<D, MT, FP8, true>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaFuncSetAttribute(gqa_decode_kernel<D, MT, FP8, false>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_decode_kernel<D, MT, FP8, false>,
+                                                      C::THREADS, C::SMEM) != cudaSuccess)
       n = 0;
     int sms = device_sm_count();
     cache[dev] = (n > 0 && sms > 0) ? n * sms : -1;
@@ -549,7 +558,7 @@ static int occupancy_ctas() {
   return cache[dev];
 }
 
-template <int D, int MT, bool FP8>
+template <int D, int MT, bool FP8, bool MQ>
 static kvattn_status launch_variant(const GqaArgs& a, const GqaParams& prm, int G) {
   using C = GqaCfg<D, MT, FP8>;
   if (occupancy_ctas<D, MT, FP8>() <= 0) return KVATTN_ERR_CUDA;  // also sets the smem attribute
@@ -563,19 +572,25 @@ static kvattn_status launch_variant(const GqaArgs& a, const GqaParams& prm, int 
   if (!encode_tensor_map_3d(&tmK, dt, cc->k, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tensor_map_3d(&tmV, dt, cc->v, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return KVATTN_ERR_CUDA;
-  return launch_pdl(gqa_decode_kernel<D, MT, FP8>, dim3(G), dim3(C::THREADS), C::SMEM, a.stream,
+  return launch_pdl(gqa_decode_kernel<D, MT, FP8, MQ>, dim3(G), dim3(C::THREADS), C::SMEM, a.stream,
                     tmK, tmV, prm) == cudaSuccess
              ? KVATTN_OK
              : KVATTN_ERR_CUDA;
 }
 
 // m-tiles of 16 rows: a unit's rows are q_len tokens x g heads (<= 64)
+template <int D, bool FP8, bool MQ>
+static kvattn_status dispatch_rows(const GqaArgs& a, const GqaParams& prm, int G) {
+  const int rows = prm.rows;
+  if (rows <= 16) return launch_variant<D, 1, FP8, MQ>(a, prm, G);
+  if (rows <= 32) return launch_variant<D, 2, FP8, MQ>(a, prm, G);
+  return launch_variant<D, 4, FP8, MQ>(a, prm, G);
+}
+
 template <int D, bool FP8>
 static kvattn_status dispatch_mt(const GqaArgs& a, const GqaParams& prm, int G) {
-  const int rows = prm.rows;
-  if (rows <= 16) return launch_variant<D, 1, FP8>(a, prm, G);
-  if (rows <= 32) return launch_variant<D, 2, FP8>(a, prm, G);
-  return launch_variant<D, 4, FP8>(a, prm, G);
+  return prm.qlen > 1 ? dispatch_rows<D, FP8, true>(a, prm, G)
+                      : dispatch_rows<D, FP8, false>(a, prm, G);
 }
 
 template <int D, bool FP8>
