@@ -10,6 +10,7 @@ larger than L2, so every step streams the KV cache from HBM.
   python bench.py [--config llama3_8b] [--steps K] [--warmup W]
   python bench.py --impl reference      # the float64 CPU oracle on a bounded sample
   python bench.py --config llama3_70b --q-len 4   # 4 new tokens per sequence (GQA)
+  python bench.py --config deepseek_v3_mla --absorb  # + query absorption, value up-projection
   torchrun --nproc-per-node N bench.py --gpus N   # N independent replicas
 
 Metric: decode-attention KV-read GB/s (algorithmic KV bytes of a step / step
@@ -19,6 +20,10 @@ With --q-len L > 1 (GQA only) a step appends the last L tokens of every
 sequence and runs the multi-token decode: L queries per sequence, causal among
 the new tokens (speculative verification).  The KV bytes read are the same as
 for one token; the work per byte is L times larger.
+
+With --absorb (MLA only) a step also runs the per-head projections around
+the decode: W_UK^T q^C before it (writing the absorbed query) and W_UV u~
+after it, with random bf16 weights of DeepSeek-V3's shapes.
 """
 from __future__ import annotations
 
@@ -57,6 +62,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (GQA; > 1 runs the multi-token decode)")
+    ap.add_argument("--absorb", action="store_true",
+                    help="MLA: add query absorption and value up-projection to every step")
     return ap.parse_args()
 
 
@@ -171,6 +178,9 @@ def config_dict(wl, args):
     if args.q_len > 1:
         d["workload"] = f"{wl.name}, {args.q_len} new tokens per sequence"
         d["q_len"] = args.q_len
+    if args.absorb:
+        d["workload"] = f"{wl.name}, with query absorption and value up-projection"
+        d.update({"d_hc": 128, "d_v": 128, "weights": "random bf16 W_UK [h][128][512], W_UV [h][128][512]"})
     else:
         d.update({"d_c": wl.d_c, "d_rope": wl.d_rope})
     return d
@@ -235,6 +245,12 @@ def run_reference(args, wl, rank):
     budget_per_step = min(0.5, 120.0 / max(1, steps + warm))
     order = list(np.argsort(wl.seq_lens))[len(wl.seq_lens) // 2:] or [0]
     qm = multi_queries(args, wl)
+    pj = None
+    if args.absorb:
+        from kv_cache_decode_paged_gb300 import inputs
+        pj = inputs.mla_projections(wl.B, h=wl.h, d_c=wl.d_c, d_rope=wl.d_rope, seed=args.seed)
+        f64 = lambda bits: inputs.bf16_to_f32(bits).astype(np.float64)
+        w_uk, w_uv = f64(pj.w_uk), f64(pj.w_uv)
 
     def one(i, heads):
         b = int(order[i % len(order)])
@@ -242,7 +258,13 @@ def run_reference(args, wl, rank):
         if wl.kind == "mla":
             rows = np.concatenate([wl.c_kv[sl], wl.k_r[sl]], axis=1)
             hq = max(1, heads)
-            oracle.mla_decode(wl.q[b, :hq], rows, wl.d_c, wl.scale)
+            if pj is None:
+                oracle.mla_decode(wl.q[b, :hq], rows, wl.d_c, wl.scale)
+            else:   # absorb, decode, up-project the first hq heads
+                qa = np.concatenate([oracle.mla_absorb_query(f64(pj.q_nope[b, :hq]), w_uk[:hq]),
+                                     f64(pj.q_rope[b, :hq])], axis=1)
+                u, _ = oracle.mla_decode(qa, f64(rows), wl.d_c, wl.scale, fmt=oracle.FMT_F64)
+                oracle.mla_apply_wuv(u, w_uv[:hq])
             return int(wl.seq_lens[b]) * per_tok * hq / wl.h
         g = wl.g
         kw = {}
@@ -295,6 +317,7 @@ def run_ours(args, wl, rank, world, local):
     import torch
 
     import kv_cache_decode_paged_gb300 as kv
+    from kv_cache_decode_paged_gb300 import inputs
     from kv_cache_decode_paged_gb300.device import GpuWorkload, dev_bits
 
     torch.cuda.set_device(local)
@@ -337,6 +360,19 @@ def run_ours(args, wl, rank, world, local):
         q_dev = dev_bits(qm, dev)
     desc = g.cache.descriptor()
     stream = torch.cuda.current_stream()
+    launches = 4 if wl.kind == "gqa" else 3   # append, planner, decode (, combine)
+    proj = None
+    if args.absorb:
+        if wl.kind != "mla":
+            raise SystemExit("--absorb needs an MLA config")
+        pj = inputs.mla_projections(wl.B, h=wl.h, d_c=wl.d_c, d_rope=wl.d_rope, seed=args.seed)
+        proj = {"q_nope": dev_bits(pj.q_nope, dev), "q_rope": dev_bits(pj.q_rope, dev),
+                "w_uk": dev_bits(pj.w_uk, dev), "w_uv": dev_bits(pj.w_uv, dev),
+                "v": torch.empty((wl.B, wl.h, pj.w_uv.shape[1]), dtype=torch.float32, device=dev)}
+        launches += 2
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
 
     def decode():
         if qm is not None:
@@ -349,13 +385,26 @@ def run_ours(args, wl, rank, world, local):
             kv.kvattn_decode_mla(g.q, desc, g.bt, g.seq_lens, wl.h, wl.d_c, wl.d_rope, wl.scale,
                                  out, lse, ws, err=g.err, stream=stream)
 
-    def step(ev=None):
+    def step(ev=None, pe=None):
+        if proj is not None:
+            if pe is not None:
+                pe[0].record(stream)
+            kv.kvattn_mla_absorb_q(proj["q_nope"], proj["q_rope"], proj["w_uk"], g.q, err=g.err,
+                                   stream=stream)
+            if pe is not None:
+                pe[1].record(stream)
         kv.kvattn_append(desc, new0, new1, seq_idx, pos, g.bt, err=g.err, stream=stream)
         if ev is not None:
             ev[0].record(stream)
         decode()
         if ev is not None:
             ev[1].record(stream)
+        if proj is not None:
+            if pe is not None:
+                pe[2].record(stream)
+            kv.kvattn_mla_up_v(out, proj["w_uv"], proj["v"], err=g.err, stream=stream)
+            if pe is not None:
+                pe[3].record(stream)
 
     gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid).replace("GPU-", "")
     sampler = ClockSampler(gpu_id)
@@ -373,7 +422,7 @@ def run_ours(args, wl, rank, world, local):
     w0 = time.monotonic()
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step(evs[i], pev[i] if proj is not None else None)
     t_end.record(stream)
     torch.cuda.synchronize()
     w1 = time.monotonic()
@@ -392,25 +441,26 @@ def run_ours(args, wl, rank, world, local):
 
     # ---- end to end: host buffers in, result out, every step
     e2e_steps = args.e2e_steps or args.steps
-    h_q = torch.from_numpy(np.ascontiguousarray(wl.q if qm is None else qm).view(np.int16)).pin_memory()
-    h_new0 = new0.cpu().pin_memory()
-    h_new1 = new1.cpu().pin_memory()
-    h_pos = pos.cpu().pin_memory()
-    h_sl = g.seq_lens.cpu().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_new0, h_new1, h_pos, h_sl))
-    d2h = h_out.numel() * 4 + h_lse.numel() * 4
+    # (device tensor, pinned host copy) of every input a step reads and every
+    # result it returns
+    if proj is None:
+        dev_in = [q_dev]
+        dev_out = [out, lse]
+    else:   # the absorbed query is made on the device from q^C and q^R
+        dev_in = [proj["q_nope"], proj["q_rope"]]
+        dev_out = [proj["v"], lse]
+    dev_in += [new0, new1, pos, g.seq_lens]
+    h_in = [t.cpu().pin_memory() for t in dev_in]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
 
     def e2e_step():
-        q_dev.copy_(h_q, non_blocking=True)
-        new0.copy_(h_new0, non_blocking=True)
-        new1.copy_(h_new1, non_blocking=True)
-        pos.copy_(h_pos, non_blocking=True)
-        g.seq_lens.copy_(h_sl, non_blocking=True)
+        for d, hst in zip(dev_in, h_in):
+            d.copy_(hst, non_blocking=True)
         step()
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        for hst, d in zip(h_out, dev_out):
+            hst.copy_(d, non_blocking=True)
 
     for _ in range(max(3, args.warmup // 4)):
         e2e_step()
@@ -459,10 +509,23 @@ def run_ours(args, wl, rank, world, local):
         "e2e": {"value": kvb * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "device_err_bits": err_bits,
     }
+    if proj is not None:
+        a_us = statistics.mean(a.elapsed_time(b) for a, b, _, _ in pev) * 1e3
+        u_us = statistics.mean(c.elapsed_time(d) for _, _, c, d in pev) * 1e3
+        B, h = wl.B, wl.h
+        a_bytes = 2 * (h * 128 * wl.d_c + B * h * 128 + B * h * wl.d_rope + B * h * wl.d)
+        u_bytes = 2 * h * 128 * wl.d_c + 4 * B * h * wl.d_c + 4 * B * h * 128
+        flops = 2 * B * h * 128 * wl.d_c
+        line["projections"] = {
+            "absorb_q": {"us": a_us, "bytes": a_bytes, "gbs": a_bytes / a_us / 1e3,
+                         "frac_of_hbm": a_bytes / a_us / 1e3 / peak, "tflops": flops / a_us / 1e6},
+            "up_v": {"us": u_us, "bytes": u_bytes, "gbs": u_bytes / u_us / 1e3,
+                     "frac_of_hbm": u_bytes / u_us / 1e3 / peak, "tflops": flops / u_us / 1e6},
+            "note": "CUDA events around each launch; bytes = weights + activations read and written"}
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

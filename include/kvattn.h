@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define KVATTN_ABI_VERSION 2
+#define KVATTN_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define KVATTN_API __attribute__((visibility("default")))
@@ -221,6 +221,47 @@ KVATTN_API kvattn_status kvattn_decode_mla(const void* q_absorbed, const kvattn_
                                 int max_blocks_per_seq, int h, int d_c, int d_rope, float scale,
                                 float* out, float* lse, void* workspace, size_t workspace_bytes,
                                 int num_ctas, int32_t* err, void* stream);
+
+/* MLA query-side absorption ("MLA：为什么一份 Latent 可以代替多头 KV Cache" and
+ * "Multi-Head Latent Attention (MLA) ...", the absorbed query vector): for every
+ * batch row b and head i,
+ *   q_absorbed[b][i] = [ W_UK,i^T q^C[b][i]  |  q^R[b][i] ],
+ * the row kvattn_decode_mla takes.  W_UK,i maps a latent to head i's key
+ * (k^C = W_UK,i c), so its transpose takes the head's query into latent space.
+ *   q_nope:      device, [batch][h][d_hc] bf16 (q^C).
+ *   q_rope:      device, [batch][h][d_rope] bf16 (q^R, already rotated; may
+ *                be null when d_rope = 0).
+ *   w_uk:        device, [h][d_hc][d_c] bf16 (W_UK,i row-major, d_c fastest).
+ *   q_absorbed:  device, [batch][h][d_c + d_rope] bf16; the product is
+ *                accumulated in float32 and rounded to nearest even.
+ * Built for d_hc = 128, d_c a multiple of 256, d_rope a multiple of 8 with
+ * d_c + d_rope <= 4096, ceil(batch / 128) and h at most 65535
+ * (KVATTN_ERR_UNSUPPORTED otherwise).  All pointers 16-byte aligned
+ * (KVATTN_ERR_INVALID_ARG otherwise).  One kernel on `stream` (tcgen05
+ * tensor cores, one CTA per head, 128 batch rows and 256 latent columns);
+ * a bounded wait that gives up sets KVATTN_DEVERR_TIMEOUT in *err and leaves
+ * that CTA's rows unwritten. */
+KVATTN_API kvattn_status kvattn_mla_absorb_q(const void* q_nope, const void* q_rope,
+                                             const void* w_uk, int batch, int h, int d_hc,
+                                             int d_c, int d_rope, void* q_absorbed, int32_t* err,
+                                             void* stream);
+
+/* MLA deferred value up-projection (same pages: W_UV,i moves outside the
+ * probability-weighted sum over cached latents):
+ *   v[b][i] = W_UV,i u~[b][i]
+ * for the decode output u~ of kvattn_decode_mla.  W_O, which maps the
+ * concatenated heads to the model width, is a plain GEMM over all heads and
+ * is not part of this library.
+ *   u_tilde:  device, [batch][h][d_c] float32.
+ *   w_uv:     device, [h][d_v][d_c] bf16 (W_UV,i row-major, d_c fastest).
+ *   v:        device, [batch][h][d_v] float32.
+ * u~ is rounded to bf16 (nearest even) for the tensor cores; products are
+ * accumulated in float32.  Built for d_v = 128 and d_c a multiple of 128 up
+ * to 65536, ceil(batch / 128) and h at most 65535 (KVATTN_ERR_UNSUPPORTED
+ * otherwise); pointers 16-byte aligned (KVATTN_ERR_INVALID_ARG otherwise).
+ * One kernel on `stream`; error behaviour as for kvattn_mla_absorb_q. */
+KVATTN_API kvattn_status kvattn_mla_up_v(const float* u_tilde, const void* w_uv, int batch, int h,
+                                         int d_c, int d_v, float* v, int32_t* err, void* stream);
 
 /* Split-KV log-sum-exp combine.
  *   Unit u owns split_count[u] consecutive partial slots starting at

@@ -37,7 +37,7 @@ EXPORTED = [
     "kvattn_status_string", "kvattn_abi_version", "kvattn_page_bytes", "kvattn_cell_bytes",
     "kvattn_append", "kvattn_decode_workspace_bytes", "kvattn_default_num_ctas",
     "kvattn_decode_gqa", "kvattn_decode_mla", "kvattn_combine", "kvattn_decode_gqa_noalloc",
-    "kvattn_decode_gqa_multi",
+    "kvattn_decode_gqa_multi", "kvattn_mla_absorb_q", "kvattn_mla_up_v",
 ]
 
 KVATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -99,6 +99,8 @@ def load_library(build: bool = True) -> ctypes.CDLL:
                                                 i32, P, P]),
             "kvattn_decode_gqa_multi": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, i32, f32, P,
                                               P, P, sz, i32, P, P]),
+            "kvattn_mla_absorb_q": (i32, [P, P, P, i32, i32, i32, i32, i32, P, P, P]),
+            "kvattn_mla_up_v": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -205,6 +207,26 @@ def kvattn_decode_mla(q_absorbed, cache: kvattn_cache, block_table, seq_lens, h,
         int(max_blocks), int(h), int(d_c), int(d_rope), float(scale), _ptr(out), _ptr(lse),
         _ptr(workspace), int(workspace.numel() * workspace.element_size()) if workspace is not None else 0,
         int(num_ctas), _ptr(err), _stream(stream)))
+
+
+def kvattn_mla_absorb_q(q_nope, q_rope, w_uk, q_absorbed, err=None, stream=None):
+    """q_nope [B][h][d_hc], q_rope [B][h][d_rope], w_uk [h][d_hc][d_c] (bf16 bits)
+    -> q_absorbed [B][h][d_c + d_rope] bf16 bits."""
+    batch, h, d_hc = q_nope.shape
+    d_c = int(w_uk.shape[2])
+    d_rope = int(q_rope.shape[2]) if q_rope is not None else 0
+    _check("kvattn_mla_absorb_q", load_library().kvattn_mla_absorb_q(
+        _ptr(q_nope), _ptr(q_rope), _ptr(w_uk), int(batch), int(h), int(d_hc), d_c, d_rope,
+        _ptr(q_absorbed), _ptr(err), _stream(stream)))
+
+
+def kvattn_mla_up_v(u_tilde, w_uv, v, err=None, stream=None):
+    """u_tilde [B][h][d_c] float32, w_uv [h][d_v][d_c] bf16 bits -> v [B][h][d_v] float32."""
+    batch, h, d_c = u_tilde.shape
+    d_v = int(w_uv.shape[1])
+    _check("kvattn_mla_up_v", load_library().kvattn_mla_up_v(
+        _ptr(u_tilde), _ptr(w_uv), int(batch), int(h), int(d_c), d_v, _ptr(v), _ptr(err),
+        _stream(stream)))
 
 
 def kvattn_combine(part_out, part_lse, split_first, split_count, rows_per_unit, dv, out, lse,

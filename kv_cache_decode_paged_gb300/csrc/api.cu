@@ -205,6 +205,56 @@ extern "C" kvattn_status kvattn_decode_mla(const void* q_absorbed, const kvattn_
   return run_decode_mla(a);
 }
 
+extern "C" kvattn_status kvattn_mla_absorb_q(const void* q_nope, const void* q_rope,
+                                            const void* w_uk, int batch, int h, int d_hc, int d_c,
+                                            int d_rope, void* q_absorbed, int32_t* err,
+                                            void* stream) {
+  if (batch < 0 || h <= 0 || d_hc <= 0 || d_c <= 0 || d_rope < 0) return KVATTN_ERR_INVALID_ARG;
+  if (batch == 0) return KVATTN_OK;
+  if (!q_nope || !w_uk || !q_absorbed || (d_rope > 0 && !q_rope)) return KVATTN_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(w_uk, 16) || !aligned(q_absorbed, 16) ||
+      (d_rope > 0 && !aligned(q_rope, 16)))
+    return KVATTN_ERR_INVALID_ARG;
+  // one K = 128 tile, 256-column N tiles, q^R copied in 16-byte pieces
+  if (d_hc != 128 || d_c % 256 || d_rope % 8 || d_c + d_rope > 4096) return KVATTN_ERR_UNSUPPORTED;
+  if ((int64_t(batch) + 127) / 128 > 65535 || h > 65535) return KVATTN_ERR_UNSUPPORTED;
+  AbsorbArgs a;
+  a.q_nope = q_nope;
+  a.q_rope = q_rope;
+  a.w_uk = w_uk;
+  a.B = batch;
+  a.h = h;
+  a.d_hc = d_hc;
+  a.d_c = d_c;
+  a.d_rope = d_rope;
+  a.q_abs = q_absorbed;
+  a.err = err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return run_mla_absorb_q(a);
+}
+
+extern "C" kvattn_status kvattn_mla_up_v(const float* u_tilde, const void* w_uv, int batch, int h,
+                                        int d_c, int d_v, float* v, int32_t* err, void* stream) {
+  if (batch < 0 || h <= 0 || d_c <= 0 || d_v <= 0) return KVATTN_ERR_INVALID_ARG;
+  if (batch == 0) return KVATTN_OK;
+  if (!u_tilde || !w_uv || !v) return KVATTN_ERR_INVALID_ARG;
+  if (!aligned(u_tilde, 16) || !aligned(w_uv, 16) || !aligned(v, 16)) return KVATTN_ERR_INVALID_ARG;
+  // N = d_v = 128 in one MMA, K = d_c in chunks of 128
+  if (d_v != 128 || d_c % 128 || d_c > 65536) return KVATTN_ERR_UNSUPPORTED;
+  if ((int64_t(batch) + 127) / 128 > 65535 || h > 65535) return KVATTN_ERR_UNSUPPORTED;
+  UpArgs a;
+  a.u = u_tilde;
+  a.w_uv = w_uv;
+  a.B = batch;
+  a.h = h;
+  a.d_c = d_c;
+  a.d_v = d_v;
+  a.v = v;
+  a.err = err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return run_mla_up_v(a);
+}
+
 extern "C" kvattn_status kvattn_combine(const float* part_out, const float* part_lse,
                                         const int32_t* split_first, const int32_t* split_count,
                                         int n_units, int rows_per_unit, int dv, float* out,

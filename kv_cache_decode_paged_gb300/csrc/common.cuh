@@ -137,6 +137,8 @@ KV_DEVI void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0, 
 KV_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every bulk store this thread committed has completed.
 KV_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Wait until every bulk store this thread committed has read its shared-memory source.
+KV_DEVI void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // 32-byte store of eight 32-bit values (address 32-byte aligned).
 KV_DEVI void st_global_v8(float* p, const uint32_t* v) {

@@ -154,4 +154,26 @@ struct MlaArgs {
 kvattn_status run_decode_mla(const MlaArgs& a);
 int mla_default_ctas(int h);
 
+// Per-head projections around MLA decode (absorb.cu).
+struct AbsorbArgs {
+  const void* q_nope;   // [B][h][d_hc] bf16
+  const void* q_rope;   // [B][h][d_rope] bf16
+  const void* w_uk;     // [h][d_hc][d_c] bf16
+  int B, h, d_hc, d_c, d_rope;
+  void* q_abs;          // [B][h][d_c + d_rope] bf16
+  int32_t* err;
+  cudaStream_t stream;
+};
+kvattn_status run_mla_absorb_q(const AbsorbArgs& a);
+
+struct UpArgs {
+  const float* u;       // [B][h][d_c] f32
+  const void* w_uv;     // [h][d_v][d_c] bf16
+  int B, h, d_c, d_v;
+  float* v;             // [B][h][d_v] f32
+  int32_t* err;
+  cudaStream_t stream;
+};
+kvattn_status run_mla_up_v(const UpArgs& a);
+
 }  // namespace kv

@@ -261,6 +261,28 @@ def multi_token_queries(wl: Workload, q_len: int, seed: int = 0) -> np.ndarray:
         wl.B, q_len, wl.h, wl.d)
 
 
+@dataclass
+class MlaProjections:
+    """Inputs of the per-head projections around MLA decode (bf16 bits)."""
+    q_nope: np.ndarray        # [B][h][d_hc]  q^C ~ N(0, 1)
+    q_rope: np.ndarray        # [B][h][d_rope] q^R ~ N(0, 1/(d_c + d_rope))
+    w_uk: np.ndarray          # [h][d_hc][d_c] ~ N(0, 1/(d_hc (d_c + d_rope)))
+    w_uv: np.ndarray          # [h][d_v][d_c] ~ N(0, 1/d_c)
+
+
+def mla_projections(B: int, h: int = 128, d_hc: int = 128, d_c: int = 512, d_rope: int = 64,
+                    d_v: int = 128, seed: int = 0) -> MlaProjections:
+    """Random weights and un-absorbed queries shaped like DeepSeek-V3's MLA.
+    The spreads make W_UK^T q^C ~ N(0, 1/(d_c + d_rope)), the spread of the
+    absorbed query in the MLA decode workload."""
+    w = d_c + d_rope
+    return MlaProjections(
+        q_nope=normal_bf16(rng_for(seed, "q_nope"), B * h * d_hc).reshape(B, h, d_hc),
+        q_rope=normal_bf16(rng_for(seed, "q_rope"), B * h * d_rope, w ** -0.5).reshape(B, h, d_rope),
+        w_uk=normal_bf16(rng_for(seed, "w_uk"), h * d_hc * d_c, (d_hc * w) ** -0.5).reshape(h, d_hc, d_c),
+        w_uv=normal_bf16(rng_for(seed, "w_uv"), h * d_v * d_c, d_c ** -0.5).reshape(h, d_v, d_c))
+
+
 def plant_needle(wl: Workload, b: int, head: int, t: int, strength: float = 30.0):
     """Overwrite K[t] of sequence b (the KV head that ``head`` reads) with
     ``strength * q/|q|`` so that one key dominates the softmax of that head."""

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert kv.kvattn_abi_version() == 2
+    assert kv.kvattn_abi_version() == 3
 
 
 def test_struct_layout():
@@ -140,3 +140,28 @@ def test_append_and_combine_validation(lib):
     assert lib.kvattn_combine(FAKE, FAKE, FAKE, FAKE, 3, 4, 6, FAKE, FAKE, None) == 1   # dv % 4
     assert lib.kvattn_combine(FAKE, FAKE, FAKE, FAKE, 0, 4, 8, FAKE, FAKE, None) == 0
     assert lib.kvattn_combine(FAKE, FAKE, FAKE, FAKE, 3, 4, 516, FAKE, FAKE, None) == 2  # dv > 512
+
+
+def test_projection_host_validation(lib):
+    # kvattn_mla_absorb_q(q_nope, q_rope, w_uk, batch, h, d_hc, d_c, d_rope, q_abs, err, stream)
+    absorb = lambda **kw: lib.kvattn_mla_absorb_q(
+        kw.get("q", FAKE), FAKE, FAKE, kw.get("batch", 64), kw.get("h", 128),
+        kw.get("d_hc", 128), kw.get("d_c", 512), kw.get("d_rope", 64), kw.get("out", FAKE),
+        None, None)
+    assert absorb(batch=0) == kv.KVATTN_OK
+    assert absorb(batch=-1) == kv.KVATTN_ERR_INVALID_ARG
+    assert absorb(q=None) == kv.KVATTN_ERR_INVALID_ARG
+    assert absorb(out=FAKE + 8) == kv.KVATTN_ERR_INVALID_ARG     # misaligned
+    assert absorb(d_hc=64) == kv.KVATTN_ERR_UNSUPPORTED
+    assert absorb(d_c=384) == kv.KVATTN_ERR_UNSUPPORTED          # not whole 256-column tiles
+    assert absorb(d_rope=60) == kv.KVATTN_ERR_UNSUPPORTED
+    assert absorb(batch=128 * 65535 + 1) == kv.KVATTN_ERR_UNSUPPORTED
+    # kvattn_mla_up_v(u, w_uv, batch, h, d_c, d_v, v, err, stream)
+    up = lambda **kw: lib.kvattn_mla_up_v(
+        kw.get("u", FAKE), FAKE, kw.get("batch", 64), kw.get("h", 128), kw.get("d_c", 512),
+        kw.get("d_v", 128), FAKE, None, None)
+    assert up(batch=0) == kv.KVATTN_OK
+    assert up(h=0) == kv.KVATTN_ERR_INVALID_ARG
+    assert up(u=None) == kv.KVATTN_ERR_INVALID_ARG
+    assert up(d_v=64) == kv.KVATTN_ERR_UNSUPPORTED
+    assert up(d_c=200) == kv.KVATTN_ERR_UNSUPPORTED
