@@ -294,8 +294,13 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
       if (valid > 0) {
         const uint32_t kb = smem_u32(stages + s * C::STAGE_BYTES);
         const uint32_t vb = kb + C::TILE_BYTES;
-        // S^T tile: 16 heads x 16 tokens, two n-tiles of 8 tokens
+        // S^T tile: 16 heads x 16 tokens, two n-tiles of 8 tokens.  The
+        // multi-token form runs every chunk through every consumer warp, so
+        // the latency of a chain of dependent MMAs sets its pace: it splits
+        // each n-tile's sum over K into two chains (acc2 takes every other
+        // K step) and adds them at the end.
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if constexpr (!FP8) {
 #pragma unroll
           for (int ks = 0; ks < NKS; ++ks) {
@@ -303,8 +308,9 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
             const int ch = 2 * ks + (lmat & 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kb + swz<C::BOX_BYTES>(tok, ch), b0, b1, b2, b3);
-            mma_bf16(acc[0], qa[ks], b0, b1);
-            mma_bf16(acc[1], qa[ks], b2, b3);
+            float(&a)[2][4] = MQ && (ks & 1) ? acc2 : acc;
+            mma_bf16(a[0], qa[ks], b0, b1);
+            mma_bf16(a[1], qa[ks], b2, b3);
           }
         } else {
           // K rows are 128 bytes = 8 chunks of 16 dims.  A b16 ldmatrix of
@@ -316,11 +322,18 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
             const int ch = 2 * cp + (lmat >> 1);
             uint32_t r0, r1, r2, r3;
             ldsm_x4(kb + swz<C::BOX_BYTES>(tok, ch), r0, r1, r2, r3);
+            float(&a)[2][4] = MQ ? acc2 : acc;
             mma_f16(acc[0], qa[2 * cp], e4m3_b01(r0), e4m3_b23(r0));
             mma_f16(acc[1], qa[2 * cp], e4m3_b01(r1), e4m3_b23(r1));
-            mma_f16(acc[0], qa[2 * cp + 1], e4m3_b01(r2), e4m3_b23(r2));
-            mma_f16(acc[1], qa[2 * cp + 1], e4m3_b01(r3), e4m3_b23(r3));
+            mma_f16(a[0], qa[2 * cp + 1], e4m3_b01(r2), e4m3_b23(r2));
+            mma_f16(a[1], qa[2 * cp + 1], e4m3_b01(r3), e4m3_b23(r3));
           }
+        }
+        if constexpr (MQ) {
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
         }
         float sc[2][4];
 #pragma unroll
