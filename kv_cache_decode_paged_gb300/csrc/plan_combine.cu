@@ -196,6 +196,10 @@ struct RowMap {
 constexpr int kCombineWarps = kCombineThreads / 32;
 constexpr int kCombineMaxCols = 4;   // float4 columns per lane: dv <= 512
 
+// COLS float4 columns per lane (dv <= 128 COLS); each warp loads BATCH splits
+// (its splits w, w + 8, ...) before merging them, so that a row split many
+// ways waits for a few batches of loads rather than one load per split.
+template <int COLS, int BATCH>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse,
                    const int32_t* __restrict__ first, const int32_t* __restrict__ count,
@@ -220,36 +224,43 @@ __global__ void __launch_bounds__(kCombineThreads)
   const float4* prow = reinterpret_cast<const float4*>(part_out + (size_t(f) * rows + r) * dv);
   const size_t wstride = size_t(rows) * v4;             // float4s between splits
   float m = -INFINITY, l = 0.f;                         // log2 units
-  float4 acc[kCombineMaxCols];
+  float4 acc[COLS];
 #pragma unroll
-  for (int j = 0; j < kCombineMaxCols; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int w = wi; w < cnt; w += kCombineWarps) {
-    const float lw = lrow[size_t(w) * rows] * kLog2e;
-    float4 v[kCombineMaxCols];
+  for (int j = 0; j < COLS; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int w0 = wi; w0 < cnt; w0 += kCombineWarps * BATCH) {
+    float lw[BATCH];
+    float4 v[BATCH][COLS];
 #pragma unroll
-    for (int j = 0; j < kCombineMaxCols; ++j)
-      v[j] = (lane + 32 * j < v4) ? prow[size_t(w) * wstride + lane + 32 * j]
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lw == -INFINITY) continue;  // a split with no valid token for this row
-    const float mn = fmaxf(m, lw);
-    const float a = exp2_approx(m - mn), e = exp2_approx(lw - mn);  // a = 0 while m = -inf
-    l = l * a + e;
+    for (int k = 0; k < BATCH; ++k) {
+      const int w = w0 + kCombineWarps * k;
+      lw[k] = w < cnt ? lrow[size_t(w) * rows] * kLog2e : -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kCombineMaxCols; ++j) {
-      acc[j].x = acc[j].x * a + e * v[j].x;
-      acc[j].y = acc[j].y * a + e * v[j].y;
-      acc[j].z = acc[j].z * a + e * v[j].z;
-      acc[j].w = acc[j].w * a + e * v[j].w;
+      for (int j = 0; j < COLS; ++j)
+        v[k][j] = (w < cnt && lane + 32 * j < v4) ? prow[size_t(w) * wstride + lane + 32 * j]
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    m = mn;
+#pragma unroll
+    for (int k = 0; k < BATCH; ++k) {
+      if (lw[k] == -INFINITY) continue;  // past the end, or a split with no valid token
+      const float mn = fmaxf(m, lw[k]);
+      const float a = exp2_approx(m - mn), e = exp2_approx(lw[k] - mn);  // a = 0 while m = -inf
+      l = l * a + e;
+#pragma unroll
+      for (int j = 0; j < COLS; ++j) {
+        acc[j].x = acc[j].x * a + e * v[k][j].x;
+        acc[j].y = acc[j].y * a + e * v[k][j].y;
+        acc[j].z = acc[j].z * a + e * v[k][j].z;
+        acc[j].w = acc[j].w * a + e * v[k][j].w;
+      }
+      m = mn;
+    }
   }
   if (lane == 0) {
     s_m[wi] = m;
     s_l[wi] = l;
   }
 #pragma unroll
-  for (int j = 0; j < kCombineMaxCols; ++j)
+  for (int j = 0; j < COLS; ++j)
     if (lane + 32 * j < v4) s_acc[wi][lane + 32 * j] = acc[j];
   __syncthreads();
   float M = -INFINITY;
@@ -349,8 +360,13 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
                       skip_single ? 1 : 0, map);
   }
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
-  return launch_pdl(combine_kernel, dim3(unsigned(items)), dim3(kCombineThreads), 0, s, part_out,
-                    part_lse, first, count, rows, dv, out, lse, skip_single ? 1 : 0, map);
+  using CombineFn = void (*)(const float*, const float*, const int32_t*, const int32_t*, int, int,
+                             float*, float*, int, RowMap);
+  const CombineFn k = dv <= 128 ? CombineFn(&combine_kernel<1, 8>)
+                    : dv <= 256 ? CombineFn(&combine_kernel<2, 4>)
+                                : CombineFn(&combine_kernel<4, 2>);
+  return launch_pdl(k, dim3(unsigned(items)), dim3(kCombineThreads), 0, s, part_out, part_lse, first,
+                    count, rows, dv, out, lse, skip_single ? 1 : 0, map);
 }
 
 // ---- device queries -----------------------------------------------------------
