@@ -80,6 +80,23 @@ def file_hash(*paths) -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (identity on one process): the slowest
+    replica sets the time of the whole job."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_replica: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: the bytes every replica read in one step, over the
+    step time (already the maximum over ranks)."""
+    return bytes_per_replica * world / (ms_per_step * 1e-3) / 1e9
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -428,11 +445,7 @@ def run_ours(args, wl, rank, world, local):
     w1 = time.monotonic()
     if dist:
         dist.barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     dec_ms = [a.elapsed_time(b) for a, b in evs]
     time.sleep(0.05)
     clocks = sampler.summary(w0, w1)
@@ -473,11 +486,8 @@ def run_ours(args, wl, rank, world, local):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     if dist:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
         dist.barrier()
 
     if rank != 0:
@@ -487,7 +497,7 @@ def run_ours(args, wl, rank, world, local):
 
     kvb = wl.kv_bytes()
     ms_step = ms_total / args.steps
-    value = kvb * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(kvb, world, ms_step)
     dec_mean = statistics.mean(dec_ms)
     achieved = kvb / (dec_mean * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -506,7 +516,7 @@ def run_ours(args, wl, rank, world, local):
                      "traffic": recorded_traffic(wl, args.config),
                      "kernel": "decode call (planner + decode kernel + combine), CUDA events",
                      "algorithmic_bytes_per_launch": kvb},
-        "e2e": {"value": kvb * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": whole_job_gbs(kvb, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "gpu_launches": launches * args.steps,
