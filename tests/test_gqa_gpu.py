@@ -193,6 +193,28 @@ def test_fp8_mqa_and_g4(oracle):
     _check(oracle, wl2, num_ctas=11)
 
 
+def _fp8_scales(wl):
+    f = lambda a: inputs.bf16_to_f32(a)
+    wl.k_scale = float(np.float32(np.abs(f(wl.k)).max()) / np.float32(448))
+    wl.v_scale = float(np.float32(np.abs(f(wl.v)).max()) / np.float32(448))
+
+
+def test_fp8_large_logits_and_needle(oracle):
+    # An E4M3 cache under 8x logits (peaked rows, the lazy rescale taken
+    # often) and with one dominant key, whose scale is refit so that it is
+    # stored without saturating.
+    wl = inputs.make_workload("llama3_70b_fp8", lens=[900, 2000], q_scale=8.0)
+    _check(oracle, wl, num_ctas=9)
+    wl2 = inputs.make_workload("llama3_70b_fp8", lens=[900, 2000])
+    inputs.plant_needle(wl2, b=1, head=13, t=1234, strength=60.0)
+    _fp8_scales(wl2)
+    g, out, _ = _check(oracle, wl2)
+    sl = wl2.seq_slice(1)
+    vc = oracle.quantize_e4m3(wl2.v[sl], wl2.v_scale)
+    vt = np.array([oracle.e4m3_decode(c) for c in vc[1234, 13 // wl2.g]]) * wl2.v_scale
+    np.testing.assert_allclose(out[1, 13], vt, atol=5e-2)
+
+
 def test_fp8_close_to_bf16_originals(oracle):
     # secondary check: the FP8 cache against the unquantised bf16 values, 5e-2
     wl = inputs.make_workload("llama3_70b_fp8", lens=[3000, 8192])
