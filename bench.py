@@ -14,7 +14,10 @@ larger than L2, so every step streams the KV cache from HBM.
   torchrun --nproc-per-node N bench.py --gpus N   # N independent replicas
 
 Metric: decode-attention KV-read GB/s (algorithmic KV bytes of a step / step
-time); also microseconds per layer-step and the fraction of ~8 TB/s.
+time); also microseconds per layer-step and the fraction of ~8 TB/s.  The
+headline times the step captured once in a CUDA graph and replayed, as a
+serving loop would run it; the line also carries the same step issued call by
+call ("direct"), and the roofline times each decode call with CUDA events.
 
 With --q-len L > 1 (GQA only) a step appends the last L tokens of every
 sequence and runs the multi-token decode: L queries per sequence, causal among
@@ -216,39 +219,43 @@ def multi_queries(args, wl):
 # ----------------------------------------------------------------------- oracle
 
 def oracle_sample_rate(wl, budget_s, oracle, qm=None):
-    """Run the oracle over whole sequences until the time budget is spent.
+    """Run the oracle over whole sequences, in a fixed shuffled order and over
+    the workload again if it finishes early, until the time budget is spent.
     Returns (GB/s of KV read, seconds, sample description)."""
-    done_bytes, t_total, seqs = 0, 0.0, []
+    done_bytes, t_total, n_seq, passes = 0, 0.0, 0, 0
     per_tok = wl.kv_bytes() / max(1, wl.total_tokens)
     import numpy as np
     order = list(np.random.default_rng(123).permutation(wl.B))
-    for b in order:
-        sl = wl.seq_slice(b)
-        t0 = time.perf_counter()
-        if wl.kind == "mla":
-            rows = np.concatenate([wl.c_kv[sl], wl.k_r[sl]], axis=1)
-            oracle.mla_decode(wl.q[b], rows, wl.d_c, wl.scale)
-        elif wl.kv_dtype == "fp8":
-            kc = oracle.quantize_e4m3(wl.k[sl], wl.k_scale)
-            vc = oracle.quantize_e4m3(wl.v[sl], wl.v_scale)
+    while t_total < budget_s:
+        passes += 1
+        for b in order:
+            sl = wl.seq_slice(b)
             t0 = time.perf_counter()
-            if qm is None:
-                oracle.gqa_decode(wl.q[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
-                                  k_scale=wl.k_scale, v_scale=wl.v_scale)
+            if wl.kind == "mla":
+                rows = np.concatenate([wl.c_kv[sl], wl.k_r[sl]], axis=1)
+                oracle.mla_decode(wl.q[b], rows, wl.d_c, wl.scale)
+            elif wl.kv_dtype == "fp8":
+                kc = oracle.quantize_e4m3(wl.k[sl], wl.k_scale)
+                vc = oracle.quantize_e4m3(wl.v[sl], wl.v_scale)
+                t0 = time.perf_counter()
+                if qm is None:
+                    oracle.gqa_decode(wl.q[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
+                                      k_scale=wl.k_scale, v_scale=wl.v_scale)
+                else:
+                    oracle.gqa_decode_multi(qm[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
+                                            k_scale=wl.k_scale, v_scale=wl.v_scale)
+            elif qm is None:
+                oracle.gqa_decode(wl.q[b], wl.k[sl], wl.v[sl], wl.scale)
             else:
-                oracle.gqa_decode_multi(qm[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
-                                        k_scale=wl.k_scale, v_scale=wl.v_scale)
-        elif qm is None:
-            oracle.gqa_decode(wl.q[b], wl.k[sl], wl.v[sl], wl.scale)
-        else:
-            oracle.gqa_decode_multi(qm[b], wl.k[sl], wl.v[sl], wl.scale)
-        t_total += time.perf_counter() - t0
-        done_bytes += int(wl.seq_lens[b]) * per_tok
-        seqs.append(int(b))
-        if t_total >= budget_s:
-            break
+                oracle.gqa_decode_multi(qm[b], wl.k[sl], wl.v[sl], wl.scale)
+            t_total += time.perf_counter() - t0
+            done_bytes += int(wl.seq_lens[b]) * per_tok
+            n_seq += 1
+            if t_total >= budget_s:
+                break
     gbs = done_bytes / t_total / 1e9 if t_total > 0 else 0.0
-    return gbs, t_total, f"{len(seqs)} of {wl.B} sequences ({done_bytes / 1e6:.1f} MB of KV), all heads"
+    return gbs, t_total, (f"{n_seq} sequences of the {wl.B} ({passes} pass(es) over the batch, "
+                          f"{done_bytes / 1e6:.1f} MB of KV), all heads")
 
 
 def run_reference(args, wl, rank):
@@ -376,6 +383,8 @@ def run_ours(args, wl, rank, world, local):
         lse = torch.empty((wl.B, L, wl.h), dtype=torch.float32, device=dev)
         q_dev = dev_bits(qm, dev)
     desc = g.cache.descriptor()
+    # Every call below enqueues on the current stream: this one, or the capture
+    # stream while the step is captured in a CUDA graph.
     stream = torch.cuda.current_stream()
     launches = 4 if wl.kind == "gqa" else 3   # append, planner, decode (, combine)
     proj = None
@@ -394,23 +403,22 @@ def run_ours(args, wl, rank, world, local):
     def decode():
         if qm is not None:
             kv.kvattn_decode_gqa_multi(q_dev, desc, g.bt, g.seq_lens, L, wl.h, wl.h_kv, wl.d,
-                                       wl.scale, out, lse, ws, err=g.err, stream=stream)
+                                       wl.scale, out, lse, ws, err=g.err)
         elif wl.kind == "gqa":
             kv.kvattn_decode_gqa(g.q, desc, g.bt, g.seq_lens, wl.h, wl.h_kv, wl.d, wl.scale,
-                                 out, lse, ws, err=g.err, stream=stream)
+                                 out, lse, ws, err=g.err)
         else:
             kv.kvattn_decode_mla(g.q, desc, g.bt, g.seq_lens, wl.h, wl.d_c, wl.d_rope, wl.scale,
-                                 out, lse, ws, err=g.err, stream=stream)
+                                 out, lse, ws, err=g.err)
 
     def step(ev=None, pe=None):
         if proj is not None:
             if pe is not None:
                 pe[0].record(stream)
-            kv.kvattn_mla_absorb_q(proj["q_nope"], proj["q_rope"], proj["w_uk"], g.q, err=g.err,
-                                   stream=stream)
+            kv.kvattn_mla_absorb_q(proj["q_nope"], proj["q_rope"], proj["w_uk"], g.q, err=g.err)
             if pe is not None:
                 pe[1].record(stream)
-        kv.kvattn_append(desc, new0, new1, seq_idx, pos, g.bt, err=g.err, stream=stream)
+        kv.kvattn_append(desc, new0, new1, seq_idx, pos, g.bt, err=g.err)
         if ev is not None:
             ev[0].record(stream)
         decode()
@@ -419,7 +427,7 @@ def run_ours(args, wl, rank, world, local):
         if proj is not None:
             if pe is not None:
                 pe[2].record(stream)
-            kv.kvattn_mla_up_v(out, proj["w_uv"], proj["v"], err=g.err, stream=stream)
+            kv.kvattn_mla_up_v(out, proj["w_uv"], proj["v"], err=g.err)
             if pe is not None:
                 pe[3].record(stream)
 
@@ -447,8 +455,34 @@ def run_ours(args, wl, rank, world, local):
         dist.barrier()
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     dec_ms = [a.elapsed_time(b) for a, b in evs]
+
+    # ---- the headline: the same step captured once in a CUDA graph and
+    # replayed, as a serving loop runs it (every kernel of the step still runs
+    # on every replay; only the host's per-launch cost between them is gone)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wg0 = time.monotonic()
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    wg1 = time.monotonic()
+    if dist:
+        dist.barrier()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1) / args.steps, dist, dev)
+    del graph
     time.sleep(0.05)
-    clocks = sampler.summary(w0, w1)
+    clocks = sampler.summary(wg0, wg1)
+    clocks_direct = sampler.summary(w0, w1)
     sampler.stop()
     err_bits = g.err_bits()
 
@@ -496,7 +530,8 @@ def run_ours(args, wl, rank, world, local):
         return
 
     kvb = wl.kv_bytes()
-    ms_step = ms_total / args.steps
+    ms_direct = ms_total / args.steps
+    ms_step = graph_ms
     value = whole_job_gbs(kvb, world, ms_step)
     dec_mean = statistics.mean(dec_ms)
     achieved = kvb / (dec_mean * 1e-3) / 1e9
@@ -519,6 +554,12 @@ def run_ours(args, wl, rank, world, local):
         "e2e": {"value": whole_job_gbs(kvb, world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
+        "timing": ("the step (append + decode call) captured once in a CUDA graph and "
+                   "replayed --steps times; 'direct' is the same step issued call by call, "
+                   "with CUDA events around each decode call"),
+        "direct": {"us_per_layer_step": ms_direct * 1e3,
+                   "value": whole_job_gbs(kvb, world, ms_direct), "unit": "GB/s",
+                   "clocks": clocks_direct},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "device_err_bits": err_bits,
