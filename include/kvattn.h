@@ -21,13 +21,23 @@
  *   "The KV cache size formula", section "vLLM: a per-layer page").
  *
  * Conventions for every call:
- *   - Ownership: the caller allocates and owns every buffer.  The library
- *     never allocates device memory; scratch space comes from the caller's
- *     workspace.  Pointers marked "device" must be device-accessible; a call
- *     only reads the host struct `kvattn_cache` during the call.
+ *   - Ownership: the caller allocates and owns every buffer.  No call
+ *     allocates device memory; scratch space comes from the caller's
+ *     workspace (kvattn_decode_gqa_noalloc instead uses a fixed array that
+ *     the library holds, described with it).  Pointers marked "device" must
+ *     be device-accessible; a call only reads the host struct `kvattn_cache`
+ *     during the call.
  *   - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
  *     Work is enqueued asynchronously; results are valid after the stream
  *     reaches that point.
+ *   - CUDA graphs: the first call of an entry point on a device does one-time
+ *     host set-up (kernel attributes, occupancy queries, the tensor-map
+ *     encoder's address); make it outside any stream capture.  After it,
+ *     kvattn_append, kvattn_decode_gqa, kvattn_decode_mla, kvattn_mla_absorb_q
+ *     and kvattn_mla_up_v only enqueue kernels on `stream`, so they can be
+ *     captured in a CUDA graph and replayed.  Replays read the buffers the
+ *     captured call was given, whatever they hold at replay time; the host
+ *     struct and scalars are fixed at capture.
  *   - Errors: invalid arguments are rejected before any launch with
  *     KVATTN_ERR_INVALID_ARG or KVATTN_ERR_UNSUPPORTED and nothing is
  *     enqueued.  KVATTN_ERR_CUDA means a CUDA call or launch failed.
