@@ -227,6 +227,7 @@ def oracle_sample_rate(wl, budget_s, oracle, qm=None):
     per_tok = wl.kv_bytes() / max(1, wl.total_tokens)
     import numpy as np
     order = list(np.random.default_rng(123).permutation(wl.B))
+    codes = {}   # E4M3 codes per sequence: the stored cache, made once, untimed
     while t_total < budget_s:
         passes += 1
         for b in order:
@@ -236,8 +237,10 @@ def oracle_sample_rate(wl, budget_s, oracle, qm=None):
                 rows = np.concatenate([wl.c_kv[sl], wl.k_r[sl]], axis=1)
                 oracle.mla_decode(wl.q[b], rows, wl.d_c, wl.scale)
             elif wl.kv_dtype == "fp8":
-                kc = oracle.quantize_e4m3(wl.k[sl], wl.k_scale)
-                vc = oracle.quantize_e4m3(wl.v[sl], wl.v_scale)
+                if b not in codes:
+                    codes[b] = (oracle.quantize_e4m3(wl.k[sl], wl.k_scale),
+                                oracle.quantize_e4m3(wl.v[sl], wl.v_scale))
+                kc, vc = codes[b]
                 t0 = time.perf_counter()
                 if qm is None:
                     oracle.gqa_decode(wl.q[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
@@ -277,6 +280,18 @@ def run_reference(args, wl, rank):
         f64 = lambda bits: inputs.bf16_to_f32(bits).astype(np.float64)
         w_uk, w_uv = f64(pj.w_uk), f64(pj.w_uv)
 
+    codes = {}
+
+    def fp8_codes(b, heads):
+        """The stored E4M3 codes of sequence b's first `heads` KV heads: the
+        cache as it sits in memory, made once outside the timed steps (the
+        step's own append writes one token per sequence)."""
+        if (b, heads) not in codes:
+            sl = wl.seq_slice(b)
+            codes[(b, heads)] = (oracle.quantize_e4m3(wl.k[sl, :heads], wl.k_scale),
+                                 oracle.quantize_e4m3(wl.v[sl, :heads], wl.v_scale))
+        return codes[(b, heads)]
+
     def one(i, heads):
         b = int(order[i % len(order)])
         sl = wl.seq_slice(b)
@@ -295,8 +310,7 @@ def run_reference(args, wl, rank):
         kw = {}
         k, v = wl.k[sl, :heads], wl.v[sl, :heads]
         if wl.kv_dtype == "fp8":
-            k = oracle.quantize_e4m3(k, wl.k_scale)
-            v = oracle.quantize_e4m3(v, wl.v_scale)
+            k, v = fp8_codes(b, heads)
             kw = dict(fmt=oracle.FMT_E4M3, k_scale=wl.k_scale, v_scale=wl.v_scale)
         if qm is None:
             oracle.gqa_decode(wl.q[b, :heads * g], k, v, wl.scale, **kw)
@@ -306,12 +320,18 @@ def run_reference(args, wl, rank):
 
     units = wl.h if wl.kind == "mla" else wl.h_kv
     heads = units
+    if wl.kv_dtype == "fp8":
+        fp8_codes(int(order[0]), heads)
     t0 = time.perf_counter()
     one(0, heads)
     dt = time.perf_counter() - t0
     while heads > 1 and dt * heads / units > budget_per_step and dt > budget_per_step:
         heads = max(1, heads // 2)
         dt /= 2
+    if wl.kv_dtype == "fp8":
+        codes.clear()
+        for i in range(max(warm, steps)):
+            fp8_codes(int(order[i % len(order)]), heads)
     for i in range(warm):
         one(i, heads)
     total_bytes = 0.0

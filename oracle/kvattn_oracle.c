@@ -78,21 +78,27 @@ double kvo_e4m3_decode(uint8_t code) {
 
 /* Encode a binary32 value to E4M3: round to the nearest representable value,
  * ties to the code with an even mantissa, and saturate magnitudes above 448 to
- * 448 (the format has no infinity).  Done by exhaustive nearest search over
- * the 127 finite non-negative codes, which is slow and plainly correct. */
+ * 448 (the format has no infinity).  The non-negative finite codes 0x00..0x7E
+ * decode to strictly increasing magnitudes, so the nearest one is found by a
+ * binary search for the first code whose magnitude is >= |x| and a comparison
+ * with the code below it. */
 uint8_t kvo_e4m3_encode(float x) {
   double a = fabs((double)x);
   uint8_t sign = (x < 0.0f || (x == 0.0f && signbit(x))) ? 0x80 : 0x00;
   if (isnan(x)) return 0x7F;
   if (a >= 448.0) return (uint8_t)(sign | 0x7E);
-  int best = 0;
-  double best_err = INFINITY;
-  for (int c = 0; c <= 0x7E; ++c) {
-    double err = fabs(kvo_e4m3_decode((uint8_t)c) - a);
-    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
-      best = c;
-      best_err = err;
-    }
+  int lo = 0, hi = 0x7E;              /* first code with magnitude >= a */
+  while (lo < hi) {
+    int mid = (lo + hi) / 2;
+    if (kvo_e4m3_decode((uint8_t)mid) >= a)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  int best = lo;
+  if (lo > 0) {
+    double up = kvo_e4m3_decode((uint8_t)lo) - a, down = a - kvo_e4m3_decode((uint8_t)(lo - 1));
+    if (down < up || (down == up && ((lo - 1) & 1) == 0)) best = lo - 1;
   }
   return (uint8_t)(sign | best);
 }

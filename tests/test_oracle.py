@@ -111,6 +111,22 @@ def test_e4m3_encode_vs_torch_in_range(oracle):
     assert (got == ref).all()
 
 
+def test_e4m3_encode_vs_torch_on_float32_samples(oracle):
+    # The quantiser encodes x / scale computed in binary32, which is not a bf16
+    # value: seeded float32 samples over the whole range, around the
+    # subnormal/normal boundary and at every scale of magnitude, code for code
+    # against torch's round-to-nearest-even cast.
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([
+        rng.uniform(-448.0, 448.0, 40000),
+        rng.standard_normal(40000) * rng.choice([1e-3, 1e-2, 1.0, 10.0], 40000),
+        np.linspace(-2.0 ** -5, 2.0 ** -5, 20001),
+    ]).astype(np.float32)
+    ref = torch.from_numpy(vals.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in vals], dtype=np.uint8)
+    assert (got == ref).all()
+
+
 def test_e4m3_encode_ties_and_saturation(oracle):
     # midpoint between 1.0 (0x38) and 1.125 (0x39) rounds to the even code
     assert oracle.e4m3_encode(1.0625) == 0x38
