@@ -1,7 +1,8 @@
 """Float64 CPU oracle for paged decode attention -- test infrastructure only.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
-baseline leg may import this package.  The product path (the CUDA library and
+baseline leg and reference arm (``bench.py --impl reference``) may import this
+package.  The product path (the CUDA library and
 its binding) never imports it, and it imports nothing from the product.
 
 The arithmetic lives in ``kvattn_oracle.c`` (plain C, double precision,

@@ -2,7 +2,7 @@
  * kvattn_oracle.c -- plain, slow, float64 CPU oracle for paged decode attention.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
- * benchmark's CPU-baseline leg may load this file's library.  It shares no
+ * benchmark's CPU-baseline leg and reference arm may load this file's library.  It shares no
  * code, header, table or constant with the CUDA library: it is written from
  * the definitions on the pages, in the pages' notation, and nothing here is
  * blocked, fused or reordered beyond what those definitions state.
