@@ -68,6 +68,7 @@ def _load():
             "kvo_mla_pool_offset": (i64, [P, i32, i32, i32, i32, i64]),
             "kvo_gqa_decode": (i32, [P, P, P, i32, f64, f64, i64, i32, i32, i32, f64, P, P]),
             "kvo_mla_decode": (i32, [P, P, i32, i64, i32, i32, i32, f64, P, P]),
+            "kvo_mla_decode_e4m3": (i32, [P, P, i64, i32, i32, i32, f64, f64, f64, P, P]),
             "kvo_mla_absorb_query": (None, [P, P, i32, i32, i32, P]),
             "kvo_mla_apply_wuv": (None, [P, P, i32, i32, i32, P]),
             "kvo_mla_explicit": (i32, [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, f64, P, P]),
@@ -239,6 +240,24 @@ def mla_decode(q, rows, d_c, scale, fmt=FMT_BF16):
                                 _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError("kvo_mla_decode: bad shape")
+    return out, lse
+
+
+def mla_decode_e4m3(q, codes, d_c, scale, c_scale, r_scale):
+    """One sequence over an FP8-E4M3 latent cache: q [h, d_c + d_rope] bf16
+    bits, codes [s, d_c + d_rope] uint8; the c_KV codes decode times c_scale,
+    the k_R codes times r_scale.  Returns (out [h, d_c], lse [h]) float64."""
+    q = _c(q, np.uint16)
+    codes = _c(codes, np.uint8)
+    h, w = q.shape
+    s = codes.shape[0]
+    assert codes.shape[1] == w
+    out = np.empty((h, d_c), dtype=np.float64)
+    lse = np.empty(h, dtype=np.float64)
+    rc = _load().kvo_mla_decode_e4m3(_ptr(q), _ptr(codes), s, h, d_c, w - d_c, float(c_scale),
+                                     float(r_scale), float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("kvo_mla_decode_e4m3: bad shape")
     return out, lse
 
 

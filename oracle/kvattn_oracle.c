@@ -301,6 +301,35 @@ int kvo_mla_decode(const void* q, const void* rows, int fmt, int64_t s, int h, i
   return 0;
 }
 
+/* MLA absorbed decode over an FP8-E4M3 latent cache.  Each cached row is
+ * stored as E4M3 codes: the c_KV part decodes to e4m3(code) * c_scale and the
+ * k_R part to e4m3(code) * r_scale, one per-tensor scale each (the pages
+ * store the MLA latent in FP8 with scaling factors: [P2] "High-Throughput
+ * Serving Kernels: FlashMLA and SGLang"; [P4] "MLA 与 KV Cache 量化可以叠加").
+ * The rows are decoded to double and the attention is kvo_mla_decode's on
+ * those values.  q: bf16 [h][d_c + d_rope]; codes: [s][d_c + d_rope]. */
+int kvo_mla_decode_e4m3(const uint16_t* q, const uint8_t* codes, int64_t s, int h, int d_c,
+                        int d_rope, double c_scale, double r_scale, double scale, double* out,
+                        double* lse) {
+  if (h <= 0 || d_c <= 0 || d_rope < 0 || s < 0) return -1;
+  int w = d_c + d_rope;
+  double* qd = (double*)malloc(sizeof(double) * (size_t)h * (size_t)w);
+  double* rows = (double*)malloc(sizeof(double) * ((size_t)s * (size_t)w + 1));
+  if (!qd || !rows) {
+    free(qd);
+    free(rows);
+    return -1;
+  }
+  for (int64_t i = 0; i < (int64_t)h * w; ++i) qd[i] = kvo_bf16_to_double(q[i]);
+  for (int64_t t = 0; t < s; ++t)
+    for (int c = 0; c < w; ++c)
+      rows[t * w + c] = kvo_e4m3_decode(codes[t * w + c]) * (c < d_c ? c_scale : r_scale);
+  int rc = kvo_mla_decode(qd, rows, KVO_FMT_F64, s, h, d_c, d_rope, scale, out, lse);
+  free(qd);
+  free(rows);
+  return rc;
+}
+
 /* Query-side absorption q~^C_i = W_UK,i^T q^C_i, W_UK viewed (h, d_hc, d_c)
  * ([P2] "Let us define the absorbed query vector"; the reference module's
  * w_uk.view(n_heads, d_head, d_c_kv)).  q_c: [h][d_hc]; w_uk: [h][d_hc][d_c];

@@ -294,6 +294,40 @@ def test_mla_matches_torch_sdpa(oracle):
     np.testing.assert_allclose(lse, ref_l.numpy(), rtol=1e-12)
 
 
+def test_mla_e4m3_latent_matches_torch(oracle):
+    # FP8 latent cache: codes decoded by torch's float8_e4m3fn, c_KV times its
+    # scale and k_R times its own (100x apart, so a swap would show), then
+    # torch's float64 attention over those rows
+    rng = np.random.default_rng(10)
+    h, d_c, d_r, s = 4, 512, 64, 29
+    q = inputs.bf16_bits((rng.standard_normal((h, d_c + d_r)) / 24).astype(np.float32))
+    c = inputs.bf16_bits(rng.standard_normal((s, d_c)).astype(np.float32))
+    kr = inputs.bf16_bits((rng.standard_normal((s, d_r)) * 100).astype(np.float32))
+    f = lambda a: inputs.bf16_to_f32(a).astype(np.float64)
+    c_scale = float(np.float32(np.abs(inputs.bf16_to_f32(c)).max()) / np.float32(448))
+    r_scale = float(np.float32(np.abs(inputs.bf16_to_f32(kr)).max()) / np.float32(448))
+    codes = np.concatenate([oracle.quantize_e4m3(c, c_scale), oracle.quantize_e4m3(kr, r_scale)], 1)
+    scale = 1 / math.sqrt(192)
+    out, lse = oracle.mla_decode_e4m3(q, codes, d_c, scale, c_scale, r_scale)
+    dec = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64)
+    rows = torch.cat([dec[:, :d_c] * c_scale, dec[:, d_c:] * r_scale], 1)
+    qt = torch.from_numpy(f(q))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt[None, :, None, :], rows[None, None], rows[:, :d_c].contiguous()[None, None],
+        scale=scale, enable_gqa=True)
+    np.testing.assert_allclose(out, ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-13)
+    ref_l = torch.logsumexp(qt @ rows.T * scale, dim=-1)
+    np.testing.assert_allclose(lse, ref_l.numpy(), rtol=1e-12)
+    # with k_R of the workload's N(0, 1) spread, the E4M3 cache stays close to
+    # its bf16 originals (3 mantissa bits)
+    kr1 = inputs.bf16_bits(rng.standard_normal((s, d_r)).astype(np.float32))
+    r1 = float(np.float32(np.abs(inputs.bf16_to_f32(kr1)).max()) / np.float32(448))
+    codes1 = np.concatenate([codes[:, :d_c], oracle.quantize_e4m3(kr1, r1)], 1)
+    out1, _ = oracle.mla_decode_e4m3(q, codes1, d_c, scale, c_scale, r1)
+    orig, _ = oracle.mla_decode(q, np.concatenate([c, kr1], 1), d_c, scale)
+    assert np.abs(out1 - orig).max() < 5e-2
+
+
 @pytest.mark.parametrize("h,d_hc,d_c,d_r,d_v,s", [(4, 16, 32, 8, 16, 5), (2, 128, 512, 64, 128, 7)])
 def test_mla_absorbed_equals_explicit(oracle, h, d_hc, d_c, d_r, d_v, s):
     """Absorbed decode (q~ = W_UK^T q^C, latent weighted sum, W_UV afterwards)
