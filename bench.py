@@ -191,8 +191,10 @@ def config_dict(wl, args):
          "seq_lens": {"min": int(wl.seq_lens.min()), "max": int(wl.seq_lens.max()),
                       "mean": float(wl.seq_lens.mean())},
          "seed": args.seed,
-         "l2": ("inputs larger than L2: every step reads %.2f GB of KV vs %d MB of L2"
-                % (wl.kv_bytes() / 1e9, L2_BYTES // 2**20)),
+         "l2": (("inputs larger than L2: every step reads %.2f GB of KV vs %d MB of L2"
+                 % (wl.kv_bytes() / 1e9, L2_BYTES // 2**20)) if wl.kv_bytes() > L2_BYTES else
+                ("inputs smaller than L2 and not flushed: %.1f KB of KV stays L2-resident "
+                 "(a launch-bound case, timed for latency)" % (wl.kv_bytes() / 1e3))),
          "parallelism": f"replicas x{args.gpus}"}
     if wl.kind == "gqa":
         d.update({"h_kv": wl.h_kv, "d_h": wl.d})
