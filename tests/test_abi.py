@@ -116,6 +116,20 @@ def test_gqa_empty_batch_is_ok_without_launch(lib):
     assert _gqa_call(lib, _gqa_cache(), batch=0) == kv.KVATTN_OK
 
 
+def test_gqa_multi_host_validation(lib):
+    c = _gqa_cache()   # h_kv = 2, d_h = 128
+
+    def call(q_len=4, h=8, batch=2):
+        return lib.kvattn_decode_gqa_multi(FAKE, ctypes.byref(c), FAKE, FAKE, batch, 4, q_len, h,
+                                           2, 128, 0.1, FAKE, FAKE, FAKE, 1 << 20, 4, None, None)
+
+    assert call(q_len=0) == kv.KVATTN_ERR_INVALID_ARG
+    assert call(q_len=-3) == kv.KVATTN_ERR_INVALID_ARG
+    assert call(h=32, q_len=5) == kv.KVATTN_ERR_UNSUPPORTED     # 16 heads x 5 tokens > 64 rows
+    assert call(h=7) == kv.KVATTN_ERR_INVALID_ARG                # h % h_kv != 0
+    assert call(batch=0) == kv.KVATTN_OK                         # nothing to do, nothing launched
+
+
 def test_mla_host_validation(lib):
     c = kv.kvattn_cache(kv.KVATTN_MLA, kv.KVATTN_BF16, 100, 64, 1, 0, 512, 64, 1.0, 1.0, 0,
                         None, None, FAKE)
