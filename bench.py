@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (GQA; > 1 runs the multi-token decode)")
+    ap.add_argument("--no-all-configs", action="store_true",
+                    help="skip timing the decode call of every workload (the all_configs object)")
     ap.add_argument("--absorb", action="store_true",
                     help="MLA: add query absorption and value up-projection to every step")
     return ap.parse_args()
@@ -130,8 +132,64 @@ def recorded_traffic(wl, config):
     return rec.get("bytes_per_launch")
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, read-only
+    queries) by a thread that polls every millisecond, so that even a timed
+    region of a few milliseconds holds samples."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_uuid: str):
+        import ctypes
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.dev = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(), ctypes.byref(self.dev)) != 0:
+                return
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+            self.nv, self.ct = nv, ctypes
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _poll(self):
+        ct, nv = self.ct, self.nv
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(clk)) == 0 and \
+                    self.reasons_fn(self.dev, ct.byref(rs)) == 0:
+                self.samples.append((time.monotonic(), float(clk.value), int(rs.value)))
+            time.sleep(0.001)
+
+    def start(self):
+        if self.ok:
+            threading.Thread(target=self._poll, daemon=True).start()
+
+    def stop(self):
+        self._stop.set()
+
+    def summary(self, t0, t1):
+        win = [(c, r) for t, c, r in self.samples if t0 <= t <= t1]
+        if not win:
+            return None
+        reasons = sorted({n for _, r in win for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in win), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(win), "window": "timed region",
+                "source": "NVML, polled every 1 ms"}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons in the background."""
+    """nvidia-smi samples of SM clock and throttle reasons in the background,
+    with NVML polling beside it for short timed regions."""
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -140,8 +198,10 @@ class ClockSampler:
         self.samples = []
         self.proc = None
         self.gpu_id = gpu_id
+        self.nvml = NvmlClocks(gpu_id)
 
     def start(self):
+        self.nvml.start()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
@@ -159,6 +219,7 @@ class ClockSampler:
                 self.samples.append((time.monotonic(), parts))
 
     def stop(self):
+        self.nvml.stop()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -167,6 +228,9 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
+        fine = self.nvml.summary(t0, t1)
+        if fine is not None:
+            return fine
         win = [s for t, s in self.samples if t0 <= t <= t1]
         window = "timed region"
         if not win:
@@ -181,7 +245,7 @@ class ClockSampler:
         reasons = sorted({names[i] for s in win for i in range(4) if s[2 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(win), "window": window}
+                "samples": len(win), "window": window, "source": "nvidia-smi, every 20 ms"}
 
 
 def config_dict(wl, args):
@@ -357,6 +421,112 @@ def run_reference(args, wl, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ every workload
+
+ALL_CONFIGS = ["tiny", "llama3_8b", "llama3_70b", "llama3_70b_fp8", "deepseek_v3_mla",
+               "long_gqa8", "long_mqa"]
+FLUSH_BYTES = 512 * 2**20   # 4x L2
+
+
+def replay_us(torch, fn, n, stream):
+    """Mean microseconds of fn captured once in a CUDA graph and replayed n
+    times between two events on `stream`."""
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        fn()
+    for _ in range(3):
+        gr.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        gr.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    del gr
+    return a.elapsed_time(b) / n * 1e3
+
+
+def time_all_configs(args, sampler, headline, dev):
+    """The decode call (planner, decode kernel, combine) of every workload,
+    replayed from a CUDA graph: back to back, and after an L2 flush before
+    every replay.  The flush reads a buffer 4x the size of L2 (a read leaves
+    clean lines behind, so no write-back lands in the decode's time); the
+    flush is timed alone the same way and subtracted."""
+    import torch
+
+    import kv_cache_decode_paged_gb300 as kv
+    from kv_cache_decode_paged_gb300 import inputs
+    from kv_cache_decode_paged_gb300.device import GpuWorkload
+
+    peak, _ = hbm_peak()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush():
+        torch.sum(flush_buf, dtype=torch.int64, out=sink)
+
+    n = max(50, args.steps)
+    res = {}
+    for name in ALL_CONFIGS:
+        if headline is not None and headline.wl.name == name:
+            g = headline
+        else:
+            g = GpuWorkload(inputs.make_workload(name, seed=args.seed), poison=False, device=dev)
+        wl = g.wl
+        ws = g.workspace()
+        dv = wl.d_c if wl.kind == "mla" else wl.d
+        out = torch.empty((wl.B, wl.h, dv), dtype=torch.float32, device=dev)
+        lse = torch.empty((wl.B, wl.h), dtype=torch.float32, device=dev)
+        desc = g.cache.descriptor()
+
+        def decode():
+            if wl.kind == "gqa":
+                kv.kvattn_decode_gqa(g.q, desc, g.bt, g.seq_lens, wl.h, wl.h_kv, wl.d, wl.scale,
+                                     out, lse, ws, err=g.err)
+            else:
+                kv.kvattn_decode_mla(g.q, desc, g.bt, g.seq_lens, wl.h, wl.d_c, wl.d_rope,
+                                     wl.scale, out, lse, ws, err=g.err)
+
+        def flushed():
+            flush()
+            decode()
+
+        torch.cuda.synchronize()
+        t0 = time.monotonic()
+        warm = replay_us(torch, decode, n, stream)
+        both = replay_us(torch, flushed, n, stream)
+        alone = replay_us(torch, flush, n, stream)
+        t1 = time.monotonic()
+        cold = max(both - alone, 1e-3)
+        kvb = wl.kv_bytes()
+        target = 0.65 if wl.kind == "mla" else 0.75
+        entry = {"kernel": "MLA absorbed decode" if wl.kind == "mla" else
+                 ("GQA decode, FP8-E4M3 cache" if wl.kv_dtype == "fp8" else "GQA decode"),
+                 "batch": wl.B, "h": wl.h, "kv_bytes": kvb, "total_tokens": wl.total_tokens,
+                 "us_decode_call": cold, "us_decode_call_back_to_back": warm,
+                 "us_l2_flush": alone,
+                 "gbs": kvb / cold / 1e3, "frac_of_measured_hbm": kvb / cold / 1e3 / peak,
+                 "pct_of_8tbs": 100.0 * kvb / cold / 1e3 / NOMINAL_HBM_GBS,
+                 "gbs_back_to_back": kvb / warm / 1e3, "target_frac": target,
+                 "clocks": sampler.summary(t0, t1), "device_err_bits": g.err_bits()}
+        if wl.kind == "gqa":
+            entry["h_kv"] = wl.h_kv
+        if name == "tiny":
+            entry["note"] = "launch-bound: 70 KB of KV, timed for latency"
+        res[name] = entry
+        del out, lse, ws, decode, flushed
+        if g is not headline:
+            del g
+        torch.cuda.empty_cache()
+    res["how"] = ("decode call replayed from a CUDA graph %d times; us_decode_call = (flush + "
+                  "decode replays - flush replays) / %d with an L2 flush (sum over a %d MB "
+                  "buffer) before every decode; gbs, frac and pct use it" % (n, n,
+                                                                             FLUSH_BYTES >> 20))
+    return res
+
+
 # -------------------------------------------------------------------------- ours
 
 def run_ours(args, wl, rank, world, local):
@@ -524,7 +694,6 @@ def run_ours(args, wl, rank, world, local):
     time.sleep(0.05)
     clocks = sampler.summary(wg0, wg1)
     clocks_direct = sampler.summary(w0, w1)
-    sampler.stop()
     err_bits = g.err_bits()
 
     # ---- end to end: host buffers in, result out, every step
@@ -566,6 +735,7 @@ def run_ours(args, wl, rank, world, local):
         dist.barrier()
 
     if rank != 0:
+        sampler.stop()
         if dist:
             dist.destroy_process_group()
         return
@@ -620,6 +790,9 @@ def run_ours(args, wl, rank, world, local):
             "up_v": {"us": u_us, "bytes": u_bytes, "gbs": u_bytes / u_us / 1e3,
                      "frac_of_hbm": u_bytes / u_us / 1e3 / peak, "tflops": flops / u_us / 1e6},
             "note": "CUDA events around each launch; bytes = weights + activations read and written"}
+    if world == 1 and not args.no_all_configs and args.q_len == 1 and not args.absorb:
+        line["all_configs"] = time_all_configs(args, sampler, g, dev)
+    sampler.stop()
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

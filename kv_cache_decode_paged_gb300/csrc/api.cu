@@ -94,14 +94,15 @@ extern "C" size_t kvattn_decode_workspace_bytes(int kind, int batch, int h, int 
   return ws_layout(batch, units, G, rows, dv).total;
 }
 
-extern "C" kvattn_status kvattn_decode_gqa_multi(const void* q, const kvattn_cache* cache,
-                                                 const int32_t* block_table,
-                                                 const int32_t* seq_lens, int batch,
-                                                 int max_blocks_per_seq, int q_len, int h,
-                                                 int h_kv, int d_h, float scale, float* out,
-                                                 float* lse, void* workspace,
-                                                 size_t workspace_bytes, int num_ctas,
-                                                 int32_t* err, void* stream) {
+namespace kv {
+
+// Host validation of a GQA decode call, in the order the checks are made;
+// KVATTN_OK with *nothing = true for an empty batch (nothing to enqueue).
+kvattn_status check_gqa_args(const void* q, const kvattn_cache* cache, const int32_t* block_table,
+                             const int32_t* seq_lens, int batch, int max_blocks_per_seq, int q_len,
+                             int h, int h_kv, int d_h, float scale, const float* out,
+                             const float* lse, int num_ctas, bool* nothing) {
+  *nothing = false;
   if (!cache || cache->kind != KVATTN_GQA) return KVATTN_ERR_INVALID_ARG;
   if (batch < 0 || max_blocks_per_seq <= 0 || h <= 0 || h_kv <= 0 || d_h <= 0 || num_ctas < 0 ||
       q_len <= 0)
@@ -110,7 +111,10 @@ extern "C" kvattn_status kvattn_decode_gqa_multi(const void* q, const kvattn_cac
   if (cache->h_kv != h_kv || cache->d_h != d_h || cache->reserved != 0) return KVATTN_ERR_INVALID_ARG;
   if (cache->num_blocks <= 0 || cache->block_size <= 0) return KVATTN_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale == INFINITY) return KVATTN_ERR_INVALID_ARG;
-  if (batch == 0) return KVATTN_OK;
+  if (batch == 0) {
+    *nothing = true;
+    return KVATTN_OK;
+  }
   if (!q || !block_table || !seq_lens || !out || !lse || !cache->k || !cache->v)
     return KVATTN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(cache->k, 16) ||
@@ -129,6 +133,24 @@ extern "C" kvattn_status kvattn_decode_gqa_multi(const void* q, const kvattn_cac
   if (int64_t(batch) * h_kv >= INT_MAX / 2 || int64_t(batch) * q_len * h >= INT_MAX)
     return KVATTN_ERR_UNSUPPORTED;
   if (num_ctas > 65535) return KVATTN_ERR_INVALID_ARG;
+  return KVATTN_OK;
+}
+
+}  // namespace kv
+
+extern "C" kvattn_status kvattn_decode_gqa_multi(const void* q, const kvattn_cache* cache,
+                                                 const int32_t* block_table,
+                                                 const int32_t* seq_lens, int batch,
+                                                 int max_blocks_per_seq, int q_len, int h,
+                                                 int h_kv, int d_h, float scale, float* out,
+                                                 float* lse, void* workspace,
+                                                 size_t workspace_bytes, int num_ctas,
+                                                 int32_t* err, void* stream) {
+  bool nothing = false;
+  const kvattn_status st = check_gqa_args(q, cache, block_table, seq_lens, batch,
+                                          max_blocks_per_seq, q_len, h, h_kv, d_h, scale, out,
+                                          lse, num_ctas, &nothing);
+  if (st != KVATTN_OK || nothing) return st;
   GqaArgs a;
   a.q = q;
   a.cache = cache;

@@ -134,6 +134,12 @@ struct GqaArgs {
   cudaStream_t stream;
 };
 kvattn_status run_decode_gqa(const GqaArgs& a);
+// Host validation of a GQA decode call (api.cu); KVATTN_OK with *nothing set
+// for an empty batch.
+kvattn_status check_gqa_args(const void* q, const kvattn_cache* cache, const int32_t* block_table,
+                             const int32_t* seq_lens, int batch, int max_blocks_per_seq, int q_len,
+                             int h, int h_kv, int d_h, float scale, const float* out,
+                             const float* lse, int num_ctas, bool* nothing);
 int gqa_default_ctas(int dtype, int h, int h_kv, int d);
 
 struct MlaArgs {

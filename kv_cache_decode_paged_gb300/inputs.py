@@ -205,10 +205,11 @@ def make_block_table(seq_lens: np.ndarray, bs: int, how: str, seed: int,
 
 def make_workload(name: str, seed: int = 0, batch: Optional[int] = None,
                   lens=None, block_size: Optional[int] = None, table: Optional[str] = None,
-                  q_scale: float = 1.0) -> Workload:
+                  q_scale: float = 1.0, heads: Optional[int] = None) -> Workload:
     """Build a named workload.  ``batch``/``lens``/``block_size``/``table``
     override the recipe (smaller parity cases of the same shapes);
-    ``q_scale`` multiplies the query spread (large-logit stress cases)."""
+    ``q_scale`` multiplies the query spread (large-logit stress cases);
+    ``heads`` (MLA only) draws queries for fewer query heads."""
     r = dict(WORKLOADS[name])
     B = int(batch if batch is not None else r["B"])
     if lens is not None:
@@ -224,7 +225,7 @@ def make_workload(name: str, seed: int = 0, batch: Optional[int] = None,
     bt, num_blocks = make_block_table(seq_lens, bs, table_kind, seed)
 
     if r["kind"] == "mla":
-        d_c, d_rope, h = r["d_c"], r["d_rope"], r["h"]
+        d_c, d_rope, h = r["d_c"], r["d_rope"], int(heads or r["h"])
         d = d_c + d_rope
         q = normal_bf16(rng_for(seed, "q"), B * h * d, r["q_std"] * q_scale).reshape(B, h, d)
         c_kv = normal_bf16(rng_for(seed, "c_kv"), S * d_c).reshape(S, d_c)
@@ -234,6 +235,8 @@ def make_workload(name: str, seed: int = 0, batch: Optional[int] = None,
                         seq_lens=seq_lens, cu_seqlens=cu, q=q, k=None, v=None,
                         c_kv=c_kv, k_r=k_r, block_table=bt, num_blocks=num_blocks)
 
+    if heads is not None:
+        raise ValueError("heads overrides the query heads of MLA workloads only")
     h, h_kv, d = r["h"], r["h_kv"], r["d"]
     q = normal_bf16(rng_for(seed, "q"), B * h * d, r["q_std"] * q_scale).reshape(B, h, d)
     k = normal_bf16(rng_for(seed, "k"), S * h_kv * d).reshape(S, h_kv, d)

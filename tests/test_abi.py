@@ -116,6 +116,37 @@ def test_gqa_empty_batch_is_ok_without_launch(lib):
     assert _gqa_call(lib, _gqa_cache(), batch=0) == kv.KVATTN_OK
 
 
+def _noalloc_call(lib, cache, **kw):
+    args = dict(q=FAKE, bt=FAKE, sl=FAKE, batch=2, maxb=4, h=8, h_kv=2, d=128, scale=0.1,
+                out=FAKE, lse=FAKE, ctas=4)
+    args.update(kw)
+    return lib.kvattn_decode_gqa_noalloc(args["q"], ctypes.byref(cache), args["bt"], args["sl"],
+                                         args["batch"], args["maxb"], args["h"], args["h_kv"],
+                                         args["d"], args["scale"], args["out"], args["lse"],
+                                         args["ctas"], None, None)
+
+
+@pytest.mark.parametrize("kw,cache_kw", [
+    (dict(h=6, h_kv=4), dict(h_kv=4)),
+    (dict(q=0), {}),
+    (dict(d=96), dict(d_h=96)),
+    ({}, dict(block_size=40)),
+    # argument errors whose (hypothetical) workspace would also exceed the
+    # built-in scratch: the argument error is what the caller hears about
+    (dict(ctas=70000), {}),
+    (dict(batch=100000, ctas=70000), {}),
+])
+def test_noalloc_reports_argument_errors_like_the_workspace_entry(lib, kw, cache_kw):
+    # no device is needed to reach these answers: the checks run first
+    want = _gqa_call(lib, _gqa_cache(**cache_kw), **kw)
+    assert want in (kv.KVATTN_ERR_INVALID_ARG, kv.KVATTN_ERR_UNSUPPORTED)
+    assert _noalloc_call(lib, _gqa_cache(**cache_kw), **kw) == want
+
+
+def test_noalloc_empty_batch_is_ok_without_launch(lib):
+    assert _noalloc_call(lib, _gqa_cache(), batch=0) == kv.KVATTN_OK
+
+
 def test_gqa_multi_host_validation(lib):
     c = _gqa_cache()   # h_kv = 2, d_h = 128
 

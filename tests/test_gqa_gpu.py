@@ -84,6 +84,21 @@ def test_forced_splits(oracle, num_ctas):
     _check(oracle, wl, num_ctas=num_ctas)
 
 
+@pytest.mark.parametrize("batch", [1500, 5000])
+def test_large_batches_reach_every_planner_path(oracle, batch):
+    # More than 1,024 sequences take the planner's multi-pass prefix scan, and
+    # 4,096 or more keep the prefix array in global memory instead of shared
+    # memory.  Short ragged lengths (empty ones included) keep the case small
+    # while the 304 default CTAs cut many units into pieces; every sequence is
+    # compared with the oracle.
+    lens = inputs.rng_for(batch, "large-batch lens").integers(0, 65, size=batch)
+    wl = inputs.make_workload("llama3_8b", lens=lens.tolist())
+    g, out, lse = _check(oracle, wl)
+    empty = np.nonzero(lens == 0)[0]
+    assert len(empty) > 0
+    assert (out[empty] == 0).all() and np.isneginf(lse[empty]).all()
+
+
 def test_split_count_does_not_change_result_beyond_rounding():
     # splits change only rounding: the probabilities enter the P.V product as
     # bf16 relative to each split's running max (2^-9 relative), far inside

@@ -31,6 +31,7 @@ def test_tiny(oracle, q_len):
     ("llama3_8b", [2049, 100], 8),                 # 32 rows: two m-tiles
     ("llama3_70b", [4099, 1000], 8),               # g = 8: 64 rows
     ("llama3_70b_fp8", [4099, 300], 4),            # FP8 cache, 32 rows
+    ("llama3_70b_fp8", [8192, 4099, 300, 17], 8),  # FP8 cache, 64 rows: the benched shape
     ("long_mqa", [9000, 40], 2),                   # MQA g = 32: 64 rows
 ])
 def test_model_shapes(oracle, name, lens, q_len):
@@ -43,6 +44,21 @@ def test_forced_splits(oracle, num_ctas):
     # (sequence, token, head) row map
     _check(oracle, inputs.make_workload("llama3_8b", lens=[3000, 129, 64, 1000]), 4,
            num_ctas=num_ctas)
+
+
+@pytest.mark.parametrize("num_ctas", [7, 300])
+def test_fp8_64_rows_forced_splits(oracle, num_ctas):
+    # FP8 cache at 64 rows per KV head (g = 8, 8 new tokens), units split over
+    # CTAs and merged by the combine
+    _check(oracle, inputs.make_workload("llama3_70b_fp8", lens=[5000, 1500, 9]), 8,
+           num_ctas=num_ctas)
+
+
+def test_fp8_64_rows_full_size_sampled(oracle):
+    # the benchmark's FP8 multi-token launch (batch 32 x 8192, default CTAs);
+    # the oracle checks three sampled sequences, every row of each
+    wl = inputs.make_workload("llama3_70b_fp8")
+    _check(oracle, wl, 8, seqs=[0, 13, 31])
 
 
 def test_short_sequences(oracle):

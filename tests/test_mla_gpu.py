@@ -76,6 +76,21 @@ def test_bad_block_id_flagged_and_finite():
     assert np.isfinite(out).all()
 
 
+@pytest.mark.parametrize("batch", [1500, 5000])
+def test_large_batches_reach_every_planner_path(oracle, batch):
+    # More than 1,024 sequences take the planner's multi-pass prefix scan and
+    # 4,096 or more its prefix array in global memory.  With more sequences
+    # than CTA pairs the balanced split runs (several sequences per pair, some
+    # split between pairs and merged in the kernel).  16 heads keep the oracle
+    # fast; every sequence is compared.
+    lens = inputs.rng_for(batch, "large-batch lens").integers(0, 131, size=batch)
+    wl = inputs.make_workload("deepseek_v3_mla", lens=lens.tolist(), heads=16)
+    g, out, lse = _check(oracle, wl)
+    empty = np.nonzero(lens == 0)[0]
+    assert len(empty) > 0
+    assert (out[empty] == 0).all() and np.isneginf(lse[empty]).all()
+
+
 def test_split_count_does_not_change_result_beyond_rounding():
     wl = inputs.make_workload("deepseek_v3_mla", lens=[3000, 5000, 100])
     g = GpuWorkload(wl)

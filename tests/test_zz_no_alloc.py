@@ -65,6 +65,40 @@ def test_noalloc_matches_workspace_entry_on_consecutive_calls():
         assert np.abs(l[fin] - ref_lse[fin]).max() <= TOL_ABS
 
 
+def test_noalloc_back_to_back_calls_with_split_units():
+    # Two problems enqueued one right after the other on one stream, with no
+    # synchronisation between them, both split over 8 CTAs so that each runs
+    # its combine over partials in the shared array.  The second call's planner
+    # must not overwrite the plan or the partials while the first call's
+    # combine still reads them; each result is checked against its own
+    # caller-workspace result after one final synchronisation.
+    import torch
+    lib = kv.load_library()
+    cases = [inputs.make_workload("llama3_8b", lens=[4000, 37, 1024, 0, 777]),
+             inputs.make_workload("llama3_70b", lens=[3000, 2500, 64])]
+    gs = [GpuWorkload(wl) for wl in cases]
+    refs = [g.decode(num_ctas=8) for g in gs]
+    outs = []
+    for g in gs:
+        wl = g.wl
+        g.err.zero_()
+        outs.append((torch.full((wl.B, wl.h, wl.d), float("nan"), dtype=torch.float32,
+                                device="cuda"),
+                     torch.full((wl.B, wl.h), float("nan"), dtype=torch.float32, device="cuda")))
+    torch.cuda.synchronize()
+    for g, (out, lse) in zip(gs, outs):
+        assert _call_noalloc(lib, g, out, lse, num_ctas=8) == kv.KVATTN_OK
+    torch.cuda.synchronize()
+    for g, (out, lse), (ref_out, ref_lse) in zip(gs, outs, refs):
+        assert g.err_bits() == 0
+        o, l = out.cpu().numpy(), lse.cpu().numpy()
+        assert np.isfinite(o).all()
+        assert _close(o, ref_out)
+        fin = np.isfinite(ref_lse)
+        assert (np.isneginf(l) == np.isneginf(ref_lse)).all()
+        assert np.abs(l[fin] - ref_lse[fin]).max() <= TOL_ABS
+
+
 def test_noalloc_rejects_problems_beyond_the_scratch():
     import torch
     lib = kv.load_library()
