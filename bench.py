@@ -465,7 +465,7 @@ def time_all_configs(args, sampler, headline, dev):
     sink = torch.empty((), dtype=torch.int64, device=dev)
 
     def flush():
-        torch.sum(flush_buf, dtype=torch.int64, out=sink)
+        torch.sum(flush_buf, dim=0, dtype=torch.int64, out=sink)
 
     n = max(50, args.steps)
     res = {}
