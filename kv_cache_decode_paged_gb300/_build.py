@@ -52,6 +52,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(BUILD, exist_ok=True)
     exe = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    # extra nvcc flags for tuning sweeps (e.g. -D overrides of kernel constants)
+    extra += os.environ.get("KVATTN_NVCC_EXTRA", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))

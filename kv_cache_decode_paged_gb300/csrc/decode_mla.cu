@@ -23,26 +23,29 @@
 // with bulk copies; both ranks add the same two f16 partials, so their softmax
 // inputs and P are bit-identical.
 //
-// Measured on GB300: a K = 16 MMA with M = 128 reading both operands from
-// shared memory costs ~78 cycles for any N <= 128 (and 128 cycles at N = 256);
-// with A in tensor memory ~123 cycles for N <= 128 and ~136 at N = 256.  A
-// bulk copy into the peer's shared memory takes ~0.6 us to land, while loads
-// from the peer's shared memory and release-ordered remote arrives each cost
-// about as much again, so partials are pushed, never pulled.  The exchange of
-// tile t+1 overlaps the softmax of tile t: a push lands well within a tile, so
-// one staging buffer suffices, and each softmax warp hands its share of the
-// receive slot back as soon as it holds the values in registers.  Four value
-// stages fit because the first 64 c_KV dims of this rank's Q sit in TMEM
-// (score K steps 2..5 read A from TMEM), the other 192 and the 32 rope dims in
-// shared memory.
+// Measured on GB300 (unrolled issue, one SM): a K = 16 MMA with M = 128 takes
+// ~48 cycles at N = 64, ~67 at N = 128 and ~131 at N = 256, with A in shared
+// memory or in tensor memory alike; with the P.V chain of another tile issued
+// beside it a tile's 22 MMAs occupy the tensor core ~1,300 cycles.  A bulk
+// copy into the peer's shared memory lands ~0.6 us after issue, and loads from
+// the peer's shared memory or release-ordered remote arrives cost about as
+// much, so partials are pushed, never pulled; per-thread asynchronous remote
+// stores (st.async) measured slower than staging plus one bulk copy per warp.
+// Two staging and two receive slots let the exchange of tile t+1 start while
+// tile t is still in the peer's receive slot.  The first 192 c_KV dims of this
+// rank's Q sit in TMEM (score K steps 2..13 read A from TMEM), the other 64
+// and the 32 rope dims in shared memory; that leaves room for four value
+// stages.  A tile's value stage lives from its load until its P.V completes
+// (load ~0.9 us, score MMAs, exchange, softmax, P.V: ~4.4 us in a timeline
+// trace), which with four stages sets the period of ~1.1 us per tile.
 //   warp 0      TMA producer: per sequence the shared-memory part of Q; per
 //               tile 4 value boxes (4-stage ring) and one rope box (2-slot
 //               ring, freed once S is computed)
 //   warp 1      TMEM owner and S issuer: S(t) into one of two S slots
-//   warp 14     P.V issuer: P.V(t) with P from one of two P slots
-//   warps 10-13 senders: per sequence Q[:, 256r : 256r + 64] into TMEM; per
-//               tile S(t) partial -> f16 -> staging -> bulk copy to the peer
-//               (one thread per head row)
+//   warp 14     P.V issuer: P.V(t) with P from the P slot
+//   warps 10-13 senders: per sequence Q[:, 256r : 256r + 192] into TMEM; per
+//               tile S(t) partial -> f16 -> staging slot -> bulk copy to the
+//               peer (one thread per head row)
 //   warps 2-9   softmax: peer partial + own partial, online softmax with lazy
 //               rescaling, P(t) -> TMEM, epilogue (two threads per head row,
 //               32 of the tile's 64 rows each)
@@ -68,12 +71,18 @@ constexpr int QF_BYTES = 128 * 128;    // Q box [128 heads x 64 dims], 128-byte 
 constexpr int QH_BYTES = 128 * 64;     // Q box [128 heads x 32 rope dims], 64-byte swizzle
 constexpr int VF_BYTES = BS * 128;     // latent box [64 rows x 64 dims]
 constexpr int RH_BYTES = BS * 64;      // latent box [64 rows x 32 rope dims]
-constexpr int NQT = 4;                                    // score K steps with Q in TMEM
+#ifndef KV_MLA_NQT
+#define KV_MLA_NQT 12
+#endif
+#ifndef KV_MLA_NSTAGE
+#define KV_MLA_NSTAGE 4
+#endif
+constexpr int NQT = KV_MLA_NQT;                           // score K steps with Q in TMEM
 constexpr int NQF = 4 - NQT / 4;                          // Q boxes in shared memory
 constexpr int OFF_QF = 0;                                 // Q dims 256r+16*NQT .. 256r+255
 constexpr int OFF_QH = NQF * QF_BYTES;                    // Q rope dims
-constexpr int Q_BYTES = NQF * QF_BYTES + QH_BYTES;        // 56 KB
-constexpr int NSTAGE = 4;                                 // value ring
+constexpr int Q_BYTES = NQF * QF_BYTES + QH_BYTES;        // 24 KB
+constexpr int NSTAGE = KV_MLA_NSTAGE;                     // value ring
 constexpr int VSTAGE = 4 * VF_BYTES;                      // 32 KB
 // The value ring is laid out box-major: box i (dims 64i .. 64i+63 of this
 // rank) of stage s sits at OFF_V + i * VBOX + s * VF_BYTES, so that the rows
@@ -84,11 +93,12 @@ constexpr int NROPE = 2;                                  // rope ring
 constexpr int OFF_R = OFF_V + NSTAGE * VSTAGE;
 constexpr int XROW = BS * 2;                              // a row of a partial tile, f16
 constexpr int XBYTES = 128 * XROW;                        // 16 KB
-constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // receive slot (the peer writes)
-constexpr int OFF_XS = OFF_X + XBYTES;                    // send staging
-constexpr int OFF_MX = OFF_XS + XBYTES;                   // row max / row sum exchange
+constexpr int NX = 2;                                     // exchange ring depth
+constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // receive slots (the peer writes)
+constexpr int OFF_XS = OFF_X + NX * XBYTES;               // send staging slots
+constexpr int OFF_MX = OFF_XS + NX * XBYTES;              // row max / row sum exchange
 constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
-constexpr int NBARS = 32;
+constexpr int NBARS = 40;
 constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
 constexpr int NSW = 256;               // softmax warps: two threads per head row
 constexpr int NSEND = 128;             // sender warps: one thread per head row
@@ -98,9 +108,10 @@ constexpr int THREADS = 64 + NSW + NSEND + 32;
 constexpr int KSTEPS = 18;             // 288 score dims per rank / 16
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;           // two S slots of 64 columns
-constexpr uint32_t TM_P = 128;         // two P slots of 32 columns (bf16 pairs)
-constexpr uint32_t TM_Q = 192;         // Q dims 256r .. 256r+16*NQT-1 (bf16 pairs)
+constexpr uint32_t TM_Q = 128;         // Q dims 256r .. 256r+16*NQT-1 (bf16 pairs)
+constexpr uint32_t TM_P = 224;         // one P slot of 32 columns (bf16 pairs)
 constexpr uint32_t TM_O = 256;         // O half: columns 256..511
+static_assert(TM_Q + 8 * NQT <= TM_P && NQT % 4 == 0 && NQT <= 16, "Q columns in TMEM");
 constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the max grows by 2^8
 static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
                   OFF_XS % 1024 == 0,
@@ -134,14 +145,14 @@ enum : int {
   kQFull = 0, kQEmpty = 1, kOFree = 2,
   kSFull0 = 3,      // 2: S(t) landed in S slot t % 2
   kSRead0 = 5,      // 2: the senders and the softmax warps have read S slot t % 2
-  kPFull0 = 7,      // 2: P(t) written to P slot t % 2
-  kPVDone0 = 9,     // 2: P.V of tile t finished
-  kXFull = 11,      // the peer's partial of tile t is in the receive slot (tx bytes)
-  kXEmpty = 12,     // the peer has read this rank's partial of tile t from its receive slot
-  kXSent = 13,      // the peer has received this rank's partial of tile t: staging is free
-  kQTmem = 15,      // the sender warps have written this sequence's Q columns to TMEM
-  kMmaDrain = 16,   // 2: each MMA issuer's last operations completed (exit path)
-  kKVFull0 = 18,                          // NSTAGE: value boxes (and rope box) landed
+  kPFull0 = 7,      // 2: P(t) written to the P slot (barrier t % 2)
+  kPVDone0 = 9,     // 2: P.V of tile t finished (barrier t % 2)
+  kXFull0 = 11,     // 2: the peer's partial of tile t is in receive slot t % 2 (tx bytes)
+  kXEmpty0 = 13,    // 2: the peer has read this rank's partial of tile t (slot t % 2)
+  kXSent0 = 15,     // 2: the peer has received the copy from staging slot t % 2
+  kQTmem = 17,      // the sender warps have written this sequence's Q columns to TMEM
+  kMmaDrain = 18,   // 2: each MMA issuer's last operations completed (exit path)
+  kKVFull0 = 20,                          // NSTAGE: value boxes (and rope box) landed
   kKVEmpty0 = kKVFull0 + mla::NSTAGE,     // NSTAGE: P.V finished with the value stage
   kRopeEmpty0 = kKVEmpty0 + mla::NSTAGE,  // 2: S finished with the rope slot
   kAbort = kRopeEmpty0 + 2,               // an int flag in this slot
@@ -183,13 +194,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int pair = blockIdx.x >> 1;
-  // Launched right behind the planner: wait for its plan, and let the combine
-  // that follows get scheduled while this grid runs.
-  pdl_wait();
-  pdl_launch_dependents();
-  const int4 st = p.cta_start[pair], en = p.cta_start[pair + 1];
-  if (!pos_less(st, en)) return;  // both ranks of the pair take the same exit
-
+  // Set-up that needs nothing from the planner runs before waiting for it:
+  // barriers, descriptors, tensor memory and the cluster handshake.
   if (threadIdx.x == 0) {
     mbar_init(&bars[kQFull], 1);
     mbar_init(&bars[kQEmpty], 1);
@@ -201,9 +207,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       mbar_init(&bars[kPVDone0 + i], 1);
       mbar_init(&bars[kRopeEmpty0 + i], 1);
     }
-    mbar_init(&bars[kXFull], 1);           // one local expect_tx arrival + the peer's bytes
-    mbar_init(&bars[kXSent], 1);           // one arrival from the peer's softmax warps
-    mbar_init(&bars[kXEmpty], NSW / 32);   // one arrival per softmax warp of the peer
+    for (int i = 0; i < NX; ++i) {
+      mbar_init(&bars[kXFull0 + i], 1);           // one local expect_tx arrival + the peer's bytes
+      mbar_init(&bars[kXEmpty0 + i], NSW / 32);   // one arrival per softmax warp of the peer
+      mbar_init(&bars[kXSent0 + i], 1);           // one arrival from the peer
+    }
     mbar_init(&bars[kQTmem], NSEND / 32);
     mbar_init(&bars[kMmaDrain], 1);
     mbar_init(&bars[kMmaDrain + 1], 1);
@@ -213,7 +221,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
-    mbar_arrive_expect_tx(&bars[kXFull], XBYTES);       // the peer's tile 0
+    tma_prefetch_desc(&tmQF);
+    tma_prefetch_desc(&tmQH);
+    tma_prefetch_desc(&tmLF);
+    tma_prefetch_desc(&tmLH);
+    for (int i = 0; i < NX; ++i) mbar_arrive_expect_tx(&bars[kXFull0 + i], XBYTES);  // tiles 0, 1
   }
   __syncwarp();  // warp 0 reconverges before the warp-aligned instructions below
   if (warp == 1) {
@@ -225,6 +237,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   // visible to the other before any remote access.
   cluster_sync_all();
   tc_fence_after();
+  // Launched right behind the planner: wait for its plan, and let whatever
+  // follows get scheduled while this grid runs.
+  pdl_wait();
+  pdl_launch_dependents();
+  const int4 st = p.cta_start[pair], en = p.cta_start[pair + 1];
+  if (!pos_less(st, en)) {   // both ranks of the pair take the same exit
+    if (warp == 1) tmem_dealloc(*tmem_slot, TMEM_COLS);
+    return;
+  }
   const uint32_t tmem = *tmem_slot;
   const int vx0 = 256 * int(rank);       // first value dim of this rank
   const int rx = 512 + 32 * int(rank);   // first rope dim of this rank
@@ -232,10 +253,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmQF);
-      tma_prefetch_desc(&tmQH);
-      tma_prefetch_desc(&tmLF);
-      tma_prefetch_desc(&tmLH);
       const uint64_t pol = policy_evict_first();
       Walker w{p.cum, 1, st, en};
       Seg sg;
@@ -367,7 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             tc_fence_after();
             // O[:, 256r:+256] (+)= P(t) . c(t)[:, 256r:+256]  (4 MMAs, A = P from TMEM)
             const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VF_BYTES, VBOX, 1024);
-            const uint32_t pa = tmem + TM_P + 32 * (t & 1);
+            const uint32_t pa = tmem + TM_P;
 #pragma unroll
             for (int kk = 0; kk < BS / 16; ++kk)
               umma_ts(tmem + TM_O, pa + 8 * kk, vb0 + uint64_t((kk * 2048) >> 4), id_o,
@@ -393,9 +410,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     // ---------------------------------------------------------------- senders
     const int r = 32 * (warp & 3) + lane;          // head row = TMEM lane
     const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-    uint8_t* xstage = smem + OFF_XS;
     const uint32_t xbuf_peer = map_peer(smem_u32(smem + OFF_X), peer);
-    const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull]), peer);
+    const uint32_t xfull_peer = map_peer(smem_u32(&bars[kXFull0]), peer);
     auto wait_all = [](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
     };
@@ -452,25 +468,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         // the abort flag is read by every lane but decided for the warp
         good = good && !__any_sync(0xffffffffu, *abort_flag != 0);
         if (!good) { ok = false; break; }
-        // Staging is free once the peer has received the previous partial (it
-        // lands ~0.6 us after its push, well within a tile); the push then waits
-        // until the peer has read the previous partial out of its receive slot.
-        // Both signals only say that reads have finished, so waits at CTA scope
-        // suffice.  Each warp stages and pushes its own 32 rows (4 KB): no
-        // barrier across the sender warps; the peer's barrier counts the bytes
-        // of all four.
-        if (u > 0 && !wait_all(&bars[kXSent], (u - 1) & 1)) { ok = false; break; }
-        uint8_t* sbuf = xstage;
+        // Two staging slots and two receive slots: partial u goes through
+        // staging slot u % 2 into the peer's receive slot u % 2.  The staging
+        // slot is free once the peer has received the copy of partial u - 2,
+        // the receive slot once the peer has read partial u - 2 out of it (both
+        // signals say that reads have finished, so waits at CTA scope suffice),
+        // so the round trip of one exchange overlaps the next.  Each warp stages
+        // and pushes its own 32 rows (4 KB): no barrier across the sender warps;
+        // the peer's barrier counts the bytes of all four.
+        const uint32_t xs = u % NX;
+        if (u >= uint32_t(NX) && !wait_all(&bars[kXSent0 + xs], ((u - NX) / NX) & 1)) { ok = false; break; }
+        uint8_t* sbuf = smem + OFF_XS + xs * XBYTES;
         uint4* srow = reinterpret_cast<uint4*>(sbuf + r * XROW);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           srow[c ^ (r & 7)] = make_uint4(hx[4 * c], hx[4 * c + 1], hx[4 * c + 2], hx[4 * c + 3]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (u > 0 && !wait_all(&bars[kXEmpty], (u - 1) & 1)) { ok = false; break; }
+        if (u >= uint32_t(NX) && !wait_all(&bars[kXEmpty0 + xs], ((u - NX) / NX) & 1)) { ok = false; break; }
         __syncwarp();
         if (lane == 0) {
           const uint32_t off = uint32_t(32 * (warp & 3)) * XROW;
-          bulk_copy_to_peer(xbuf_peer + off, sbuf + off, 32 * XROW, xfull_peer);
+          bulk_copy_to_peer(xbuf_peer + xs * XBYTES + off, sbuf + off, 32 * XROW,
+                            xfull_peer + xs * 8u);
         }
       }
     }
@@ -479,9 +498,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       *abort_flag = 1;
     }
     // Drain: the peer's last arrivals on this CTA's barriers (received / read)
-    if (u > 0) {
-      mbar_wait_cluster(&bars[kXSent], (u - 1) & 1);
-      mbar_wait_cluster(&bars[kXEmpty], (u - 1) & 1);
+    // for the last partials pushed
+    for (uint32_t k = u > uint32_t(NX) ? u - NX : 0; k < u; ++k) {
+      mbar_wait_cluster(&bars[kXSent0 + k % NX], (k / NX) & 1);
+      mbar_wait_cluster(&bars[kXEmpty0 + k % NX], (k / NX) & 1);
     }
   } else {
     // ------------------------------------------ softmax / epilogue warps (2..9)
@@ -491,8 +511,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     const int tid = threadIdx.x - SW0;             // 0..255
     const uint8_t* xbuf = smem + OFF_X;
     float* mx_s = reinterpret_cast<float*>(smem + OFF_MX);   // [2][128]
-    const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty]), peer);
-    const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent]), peer);
+    const uint32_t xempty_peer = map_peer(smem_u32(&bars[kXEmpty0]), peer);
+    const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent0]), peer);
     Walker w{p.cum, 1, st, en};
     Seg sg;
     uint32_t it = 0, received = 0;
@@ -528,21 +548,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         }
         // The peer's bulk copy writes this CTA's shared memory and completes on
         // this CTA's barrier: observing the phase makes the bytes visible.
-        good = good && wait_all(&bars[kXFull], t & 1);
+        const uint32_t xs = t % NX;
+        good = good && wait_all(&bars[kXFull0 + xs], (t / NX) & 1);
         received += good ? 1u : 0u;
         if (good && tid == 0) {
-          // the bulk copy has landed, so it has read the peer's staging buffer
-          mbar_arrive_remote_relaxed(xsent_peer);
-          // arm for tile t + 1: the peer pushes it only after this rank's
-          // receive slot is released below, after every thread saw this phase
-          mbar_arrive_expect_tx(&bars[kXFull], XBYTES);
+          // the bulk copy has landed, so it has read the peer's staging slot
+          mbar_arrive_remote_relaxed(xsent_peer + xs * 8u);
+          // arm for tile t + NX: the peer pushes it into this slot only after
+          // the slot is released below, after every thread saw this phase
+          mbar_arrive_expect_tx(&bars[kXFull0 + xs], XBYTES);
         }
         // hs: f16 pairs of full raw scores, tokens 32hh + 2j and + 2j + 1
         uint32_t hs[16];
         float mx = -INFINITY;
         if (good) {
           const int valid = len - (sg.j0 + int(k)) * BS - 32 * hh;
-          const uint4* xr = reinterpret_cast<const uint4*>(xbuf + r * XROW);
+          const uint4* xr = reinterpret_cast<const uint4*>(xbuf + xs * XBYTES + r * XROW);
           uint4 pv[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) pv[c] = xr[(4 * hh + c) ^ (r & 7)];
@@ -550,7 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           // share of the receive slot, so that the peer can push the next
           // partial while this tile's softmax goes on.
           __syncwarp();
-          if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer);
+          if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer + xs * 8u);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             hs[4 * c] = hadd2_u32(own[4 * c], pv[c].x);
@@ -608,8 +629,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             m_ref = m_new;
           }
         }
-        // P slot t % 2 was last read by P.V(t - 2)
-        good = good && (t < 2 || wait_all(&bars[kPVDone0 + slot], ((t - 2) >> 1) & 1));
+        // the P slot was last read by P.V(t - 1)
+        good = good && (t < 1 || wait_all(&bars[kPVDone0 + ((t - 1) & 1)], ((t - 1) >> 1) & 1));
         if (good) {
           tc_fence_after();
           uint32_t pk[16];
@@ -623,7 +644,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             pk[j] = pack_bf16(p0, p1);
           }
           l += lsum;
-          tmem_st16(tmem + lane_off + TM_P + 32 * slot + 16 * hh, pk);
+          tmem_st16(tmem + lane_off + TM_P + 16 * hh, pk);
           tmem_st_wait();
           const int vt = len - (sg.j0 + int(k)) * BS;   // valid rows of the whole tile
           if (vt < BS) {
@@ -701,7 +722,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             tma_store_3d(&tmO, ob + cb * (32 * 128), 256 * int(rank) + 128 * hh + 32 * cb,
                          32 * (warp & 3), sg.b);
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read();   // the staging is reused; the stores themselves finish on their own
         }
         __syncwarp();
       } else {
@@ -739,14 +760,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     if (!ok) {
       report(p.err, KVATTN_DEVERR_TIMEOUT);
       *abort_flag = 1;
-      // The peer may have pushed one partial that was not consumed (it pushes
-      // the next only after this rank released the receive slot); it lands
-      // before this CTA's shared memory goes away.
+      // The peer may have pushed up to NX partials that were not consumed (it
+      // pushes into a receive slot only after this rank released it); they
+      // land before this CTA's shared memory goes away.
       uint32_t total = 0;
       Walker w2{p.cum, 1, st, en};
       Seg s2;
       while (w2.next(s2)) total += uint32_t(s2.j1 - s2.j0);
-      if (received < total) mbar_wait_cluster(&bars[kXFull], received & 1);
+      for (uint32_t k = received; k < total && k < received + NX; ++k)
+        mbar_wait_cluster(&bars[kXFull0 + k % NX], (k / NX) & 1);
     } else {
       // Publish this rank's halves of the partials it wrote and merge the
       // groups and sequences they complete (merge.cuh): each rank merges its
