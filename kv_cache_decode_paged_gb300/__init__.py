@@ -271,12 +271,17 @@ class PagedCache:
                    v_scale=v_scale, k=k, v=v)
 
     @classmethod
-    def allocate_mla(cls, num_blocks, block_size, d_c=512, d_rope=64, device="cuda", fill_bits=None):
+    def allocate_mla(cls, num_blocks, block_size, d_c=512, d_rope=64, dtype=KVATTN_BF16,
+                     k_scale=1.0, v_scale=1.0, device="cuda", fill_bits=None):
+        """MLA latent pool; for an E4M3 pool k_scale scales the c_KV codes and
+        v_scale the k_R codes."""
         import torch
-        lat = torch.empty((num_blocks, block_size, d_c + d_rope), dtype=torch.int16, device=device)
+        tdt = torch.uint8 if dtype == KVATTN_FP8_E4M3 else torch.int16
+        lat = torch.empty((num_blocks, block_size, d_c + d_rope), dtype=tdt, device=device)
         if fill_bits is not None:
-            lat.fill_(_signed(fill_bits, torch.int16))
-        return cls(KVATTN_MLA, KVATTN_BF16, num_blocks, block_size, d_c=d_c, d_rope=d_rope, latent=lat)
+            lat.fill_(_signed(fill_bits, tdt))
+        return cls(KVATTN_MLA, dtype, num_blocks, block_size, d_c=d_c, d_rope=d_rope,
+                   k_scale=k_scale, v_scale=v_scale, latent=lat)
 
     def descriptor(self) -> kvattn_cache:
         return kvattn_cache(self.kind, self.dtype, self.num_blocks, self.block_size, self.h_kv,

@@ -201,7 +201,9 @@ extern "C" kvattn_status kvattn_decode_mla(const void* q_absorbed, const kvattn_
   if (!aligned(q_absorbed, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
       !aligned(cache->latent, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4))
     return KVATTN_ERR_INVALID_ARG;
-  if (cache->dtype != KVATTN_BF16) return KVATTN_ERR_UNSUPPORTED;
+  if (cache->dtype != KVATTN_BF16 && cache->dtype != KVATTN_FP8_E4M3) return KVATTN_ERR_UNSUPPORTED;
+  if (cache->dtype == KVATTN_FP8_E4M3 && !(cache->k_scale > 0.f && cache->v_scale > 0.f))
+    return KVATTN_ERR_INVALID_ARG;
   if (d_c != 512 || d_rope != 64 || h > 128) return KVATTN_ERR_UNSUPPORTED;
   if (cache->block_size != 64) return KVATTN_ERR_UNSUPPORTED;
   if (cache->num_blocks >= INT_MAX / 64) return KVATTN_ERR_UNSUPPORTED;

@@ -48,11 +48,6 @@ __device__ __forceinline__ int64_t resolve_block(const AppendArgs& a, int64_t n)
   return blk;
 }
 
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 
 __device__ __forceinline__ uint2 quantize8(uint4 x, float scale) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -92,6 +87,10 @@ __global__ void __launch_bounds__(256) append_gqa_kernel(AppendArgs a) {
   }
 }
 
+// MLA rows [c_KV | k_R]; an FP8 pool quantises c_KV with k_scale and k_R with
+// v_scale (one per-tensor scale each: "MLA 与 KV Cache 量化可以叠加" quantises the
+// latent and the RoPE key separately).
+template <bool FP8>
 __global__ void __launch_bounds__(256) append_mla_kernel(AppendArgs a) {
   const int cc = a.d / 8, cr = a.d_rope / 8, width = a.d + a.d_rope;
   const int chunks = cc + cr;
@@ -103,10 +102,14 @@ __global__ void __launch_bounds__(256) append_mla_kernel(AppendArgs a) {
     const int64_t blk = resolve_block(a, n);
     if (blk < 0) continue;
     const int t = a.pos[n];
-    uint16_t* row = static_cast<uint16_t*>(a.dst0) + (blk * a.bs + t % a.bs) * int64_t(width);
+    const int64_t row0 = (blk * a.bs + t % a.bs) * int64_t(width);
     const uint4 x = c < cc ? reinterpret_cast<const uint4*>(a.src0 + n * a.d)[c]
                            : reinterpret_cast<const uint4*>(a.src1 + n * a.d_rope)[c - cc];
-    reinterpret_cast<uint4*>(row)[c] = x;
+    if (FP8)
+      reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.dst0) + row0)[c] =
+          quantize8(x, c < cc ? a.k_scale : a.v_scale);
+    else
+      reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.dst0) + row0)[c] = x;
   }
 }
 
@@ -163,18 +166,25 @@ extern "C" kvattn_status kvattn_append(const kvattn_cache* cache, const void* k_
     else
       append_gqa_kernel<false><<<blocks, threads, 0, s>>>(a);
   } else if (cache->kind == KVATTN_MLA) {
-    if (cache->dtype != KVATTN_BF16) return KVATTN_ERR_UNSUPPORTED;
+    if (cache->dtype != KVATTN_BF16 && cache->dtype != KVATTN_FP8_E4M3) return KVATTN_ERR_UNSUPPORTED;
     if (cache->d_c <= 0 || cache->d_rope < 0 || cache->d_c % 8 || cache->d_rope % 8 || !cache->latent)
       return KVATTN_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(cache->latent) & 15) return KVATTN_ERR_INVALID_ARG;
+    const bool fp8 = cache->dtype == KVATTN_FP8_E4M3;
+    if (reinterpret_cast<uintptr_t>(cache->latent) & (fp8 ? 7 : 15)) return KVATTN_ERR_INVALID_ARG;
+    if (fp8 && !(cache->k_scale > 0.f && cache->v_scale > 0.f)) return KVATTN_ERR_INVALID_ARG;
     a.h_kv = 1;
     a.d = cache->d_c;
     a.d_rope = cache->d_rope;
+    a.k_scale = cache->k_scale;
+    a.v_scale = cache->v_scale;
     a.dst0 = cache->latent;
     work = n_tokens * ((a.d + a.d_rope) / 8);
     const int64_t blocks64 = (work + threads - 1) / threads;
     const int blocks = int(blocks64 < (1 << 20) ? blocks64 : (1 << 20));
-    append_mla_kernel<<<blocks, threads, 0, s>>>(a);
+    if (fp8)
+      append_mla_kernel<true><<<blocks, threads, 0, s>>>(a);
+    else
+      append_mla_kernel<false><<<blocks, threads, 0, s>>>(a);
   } else {
     return KVATTN_ERR_INVALID_ARG;
   }

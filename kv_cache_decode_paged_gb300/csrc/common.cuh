@@ -199,6 +199,22 @@ KV_DEVI uint32_t pack_f16(float lo, float hi) {
   return r;
 }
 
+// Two floats to two FP8-E4M3 codes, round to nearest even, saturating to
+// +-448 (E4M3 has no infinity); `lo` lands in the low byte.
+KV_DEVI uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes (low byte first) to an f16 pair; exact, every E4M3 value is
+// an f16 value.
+KV_DEVI uint32_t e4m3x2_to_f16x2(uint16_t pair) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
+}
+
 // 2^x (PTX ex2.approx; 2^-inf = +0).
 KV_DEVI float exp2_approx(float x) {
   float y;

@@ -76,14 +76,8 @@ struct GqaCfg {
 // Rescale O only when a row's running max grows by more than 2^8.
 constexpr float kRescaleLog2 = 8.f;
 
-// Two E4M3 codes -> an f16 pair, exactly (every E4M3 value, subnormals and
-// NaN included, is representable in f16): the hardware conversion of a packed
-// byte pair, low byte to the low half.
-KV_DEVI uint32_t e4m3x2_to_f16x2(uint16_t pair) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
-  return r;
-}
+// (e4m3x2_to_f16x2, common.cuh: the hardware conversion of a packed byte
+// pair, exact for every E4M3 value, subnormals and NaN included)
 // codes 0,1 and 2,3 of w
 KV_DEVI uint32_t e4m3_b01(uint32_t w) { return e4m3x2_to_f16x2(uint16_t(w & 0xffffu)); }
 KV_DEVI uint32_t e4m3_b23(uint32_t w) { return e4m3x2_to_f16x2(uint16_t(w >> 16)); }

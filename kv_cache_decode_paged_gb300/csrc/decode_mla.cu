@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -64,61 +65,104 @@
 namespace kv {
 
 namespace mla {
+// Shared by both cache formats.
 constexpr int ROWW = 576;              // latent row width (d_c + d_rope)
 constexpr int DC = 512;
 constexpr int BS = 64;                 // tokens per page = tokens per tile
-constexpr int QF_BYTES = 128 * 128;    // Q box [128 heads x 64 dims], 128-byte swizzle
-constexpr int QH_BYTES = 128 * 64;     // Q box [128 heads x 32 rope dims], 64-byte swizzle
-constexpr int VF_BYTES = BS * 128;     // latent box [64 rows x 64 dims]
-constexpr int RH_BYTES = BS * 64;      // latent box [64 rows x 32 rope dims]
+constexpr int NROPE = 2;               // rope ring
+constexpr int XROW = BS * 2;           // a row of a partial tile, f16
+constexpr int XBYTES = 128 * XROW;     // 16 KB
+constexpr int NX = 2;                  // exchange ring depth
+constexpr int NBARS = 48;
+constexpr int NSTAGE_MAX = 8;          // barrier slots reserved per value stage ring
+constexpr int NSW = 256;               // softmax warps: two threads per head row
+constexpr int NSEND = 128;             // sender warps: one thread per head row
+constexpr int SW0 = 64, SEND0 = 64 + NSW;
+constexpr int PV_WARP = (SEND0 + NSEND) / 32;   // the P.V issuer
+constexpr int THREADS = 64 + NSW + NSEND + 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0;           // two S slots of 64 columns
+constexpr uint32_t TM_Q = 128;         // the TMEM part of this rank's Q
+constexpr uint32_t TM_P = 224;         // one P slot of 32 columns
+constexpr uint32_t TM_O = 256;         // O half: columns 256..511
+constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the max grows by 2^8
+
 #ifndef KV_MLA_NQT
 #define KV_MLA_NQT 12
 #endif
 #ifndef KV_MLA_NSTAGE
 #define KV_MLA_NSTAGE 4
 #endif
-constexpr int NQT = KV_MLA_NQT;                           // score K steps with Q in TMEM
-constexpr int NQF = 4 - NQT / 4;                          // Q boxes in shared memory
-constexpr int OFF_QF = 0;                                 // Q dims 256r+16*NQT .. 256r+255
-constexpr int OFF_QH = NQF * QF_BYTES;                    // Q rope dims
-constexpr int Q_BYTES = NQF * QF_BYTES + QH_BYTES;        // 24 KB
-constexpr int NSTAGE = KV_MLA_NSTAGE;                     // value ring
-constexpr int VSTAGE = 4 * VF_BYTES;                      // 32 KB
-// The value ring is laid out box-major: box i (dims 64i .. 64i+63 of this
-// rank) of stage s sits at OFF_V + i * VBOX + s * VF_BYTES, so that the rows
-// of two consecutive stages form one 128-row operand.
-constexpr int VBOX = NSTAGE * VF_BYTES;
-constexpr int OFF_V = Q_BYTES;
-constexpr int NROPE = 2;                                  // rope ring
-constexpr int OFF_R = OFF_V + NSTAGE * VSTAGE;
-constexpr int XROW = BS * 2;                              // a row of a partial tile, f16
-constexpr int XBYTES = 128 * XROW;                        // 16 KB
-constexpr int NX = 2;                                     // exchange ring depth
-constexpr int OFF_X = OFF_R + NROPE * RH_BYTES;           // receive slots (the peer writes)
-constexpr int OFF_XS = OFF_X + NX * XBYTES;               // send staging slots
-constexpr int OFF_MX = OFF_XS + NX * XBYTES;              // row max / row sum exchange
-constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
-constexpr int NBARS = 40;
-constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
-constexpr int NSW = 256;               // softmax warps: two threads per head row
-constexpr int NSEND = 128;             // sender warps: one thread per head row
-constexpr int SW0 = 64, SEND0 = 64 + NSW;
-constexpr int PV_WARP = (SEND0 + NSEND) / 32;   // the P.V issuer
-constexpr int THREADS = 64 + NSW + NSEND + 32;
-constexpr int KSTEPS = 18;             // 288 score dims per rank / 16
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;           // two S slots of 64 columns
-constexpr uint32_t TM_Q = 128;         // Q dims 256r .. 256r+16*NQT-1 (bf16 pairs)
-constexpr uint32_t TM_P = 224;         // one P slot of 32 columns (bf16 pairs)
-constexpr uint32_t TM_O = 256;         // O half: columns 256..511
-static_assert(TM_Q + 8 * NQT <= TM_P && NQT % 4 == 0 && NQT <= 16, "Q columns in TMEM");
-constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the max grows by 2^8
-static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
-                  OFF_XS % 1024 == 0,
-              "swizzled tiles need 1024-byte alignment");
-static_assert(SMEM <= 232448, "shared memory");
-static_assert((NSW / 32) * 4 * 32 * 128 <= NSTAGE * VSTAGE, "epilogue staging fits the value ring");
-static_assert(merge_scratch_floats(128) * 4 <= NSTAGE * VSTAGE, "merge scratch fits the value ring");
+#ifndef KV_MLA_NSTAGE_FP8
+#define KV_MLA_NSTAGE_FP8 7
+#endif
+
+// Per cache format.  A value stage holds this rank's 256 c_KV dims of one page
+// as boxes of 128-byte rows: bf16 four boxes of 64 dims, E4M3 two boxes of 128.
+template <bool FP8>
+struct Geo;
+template <>
+struct Geo<false> {
+  static constexpr int NVB = 4;                        // value boxes per stage
+  static constexpr int BOX_DIMS = 64;
+  static constexpr int VF_BYTES = BS * 128;            // one box: [64 rows x 64 dims]
+  static constexpr int RH_BYTES = BS * 64;             // rope box [64 rows x this rank's 32 dims]
+  static constexpr int QF_BYTES = 128 * 128;           // Q box [128 heads x 64 dims], 128-byte swizzle
+  static constexpr int QH_BYTES = 128 * 64;            // Q box [128 heads x 32 rope dims], 64-byte swizzle
+  static constexpr int NQT = KV_MLA_NQT;               // score K steps with Q in TMEM
+  static constexpr int NQF = 4 - NQT / 4;              // Q boxes in shared memory
+  static constexpr int Q_BYTES = NQF * QF_BYTES + QH_BYTES;   // 24 KB
+  static constexpr int NSTAGE = KV_MLA_NSTAGE;         // value ring
+  static_assert(TM_Q + 8 * NQT <= TM_P && NQT % 4 == 0 && NQT <= 16, "Q columns in TMEM");
+};
+// E4M3: the query and the probabilities enter the MMAs as two E4M3 terms each
+// (hi = e4m3(x), lo = e4m3(x - hi)); the hi term of Q sits in TMEM (72
+// columns: 288 codes, four per column), the lo term in shared memory.  The
+// rope box carries all 64 rope dims (64-byte rows); each rank multiplies its
+// own 32 of them.
+template <>
+struct Geo<true> {
+  static constexpr int NVB = 2;
+  static constexpr int BOX_DIMS = 128;
+  static constexpr int VF_BYTES = BS * 128;            // one box: [64 rows x 128 codes]
+  static constexpr int RH_BYTES = BS * 64;             // rope box [64 rows x 64 codes]
+  static constexpr int QF_BYTES = 128 * 128;           // lo term, [128 heads x 128 codes]
+  static constexpr int QH_BYTES = 128 * 64;            // lo term, rope [128 heads x 64 B rows]
+  static constexpr int NQF = 2;
+  static constexpr int Q_BYTES = NQF * QF_BYTES + QH_BYTES;   // 40 KB
+  static constexpr int NSTAGE = KV_MLA_NSTAGE_FP8;
+  static_assert(TM_Q + 72 <= TM_P, "Q hi columns in TMEM");
+};
+
+// Shared-memory layout per cache format.
+template <bool FP8>
+struct Lay {
+  using G = Geo<FP8>;
+  static constexpr int VSTAGE = G::NVB * G::VF_BYTES;
+  // The value ring is laid out box-major: box i of stage s sits at
+  // OFF_V + i * VBOX + s * VF_BYTES.
+  static constexpr int VBOX = G::NSTAGE * G::VF_BYTES;
+  static constexpr int OFF_QF = 0;
+  static constexpr int OFF_QH = G::NQF * G::QF_BYTES;
+  static constexpr int OFF_V = G::Q_BYTES;
+  static constexpr int OFF_R = OFF_V + G::NSTAGE * VSTAGE;
+  static constexpr int OFF_X = OFF_R + NROPE * G::RH_BYTES;   // receive slots (the peer writes)
+  static constexpr int OFF_XS = OFF_X + NX * XBYTES;          // send staging slots
+  static constexpr int OFF_MX = OFF_XS + NX * XBYTES;         // row max / row sum exchange
+  static constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
+  static constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
+  static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
+                    OFF_XS % 1024 == 0 && OFF_QH % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(G::NSTAGE <= NSTAGE_MAX, "barrier slots per stage");
+  // The last epilogue stages O (128 KB) in idle shared memory: the value ring
+  // (bf16), or Q and the value ring (E4M3, whose ring is smaller)
+  static constexpr int OFF_EPI = FP8 ? 0 : OFF_V;
+  static_assert(OFF_EPI + (NSW / 32) * 4 * 32 * 128 <= OFF_R, "epilogue staging fits");
+  static_assert(merge_scratch_floats(128) * 4 <= G::NSTAGE * VSTAGE,
+                "merge scratch fits the value ring");
+};
 }  // namespace mla
 
 struct MlaParams {
@@ -137,8 +181,92 @@ struct MlaParams {
   int B, h, max_blocks, G;
   int64_t num_blocks;
   float scale_log2;
+  float c_scale;           // E4M3 cache: value of a c_KV code unit (1 for bf16)
+  float r_ratio;           // E4M3 cache: k_R scale / c_KV scale (1 for bf16)
   int32_t* err;
 };
+
+// E4M3 query of one head row for one rank of the pair: the rank's 256 c_KV
+// dims and 32 rope dims (the rope scaled by r_ratio, so that one accumulator
+// adds both parts in c_KV code units), times 2^e, split into two E4M3 terms
+// hi = e4m3(x) and lo = e4m3(x - hi).  2^e brings the row's largest magnitude
+// into [128, 256), inside E4M3's normal range with room below for lo.  The hi
+// codes go to TMEM (columns TM_Q .. TM_Q + 71, four codes per column: c_KV dims
+// first, rope last), the lo codes to shared memory in the layouts the MMAs
+// read (c_KV: two 128-code atoms with 128-byte rows and swizzle; rope: 64-byte
+// rows with 64-byte swizzle, this rank's codes at bytes 32r .. 32r+31).
+// A partial score times 2^-e is in c_KV code units.  The exponent is computed
+// by q_row_exp, which the softmax warps call too (same inputs, same e).
+KV_DEVI uint4 q_load8(const uint16_t* qrow, bool live, int dim0, int i) {
+  return live ? __ldg(reinterpret_cast<const uint4*>(qrow + dim0) + i) : make_uint4(0, 0, 0, 0);
+}
+KV_DEVI float bf16_half(uint32_t w, int hi) {
+  return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
+}
+KV_DEVI int q_row_exp(const uint16_t* qrow, bool live, uint32_t rank, float r_ratio) {
+  const int c0 = 256 * int(rank), r0 = 512 + 32 * int(rank);
+  float mx = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < 36; ++i) {
+    const uint4 x = i < 32 ? q_load8(qrow, live, c0, i) : q_load8(qrow, live, r0, i - 32);
+    const float f = i < 32 ? 1.f : r_ratio;
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mx = fmaxf(mx, fmaxf(fabsf(bf16_half(w[k], 0) * f), fabsf(bf16_half(w[k], 1) * f)));
+  }
+  return mx > 0.f ? min(max(7 - (int((__float_as_uint(mx) >> 23) & 255) - 127), -120), 120) : 0;
+}
+// Two E4M3 terms of a float pair: hi = e4m3(x), lo = e4m3(x - hi), each a
+// 16-bit code pair (first value in the low byte).
+KV_DEVI void e4m3_two_terms(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = e4m3x2(x0, x1);
+  const uint32_t hf = e4m3x2_to_f16x2(uint16_t(hi));
+  const float2 hd = __half22float2(*reinterpret_cast<const __half2*>(&hf));
+  lo = e4m3x2(x0 - hd.x, x1 - hd.y);
+}
+KV_DEVI void build_q_e4m3(const uint16_t* qrow, bool live, uint32_t rank, float r_ratio, int e,
+                          uint32_t tq, uint8_t* lo_c, uint8_t* lo_r, int r) {
+  const int c0 = 256 * int(rank), r0 = 512 + 32 * int(rank);
+  const float sc = __uint_as_float(uint32_t(127 + e) << 23);
+#pragma unroll 1
+  for (int k = 0; k < 9; ++k) {     // 32 dims at a time: c_KV 0..7, rope 8
+    const float f = k < 8 ? sc : sc * r_ratio;
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = k < 8 ? q_load8(qrow, live, c0 + 32 * k, i) : q_load8(qrow, live, r0, i);
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; j += 2) {
+        // codes 8i + 2j .. 8i + 2j + 3 (two pairs) into word 2i + j / 2
+        uint32_t hw = 0, lw = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint32_t h, l;
+          e4m3_two_terms(bf16_half(w[j + t], 0) * f, bf16_half(w[j + t], 1) * f, h, l);
+          hw |= h << (16 * t);
+          lw |= l << (16 * t);
+        }
+        hi[2 * i + j / 2] = hw;
+        lo[2 * i + j / 2] = lw;
+      }
+    }
+    tmem_st8(tq + 8 * k, hi);
+    if (k < 8) {
+      uint8_t* row = lo_c + (k >> 2) * (128 * 128) + r * 128;
+      const int pc = 2 * (k & 3);
+      *reinterpret_cast<uint4*>(row + ((pc ^ (r & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(row + (((pc + 1) ^ (r & 7)) << 4)) =
+          make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    } else {
+      uint8_t* row = lo_r + r * 64;
+      const int pc = 2 * int(rank), sw = (r >> 1) & 3;
+      *reinterpret_cast<uint4*>(row + ((pc ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(row + (((pc + 1) ^ sw) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    }
+  }
+}
 
 // Barrier indices
 enum : int {
@@ -153,8 +281,8 @@ enum : int {
   kQTmem = 17,      // the sender warps have written this sequence's Q columns to TMEM
   kMmaDrain = 18,   // 2: each MMA issuer's last operations completed (exit path)
   kKVFull0 = 20,                          // NSTAGE: value boxes (and rope box) landed
-  kKVEmpty0 = kKVFull0 + mla::NSTAGE,     // NSTAGE: P.V finished with the value stage
-  kRopeEmpty0 = kKVEmpty0 + mla::NSTAGE,  // 2: S finished with the rope slot
+  kKVEmpty0 = kKVFull0 + mla::NSTAGE_MAX,     // NSTAGE: P.V finished with the value stage
+  kRopeEmpty0 = kKVEmpty0 + mla::NSTAGE_MAX,  // 2: S finished with the rope slot
   kAbort = kRopeEmpty0 + 2,               // an int flag in this slot
   kMergeFlags = kAbort + 1,               // 2 slots: 3 ints for the in-kernel merge
   kNumBars = kMergeFlags + 2
@@ -177,6 +305,7 @@ KV_DEVI uint32_t hmax2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+template <bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmQF,
                       const __grid_constant__ CUtensorMap tmQH,
@@ -184,6 +313,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
                       const __grid_constant__ CUtensorMap tmLH,
                       const __grid_constant__ CUtensorMap tmO, const MlaParams p) {
   using namespace mla;
+  using G = Geo<FP8>;
+  using L = Lay<FP8>;
+  constexpr int NSTAGE = G::NSTAGE, VF_BYTES = G::VF_BYTES, RH_BYTES = G::RH_BYTES;
+  constexpr int QF_BYTES = G::QF_BYTES, NQF = G::NQF, Q_BYTES = G::Q_BYTES;
+  constexpr int VSTAGE = L::VSTAGE, VBOX = L::VBOX, OFF_QF = L::OFF_QF, OFF_QH = L::OFF_QH;
+  constexpr int OFF_V = L::OFF_V, OFF_R = L::OFF_R, OFF_X = L::OFF_X, OFF_XS = L::OFF_XS;
+  constexpr int OFF_MX = L::OFF_MX, OFF_BAR = L::OFF_BAR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -221,8 +357,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
-    tma_prefetch_desc(&tmQF);
-    tma_prefetch_desc(&tmQH);
+    if (!FP8) {   // the E4M3 form builds Q from global memory without TMA
+      tma_prefetch_desc(&tmQF);
+      tma_prefetch_desc(&tmQH);
+    }
     tma_prefetch_desc(&tmLF);
     tma_prefetch_desc(&tmLH);
     for (int i = 0; i < NX; ++i) mbar_arrive_expect_tx(&bars[kXFull0 + i], XBYTES);  // tiles 0, 1
@@ -248,7 +386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   }
   const uint32_t tmem = *tmem_slot;
   const int vx0 = 256 * int(rank);       // first value dim of this rank
-  const int rx = 512 + 32 * int(rank);   // first rope dim of this rank
+  // first rope dim this rank loads: its own 32 (bf16), or all 64 (E4M3)
+  const int rx = FP8 ? 512 : 512 + 32 * int(rank);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -259,12 +398,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       uint32_t it = 0, seg = 0;
       bool ok = true;
       while (ok && w.next(sg)) {
-        if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
-        for (int i = 0; i < NQF; ++i)
-          tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 16 * NQT + 64 * i, 0, sg.b,
-                             &bars[kQFull]);
-        tma_load_3d_nohint(smem + OFF_QH, &tmQH, rx, 0, sg.b, &bars[kQFull]);
+        if constexpr (!FP8) {
+          // bf16: the shared-memory part of Q is loaded as it is (the E4M3
+          // form is built by the sender warps)
+          if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
+          for (int i = 0; i < NQF; ++i)
+            tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 16 * G::NQT + 64 * i, 0,
+                               sg.b, &bars[kQFull]);
+          tma_load_3d_nohint(smem + OFF_QH, &tmQH, rx, 0, sg.b, &bars[kQFull]);
+        }
         const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
         for (int j = sg.j0; j < sg.j1 && ok; ++j, ++it) {
           const int s = it % NSTAGE, q = it & 1;
@@ -281,8 +424,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             page = blk;
           uint8_t* stg = smem + OFF_V + s * VF_BYTES;
           mbar_arrive_expect_tx(&bars[kKVFull0 + s], uint32_t(VSTAGE + RH_BYTES));
-          for (int i = 0; i < 4; ++i)
-            tma_load_3d(stg + i * VBOX, &tmLF, vx0 + 64 * i, 0, page, &bars[kKVFull0 + s], pol);
+          for (int i = 0; i < G::NVB; ++i)
+            tma_load_3d(stg + i * VBOX, &tmLF, vx0 + G::BOX_DIMS * i, 0, page, &bars[kKVFull0 + s],
+                        pol);
           tma_load_3d(smem + OFF_R + q * RH_BYTES, &tmLH, rx, 0, page, &bars[kKVFull0 + s], pol);
           if (*abort_flag) ok = false;
         }
@@ -294,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       }
       // Every load this thread issued lands before the CTA can exit (on the
       // normal path the consumers have waited for all of them already).
-      if (seg > 0) mbar_wait(&bars[kQFull], (seg - 1) & 1);
+      if (!FP8 && seg > 0) mbar_wait(&bars[kQFull], (seg - 1) & 1);
       for (uint32_t k = it > uint32_t(NSTAGE) ? it - NSTAGE : 0; k < it; ++k)
         mbar_wait(&bars[kKVFull0 + k % NSTAGE], (k / NSTAGE) & 1);
     }
@@ -310,43 +454,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       uint32_t it = 0, seg = 0;
       bool ok = true;
       if (warp == 1) {
-        const uint32_t id_s = idesc_bf16(128, BS, false);
+        const uint32_t id_s = FP8 ? idesc_e4m3(128, BS, false) : idesc_bf16(128, BS, false);
         const uint32_t qf = smem_u32(smem + OFF_QF), qh = smem_u32(smem + OFF_QH);
         // Descriptors are built once; a K step only moves the start address,
         // whose field is the low bits of the descriptor (address / 16, no carry
         // below 256 KB).  The issue loop is unrolled: with the address
         // arithmetic in the loop the issue, not the tensor core, set the pace.
         const uint64_t qa0 = sdesc_sw128(qf, 16, 1024), qh0 = sdesc_sw64(qh, 512);
-        // S(t) = Q[:, D_r] . row(t)[:, D_r]^T into S slot t % 2, K steps [J0, J1)
-        // of 18 (K = 16 each).  Steps 0 and 1 are the rope dims, so that the
-        // small rope ring can be refilled as soon as they are done; steps 2..9
-        // take Q from TMEM, 10..17 from shared memory.
+        // E4M3: the rope box and the lo term's rope region have 64-byte rows;
+        // this rank's 32 rope codes are bytes 32r .. 32r+31 of each.
+        const uint64_t rope_k = FP8 ? uint64_t(2 * rank) : 0;
+        // S(t) = Q[:, D_r] . row(t)[:, D_r]^T into S slot t % 2, MMAs [J0, J1)
+        // of 18.  MMAs 0 and 1 cover the rope dims, so that the small rope
+        // ring can be refilled as soon as they are done.
+        //   bf16 (K = 16): MMA j >= 2 covers c_KV dims 16m .. 16m+15 of this
+        //     rank, m = j - 2, with Q from TMEM for m < NQT, else from shared
+        //     memory.
+        //   E4M3 (K = 32): the rope dims and then each 32 c_KV dims m = 0..7
+        //     take two MMAs, the hi term of Q (TMEM) and the lo term (shared
+        //     memory), accumulating into the same S.
         auto issue_s = [&](uint32_t t, auto j0c, auto j1c) {
           constexpr int J0 = decltype(j0c)::value, J1 = decltype(j1c)::value;
           const uint32_t d = tmem + TM_S + BS * (t & 1);
           const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VF_BYTES, 16, 1024);
-          const uint64_t rb0 = sdesc_sw64(r_base + (t & 1) * RH_BYTES, 512);
+          const uint64_t rb0 = sdesc_sw64(r_base + (t & 1) * RH_BYTES, 512) + rope_k;
 #pragma unroll
           for (int j = J0; j < J1; ++j) {
-            if (j < 2) {        // rope dims of this rank
-              umma_ss(d, qh0 + uint64_t((j * 32) >> 4), rb0 + uint64_t((j * 32) >> 4), id_s, j > 0);
+            if constexpr (FP8) {
+              if (j < 2) {
+                if (j == 0)
+                  umma_ts_f8(d, tmem + TM_Q + 64, rb0, id_s, 0u);
+                else
+                  umma_ss_f8(d, qh0 + rope_k, rb0, id_s, 1u);
+              } else {
+                const int m = (j - 2) >> 1;   // c_KV dims 32m .. 32m+31 of this rank
+                const uint64_t b = vb0 + uint64_t(((m >> 2) * VBOX + (m & 3) * 32) >> 4);
+                if (((j - 2) & 1) == 0)
+                  umma_ts_f8(d, tmem + TM_Q + 8 * m, b, id_s, 1u);
+                else
+                  umma_ss_f8(d, qa0 + uint64_t(((m >> 2) * QF_BYTES + (m & 3) * 32) >> 4), b, id_s,
+                             1u);
+              }
             } else {
-              const int m = j - 2;  // c_KV dims 16m .. 16m+15 of this rank
-              const uint64_t b = vb0 + uint64_t(((m >> 2) * VBOX + (m & 3) * 32) >> 4);
-              if (m < NQT)
-                umma_ts(d, tmem + TM_Q + 8 * m, b, id_s, 1u);
-              else
-                umma_ss(d, qa0 + uint64_t((((m - NQT) >> 2) * QF_BYTES + (m & 3) * 32) >> 4), b,
-                        id_s, 1u);
+              if (j < 2) {        // rope dims of this rank
+                umma_ss(d, qh0 + uint64_t((j * 32) >> 4), rb0 + uint64_t((j * 32) >> 4), id_s,
+                        j > 0);
+              } else {
+                const int m = j - 2;  // c_KV dims 16m .. 16m+15 of this rank
+                const uint64_t b = vb0 + uint64_t(((m >> 2) * VBOX + (m & 3) * 32) >> 4);
+                if (m < G::NQT)
+                  umma_ts(d, tmem + TM_Q + 8 * m, b, id_s, 1u);
+                else
+                  umma_ss(d,
+                          qa0 + uint64_t((((m - G::NQT) >> 2) * QF_BYTES + (m & 3) * 32) >> 4),
+                          b, id_s, 1u);
+              }
             }
           }
         };
         using C0 = std::integral_constant<int, 0>;
         using C2 = std::integral_constant<int, 2>;
-        using C18 = std::integral_constant<int, KSTEPS>;
+        using C18 = std::integral_constant<int, 18>;
         while (ok && w.next(sg)) {
           const uint32_t end = it + uint32_t(sg.j1 - sg.j0);
-          if (!mbar_wait(&bars[kQFull], seg & 1) || !mbar_wait(&bars[kQTmem], seg & 1)) {
+          if ((!FP8 && !mbar_wait(&bars[kQFull], seg & 1)) || !mbar_wait(&bars[kQTmem], seg & 1)) {
             ok = false;
             break;
           }
@@ -370,7 +541,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           if (*abort_flag) ok = false;
         }
       } else {
-        const uint32_t id_o = idesc_bf16(128, 256, true);
+        const uint32_t id_o = FP8 ? idesc_e4m3(128, 256, true) : idesc_bf16(128, 256, true);
         while (ok && w.next(sg)) {
           const uint32_t end = it + uint32_t(sg.j1 - sg.j0);
           for (uint32_t t = it; t < end; ++t) {
@@ -383,12 +554,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             }
             tc_fence_after();
             // O[:, 256r:+256] (+)= P(t) . c(t)[:, 256r:+256]  (4 MMAs, A = P from TMEM)
+            //   bf16: 16 tokens per MMA.  E4M3: 32 tokens per MMA, for the hi
+            //   and the lo term of P (columns TM_P and TM_P + 16).
             const uint64_t vb0 = sdesc_sw128(v_base + (t % NSTAGE) * VF_BYTES, VBOX, 1024);
             const uint32_t pa = tmem + TM_P;
+            if constexpr (FP8) {
 #pragma unroll
-            for (int kk = 0; kk < BS / 16; ++kk)
-              umma_ts(tmem + TM_O, pa + 8 * kk, vb0 + uint64_t((kk * 2048) >> 4), id_o,
-                      (t > it || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk)
+                umma_ts_f8(tmem + TM_O, pa + 16 * (kk >> 1) + 8 * (kk & 1),
+                           vb0 + uint64_t(((kk & 1) * 32 * 128) >> 4), id_o,
+                           (t > it || kk > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < BS / 16; ++kk)
+                umma_ts(tmem + TM_O, pa + 8 * kk, vb0 + uint64_t((kk * 2048) >> 4), id_o,
+                        (t > it || kk > 0) ? 1u : 0u);
+            }
             umma_commit(&bars[kKVEmpty0 + (t % NSTAGE)]);
             umma_commit(&bars[kPVDone0 + (t & 1)]);
           }
@@ -419,26 +600,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     Seg sg;
     uint32_t u = 0, seg = 0;
     bool ok = true;
+    float part_scale = 1.f;   // partial score -> raw score units (E4M3: c_scale * 2^-e)
     while (ok && w.next(sg)) {
-      // This sequence's Q[:, 256r : 256r + 16 NQT] into TMEM, once the previous
-      // sequence's score MMAs (which read it) have completed.  Rows past h are 0.
+      // This sequence's Q[:, 256r : 256r + 16 NQT] into TMEM (bf16), or both
+      // E4M3 terms of its Q (hi into TMEM, lo into shared memory), once the
+      // previous sequence's score MMAs (which read it) have completed.  Rows
+      // past h are 0.
       bool qgood = seg == 0 || wait_all(&bars[kQEmpty], (seg - 1) & 1);
       if (qgood) {
         tc_fence_after();
-        const uint4* src =
-            reinterpret_cast<const uint4*>(p.q + (int64_t(sg.b) * p.h + r) * ROWW + 256 * rank);
+        if constexpr (FP8) {
+          const uint16_t* qrow = p.q + (int64_t(sg.b) * p.h + r) * ROWW;
+          const int e = q_row_exp(qrow, r < p.h, rank, p.r_ratio);
+          part_scale = p.c_scale * __uint_as_float(uint32_t(127 - e) << 23);
+          build_q_e4m3(qrow, r < p.h, rank, p.r_ratio, e, tmem + lane_off + TM_Q, smem + OFF_QF,
+                       smem + OFF_QH, r);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        } else {
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.q + (int64_t(sg.b) * p.h + r) * ROWW + 256 * rank);
 #pragma unroll
-        for (int half = 0; half < NQT / 4; ++half) {
-          uint32_t qv[32];
+          for (int half = 0; half < G::NQT / 4; ++half) {
+            uint32_t qv[32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 x = r < p.h ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
-            qv[4 * i] = x.x;
-            qv[4 * i + 1] = x.y;
-            qv[4 * i + 2] = x.z;
-            qv[4 * i + 3] = x.w;
+            for (int i = 0; i < 8; ++i) {
+              const uint4 x = r < p.h ? __ldg(src + 8 * half + i) : make_uint4(0, 0, 0, 0);
+              qv[4 * i] = x.x;
+              qv[4 * i + 1] = x.y;
+              qv[4 * i + 2] = x.z;
+              qv[4 * i + 3] = x.w;
+            }
+            tmem_st32(tmem + lane_off + TM_Q + 32 * half, qv);
           }
-          tmem_st32(tmem + lane_off + TM_Q + 32 * half, qv);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -459,6 +652,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
+          if constexpr (FP8) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              v0[j] = __float_as_uint(__uint_as_float(v0[j]) * part_scale);
+              v1[j] = __float_as_uint(__uint_as_float(v1[j]) * part_scale);
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             hx[j] = partial_pair(v0[2 * j], v0[2 * j + 1]);
@@ -528,6 +728,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       const uint32_t n = uint32_t(sg.j1 - sg.j0);
       float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
       bool good = true;
+      // E4M3: this rank's partial scores come out of the MMAs in c_KV code
+      // units times 2^e; the senders scale theirs the same way (q_row_exp)
+      float part_scale = 1.f;
+      if constexpr (FP8)
+        part_scale = p.c_scale *
+                     __uint_as_float(uint32_t(127 - q_row_exp(p.q + (int64_t(sg.b) * p.h + r) * ROWW,
+                                                               r < p.h, rank, p.r_ratio))
+                                     << 23);
       for (uint32_t k = 0; k < n; ++k) {
         const uint32_t t = it + k;
         const uint32_t slot = t & 1;
@@ -543,6 +751,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
+          if constexpr (FP8) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * part_scale);
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) own[j] = partial_pair(v[2 * j], v[2 * j + 1]);
         }
@@ -641,10 +853,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             const float p0 = exp2_approx(fmaf(f.x, p.scale_log2, -m_ref));
             const float p1 = exp2_approx(fmaf(f.y, p.scale_log2, -m_ref));
             lsum += p0 + p1;
-            pk[j] = pack_bf16(p0, p1);
+            if constexpr (FP8) {
+              // two E4M3 terms; p <= 2^8 (the lazy-rescale threshold) stays
+              // inside E4M3's range.  Word j / 2 of each term holds tokens
+              // 32hh + 4(j / 2) .. + 3.
+              uint32_t h2, l2;
+              e4m3_two_terms(p0, p1, h2, l2);
+              if (j & 1) {
+                pk[j >> 1] |= h2 << 16;
+                pk[8 + (j >> 1)] |= l2 << 16;
+              } else {
+                pk[j >> 1] = h2;
+                pk[8 + (j >> 1)] = l2;
+              }
+            } else {
+              pk[j] = pack_bf16(p0, p1);
+            }
           }
           l += lsum;
-          tmem_st16(tmem + lane_off + TM_P + 16 * hh, pk);
+          if constexpr (FP8) {
+            tmem_st8(tmem + lane_off + TM_P + 8 * hh, pk);            // hi term
+            tmem_st8(tmem + lane_off + TM_P + 16 + 8 * hh, pk + 8);   // lo term
+          } else {
+            tmem_st16(tmem + lane_off + TM_P + 16 * hh, pk);
+          }
           tmem_st_wait();
           const int vt = len - (sg.j0 + int(k)) * BS;   // valid rows of the whole tile
           if (vt < BS) {
@@ -652,8 +884,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             // boxes that P.V reads: P is 0 there, but 0 * NaN is NaN.
             uint8_t* stg = smem + OFF_V + (t % NSTAGE) * VF_BYTES;
             const int v0 = max(vt, 0);
-            for (int idx = tid; idx < (BS - v0) * 4 * 8; idx += NSW) {
-              const int row = v0 + idx / 32, rem = idx % 32;
+            constexpr int PIECES = G::NVB * 8;   // 16-byte pieces of a row, all boxes
+            for (int idx = tid; idx < (BS - v0) * PIECES; idx += NSW) {
+              const int row = v0 + idx / PIECES, rem = idx % PIECES;
               *reinterpret_cast<uint4*>(stg + (rem >> 3) * VBOX + row * 128 + (rem & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
@@ -691,17 +924,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           ++nseg;
         }
       }
-      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
+      // E4M3: O is in c_KV code units; c_scale turns it into values
+      const float inv = lrow > 0.f ? p.c_scale / lrow : 0.f;
       Walker wn = w;
       Seg sn;
       if (sg.full && !wn.next(sn)) {
-        // The CTA's last segment, final rows: the value ring is idle (every load was
-        // consumed by a P.V that has completed), so each warp stages its 32 rows
-        // x 128 columns there in four 128-byte swizzled boxes and one lane
+        // The CTA's last segment, final rows: the value ring (and Q) are idle
+        // (every load was consumed by a P.V that has completed, after every
+        // score MMA), so each warp stages its 32 rows x 128 columns there
+        // (L::OFF_EPI) in four 128-byte swizzled boxes and one lane
         // stores them with TMA (whole lines, instead of one 16-byte piece of
         // 32 rows per store instruction).  Rows past h fall outside the
         // tensor and are clipped.
-        uint8_t* ob = smem + OFF_V + (warp - 2) * (4 * 32 * 128);
+        uint8_t* ob = smem + L::OFF_EPI + (warp - 2) * (4 * 32 * 128);
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
           uint32_t o[32];
@@ -816,16 +1051,18 @@ static int mla_pairs_for_device() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   std::call_once(flags[dev], [dev] {
     int result = -1;
-    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             mla::SMEM) == cudaSuccess) {
+    if (cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mla::Lay<false>::SMEM) == cudaSuccess &&
+        cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             mla::Lay<true>::SMEM) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * 1024, 1, 1);
       cfg.blockDim = dim3(mla::THREADS, 1, 1);
-      cfg.dynamicSmemBytes = mla::SMEM;
+      cfg.dynamicSmemBytes = std::max(mla::Lay<false>::SMEM, mla::Lay<true>::SMEM);
       cfg.attrs = nullptr;  // the kernel fixes its cluster shape at compile time
       cfg.numAttrs = 0;
       int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_kernel, &cfg) == cudaSuccess &&
+      if (cudaOccupancyMaxActiveClusters(&clusters, mla_decode_kernel<false>, &cfg) == cudaSuccess &&
           clusters > 0)
         result = clusters;
     }
@@ -841,6 +1078,7 @@ int mla_default_ctas(int h) {
 
 kvattn_status run_decode_mla(const MlaArgs& a) {
   const kvattn_cache* cc = a.cache;
+  const bool fp8 = cc->dtype == KVATTN_FP8_E4M3;
   const int pairs_max = mla_pairs_for_device();
   if (pairs_max <= 0) return KVATTN_ERR_CUDA;
   const int G = a.G > 0 ? a.G : pairs_max;
@@ -872,8 +1110,8 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   pa.err = a.err;
   if (launch_plan(pa, a.stream) != cudaSuccess) return KVATTN_ERR_CUDA;
 
-  alignas(64) CUtensorMap tmQF, tmQH, tmLF, tmLH, tmO;
-  {
+  alignas(64) CUtensorMap tmQF = {}, tmQH = {}, tmLF, tmLH, tmO;
+  if (!fp8) {
     const uint64_t dims[3] = {uint64_t(mla::ROWW), uint64_t(a.h), uint64_t(a.B)};
     const uint64_t strides[2] = {uint64_t(mla::ROWW) * 2, uint64_t(mla::ROWW) * 2 * a.h};
     const uint32_t boxf[3] = {64u, 128u, 1u}, boxh[3] = {32u, 128u, 1u};
@@ -884,13 +1122,20 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
       return KVATTN_ERR_CUDA;
   }
   {
+    // latent rows of 576 elements; value boxes of 128-byte rows (64 bf16 or
+    // 128 E4M3 dims), rope boxes of 64-byte rows (this rank's 32 bf16 dims,
+    // or all 64 E4M3 dims)
+    const uint64_t eb = fp8 ? 1 : 2;
     const uint64_t dims[3] = {uint64_t(mla::ROWW), uint64_t(mla::BS), uint64_t(cc->num_blocks)};
-    const uint64_t strides[2] = {uint64_t(mla::ROWW) * 2, uint64_t(mla::ROWW) * 2 * mla::BS};
-    const uint32_t boxf[3] = {64u, uint32_t(mla::BS), 1u}, boxh[3] = {32u, uint32_t(mla::BS), 1u};
-    if (!encode_tensor_map_3d(&tmLF, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->latent, dims, strides,
-                              boxf, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_3d(&tmLH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->latent, dims, strides,
-                              boxh, CU_TENSOR_MAP_SWIZZLE_64B))
+    const uint64_t strides[2] = {uint64_t(mla::ROWW) * eb, uint64_t(mla::ROWW) * eb * mla::BS};
+    const uint32_t boxf[3] = {fp8 ? 128u : 64u, uint32_t(mla::BS), 1u};
+    const uint32_t boxh[3] = {fp8 ? 64u : 32u, uint32_t(mla::BS), 1u};
+    const CUtensorMapDataType dt =
+        fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_tensor_map_3d(&tmLF, dt, cc->latent, dims, strides, boxf,
+                              CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_3d(&tmLH, dt, cc->latent, dims, strides, boxh,
+                              CU_TENSOR_MAP_SWIZZLE_64B))
       return KVATTN_ERR_CUDA;
   }
   {
@@ -921,13 +1166,16 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   prm.max_blocks = a.max_blocks;
   prm.num_blocks = cc->num_blocks;
   prm.scale_log2 = a.scale * kLog2e;
+  prm.c_scale = fp8 ? cc->k_scale : 1.f;
+  prm.r_ratio = fp8 ? cc->v_scale / cc->k_scale : 1.f;
   prm.err = a.err;
   // the kernel fixes its cluster shape (a CTA pair) at compile time
-  if (launch_pdl(mla_decode_kernel, dim3(2 * G), dim3(mla::THREADS), mla::SMEM, a.stream, tmQF,
-                 tmQH, tmLF, tmLH, tmO, prm) != cudaSuccess)
-    return KVATTN_ERR_CUDA;
-
-  return KVATTN_OK;
+  const cudaError_t e =
+      fp8 ? launch_pdl(mla_decode_kernel<true>, dim3(2 * G), dim3(mla::THREADS),
+                       mla::Lay<true>::SMEM, a.stream, tmQF, tmQH, tmLF, tmLH, tmO, prm)
+          : launch_pdl(mla_decode_kernel<false>, dim3(2 * G), dim3(mla::THREADS),
+                       mla::Lay<false>::SMEM, a.stream, tmQF, tmQH, tmLF, tmLH, tmO, prm);
+  return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA;
 }
 
 }  // namespace kv

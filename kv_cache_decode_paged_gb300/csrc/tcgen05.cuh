@@ -43,6 +43,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
          | (uint32_t(M >> 4) << 24);             // M / 16
 }
 
+// Instruction descriptor, kind::f8f6f4 with A and B both E4M3 (format code 0),
+// D f32, A K-major, B K-major or MN-major, shape M x N (K = 32 per MMA).
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool b_mn_major) {
+  return (1u << 4)                               // D format: f32
+         | ((b_mn_major ? 1u : 0u) << 16)        // B major-ness
+         | (uint32_t(N >> 3) << 17)              // N / 8
+         | (uint32_t(M >> 4) << 24);             // M / 16
+}
+
 // Shared-memory matrix descriptor for a 128-byte swizzled operand.
 //   K-major: rows of 128 bytes, 8-row atoms `sbo` bytes apart (lbo unused).
 //   MN-major: 128-byte lines along MN, 64-element MN chunks `lbo` bytes apart,
@@ -89,6 +98,25 @@ KV_DEVI void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t 
       : "memory");
 }
 
+// The same for kind::f8f6f4 (8-bit A and B, K = 32 per MMA).
+KV_DEVI void umma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// A in TMEM holds four 8-bit codes per 32-bit column (code 4j + i in byte i).
+KV_DEVI void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread completes.
 KV_DEVI void umma_commit(uint64_t* bar) {
   asm volatile(
@@ -127,6 +155,12 @@ KV_DEVI void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "%13,%14,%15,%16};" ::"r"(taddr),
       KV_W8(0), KV_W8(8)
       : "memory");
+}
+KV_DEVI void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                   taddr),
+               KV_W8(0)
+               : "memory");
 }
 KV_DEVI void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

@@ -49,9 +49,12 @@ class GpuWorkload:
             self.v_tok = dev_bits(wl.v, device)
             self.append(self.k_tok, self.v_tok, self.seq_idx, self.pos)
         else:
-            fill = inputs.BF16_NAN if poison else None
-            self.cache = PagedCache.allocate_mla(wl.num_blocks, wl.block_size, wl.d_c,
-                                                    wl.d_rope, device=device, fill_bits=fill)
+            fp8 = wl.kv_dtype == "fp8"
+            fill = (inputs.E4M3_NAN if fp8 else inputs.BF16_NAN) if poison else None
+            self.cache = PagedCache.allocate_mla(wl.num_blocks, wl.block_size, wl.d_c, wl.d_rope,
+                                                    dtype=KVATTN_FP8_E4M3 if fp8 else KVATTN_BF16,
+                                                    k_scale=wl.k_scale, v_scale=wl.v_scale,
+                                                    device=device, fill_bits=fill)
             self.k_tok = dev_bits(wl.c_kv, device)
             self.v_tok = dev_bits(wl.k_r, device)
             self.append(self.k_tok, self.v_tok, self.seq_idx, self.pos)

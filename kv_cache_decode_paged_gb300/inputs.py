@@ -48,6 +48,12 @@ WORKLOADS = {
                             lens=("fixed", [4096] * 64), bs=64, table="permuted",
                             kv_dtype="bf16", q_std=1.0 / 24.0,
                             scale=1.0 / math.sqrt(192.0)),
+    # the same layer over an FP8-E4M3 latent cache (per-tensor scales, one for
+    # c_KV and one for k_R, each amax / 448)
+    "deepseek_v3_mla_fp8": dict(kind="mla", B=64, h=128, d_c=512, d_rope=64,
+                                lens=("fixed", [4096] * 64), bs=64, table="permuted",
+                                kv_dtype="fp8", q_std=1.0 / 24.0,
+                                scale=1.0 / math.sqrt(192.0)),
     # long ragged contexts that need split-KV: GQA-8 and MQA on the same lengths
     "long_gqa8": dict(kind="gqa", B=16, h=64, h_kv=8, d=128, lens=("loguniform", 1024, 131072),
                       bs=16, table="permuted", kv_dtype="bf16", q_std=1.0),
@@ -230,10 +236,15 @@ def make_workload(name: str, seed: int = 0, batch: Optional[int] = None,
         q = normal_bf16(rng_for(seed, "q"), B * h * d, r["q_std"] * q_scale).reshape(B, h, d)
         c_kv = normal_bf16(rng_for(seed, "c_kv"), S * d_c).reshape(S, d_c)
         k_r = normal_bf16(rng_for(seed, "k_r"), S * d_rope).reshape(S, d_rope)
-        return Workload(name=name, kind="mla", B=B, h=h, h_kv=1, d=d, d_c=d_c, d_rope=d_rope,
-                        block_size=bs, kv_dtype=r["kv_dtype"], scale=float(r["scale"]),
-                        seq_lens=seq_lens, cu_seqlens=cu, q=q, k=None, v=None,
-                        c_kv=c_kv, k_r=k_r, block_table=bt, num_blocks=num_blocks)
+        wl = Workload(name=name, kind="mla", B=B, h=h, h_kv=1, d=d, d_c=d_c, d_rope=d_rope,
+                      block_size=bs, kv_dtype=r["kv_dtype"], scale=float(r["scale"]),
+                      seq_lens=seq_lens, cu_seqlens=cu, q=q, k=None, v=None,
+                      c_kv=c_kv, k_r=k_r, block_table=bt, num_blocks=num_blocks)
+        if wl.kv_dtype == "fp8":
+            # per-tensor scales amax / 448 in float32: k_scale for c_KV, v_scale for k_R
+            wl.k_scale = fp8_scale(c_kv)
+            wl.v_scale = fp8_scale(k_r)
+        return wl
 
     if heads is not None:
         raise ValueError("heads overrides the query heads of MLA workloads only")
@@ -246,11 +257,16 @@ def make_workload(name: str, seed: int = 0, batch: Optional[int] = None,
                   seq_lens=seq_lens, cu_seqlens=cu, q=q, k=k, v=v, c_kv=None, k_r=None,
                   block_table=bt, num_blocks=num_blocks)
     if wl.kv_dtype == "fp8":
-        # per-tensor scale = amax / 448 (448 is the largest finite E4M3 value),
-        # evaluated in float32 over the stored bf16 values
-        wl.k_scale = float(np.float32(np.abs(bf16_to_f32(k)).max()) / np.float32(448.0))
-        wl.v_scale = float(np.float32(np.abs(bf16_to_f32(v)).max()) / np.float32(448.0))
+        wl.k_scale = fp8_scale(k)
+        wl.v_scale = fp8_scale(v)
     return wl
+
+
+def fp8_scale(bits: np.ndarray) -> float:
+    """Per-tensor E4M3 scale = amax / 448 (448 is the largest finite E4M3
+    value), evaluated in float32 over the stored bf16 values."""
+    amax = np.float32(np.abs(bf16_to_f32(bits)).max()) if bits.size else np.float32(1.0)
+    return float(amax / np.float32(448.0)) if amax > 0 else 1.0
 
 
 def multi_token_queries(wl: Workload, q_len: int, seed: int = 0) -> np.ndarray:

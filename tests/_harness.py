@@ -20,6 +20,9 @@ def oracle_seq(oracle, wl: inputs.Workload, b: int):
     """Oracle output for sequence b on the stored values (bf16 or E4M3 codes)."""
     sl = wl.seq_slice(b)
     if wl.kind == "mla":
+        if wl.kv_dtype == "fp8":
+            return oracle.mla_decode_e4m3(wl.q[b], mla_codes(oracle, wl, sl), wl.d_c, wl.scale,
+                                          wl.k_scale, wl.v_scale)
         rows = np.concatenate([wl.c_kv[sl], wl.k_r[sl]], axis=1)
         return oracle.mla_decode(wl.q[b], rows, wl.d_c, wl.scale)
     if wl.kv_dtype == "fp8":
@@ -28,6 +31,13 @@ def oracle_seq(oracle, wl: inputs.Workload, b: int):
         return oracle.gqa_decode(wl.q[b], kc, vc, wl.scale, fmt=oracle.FMT_E4M3,
                                  k_scale=wl.k_scale, v_scale=wl.v_scale)
     return oracle.gqa_decode(wl.q[b], wl.k[sl], wl.v[sl], wl.scale)
+
+
+def mla_codes(oracle, wl: inputs.Workload, sl):
+    """The stored E4M3 latent rows of tokens sl: c_KV codes (scale k_scale)
+    then k_R codes (scale v_scale)."""
+    return np.concatenate([oracle.quantize_e4m3(wl.c_kv[sl], wl.k_scale),
+                           oracle.quantize_e4m3(wl.k_r[sl], wl.v_scale)], axis=1)
 
 
 def oracle_all(oracle, wl, seqs=None):

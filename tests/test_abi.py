@@ -173,6 +173,14 @@ def test_mla_host_validation(lib):
     assert call(batch=0) == kv.KVATTN_OK
     c.block_size = 16
     assert call() == kv.KVATTN_ERR_UNSUPPORTED
+    c.block_size = 64
+    c.dtype = kv.KVATTN_FP8_E4M3          # E4M3 latent: both per-tensor scales must be > 0
+    c.k_scale = 0.0
+    assert call() == kv.KVATTN_ERR_INVALID_ARG
+    c.k_scale, c.v_scale = 0.01, -1.0
+    assert call() == kv.KVATTN_ERR_INVALID_ARG
+    c.dtype = 7
+    assert call() == kv.KVATTN_ERR_UNSUPPORTED
 
 
 def test_append_and_combine_validation(lib):
