@@ -149,7 +149,8 @@ struct Lay {
   static constexpr int OFF_X = OFF_R + NROPE * G::RH_BYTES;   // receive slots (the peer writes)
   static constexpr int OFF_XS = OFF_X + NX * XBYTES;          // send staging slots
   static constexpr int OFF_MX = OFF_XS + NX * XBYTES;         // row max / row sum exchange
-  static constexpr int OFF_BAR = OFF_MX + 2 * 128 * 4;
+  static constexpr int OFF_QSC = OFF_MX + 2 * 128 * 4;        // E4M3: per-row partial scale
+  static constexpr int OFF_BAR = OFF_QSC + 128 * 4;
   static constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
   static_assert(OFF_V % 1024 == 0 && OFF_R % 1024 == 0 && OFF_X % 1024 == 0 &&
                     OFF_XS % 1024 == 0 && OFF_QH % 1024 == 0,
@@ -203,17 +204,27 @@ KV_DEVI uint4 q_load8(const uint16_t* qrow, bool live, int dim0, int i) {
 KV_DEVI float bf16_half(uint32_t w, int hi) {
   return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
 }
+// The row is read 12 loads at a time (all in flight together): one load per
+// round trip to L2 made this the longest step of a sequence's start.
 KV_DEVI int q_row_exp(const uint16_t* qrow, bool live, uint32_t rank, float r_ratio) {
   const int c0 = 256 * int(rank), r0 = 512 + 32 * int(rank);
   float mx = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < 36; ++i) {
-    const uint4 x = i < 32 ? q_load8(qrow, live, c0, i) : q_load8(qrow, live, r0, i - 32);
-    const float f = i < 32 ? 1.f : r_ratio;
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll 1
+  for (int g = 0; g < 3; ++g) {
+    uint4 x[12];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      mx = fmaxf(mx, fmaxf(fabsf(bf16_half(w[k], 0) * f), fabsf(bf16_half(w[k], 1) * f)));
+    for (int i = 0; i < 12; ++i) {
+      const int idx = 12 * g + i;
+      x[i] = idx < 32 ? q_load8(qrow, live, c0, idx) : q_load8(qrow, live, r0, idx - 32);
+    }
+#pragma unroll
+    for (int i = 0; i < 12; ++i) {
+      const float f = 12 * g + i < 32 ? 1.f : r_ratio;
+      const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mx = fmaxf(mx, fmaxf(fabsf(bf16_half(w[k], 0) * f), fabsf(bf16_half(w[k], 1) * f)));
+    }
   }
   return mx > 0.f ? min(max(7 - (int((__float_as_uint(mx) >> 23) & 255) - 127), -120), 120) : 0;
 }
@@ -230,12 +241,21 @@ KV_DEVI void build_q_e4m3(const uint16_t* qrow, bool live, uint32_t rank, float 
   const int c0 = 256 * int(rank), r0 = 512 + 32 * int(rank);
   const float sc = __uint_as_float(uint32_t(127 + e) << 23);
 #pragma unroll 1
-  for (int k = 0; k < 9; ++k) {     // 32 dims at a time: c_KV 0..7, rope 8
+  for (int g = 0; g < 3; ++g) {     // 96 dims (12 loads in flight) at a time
+  uint4 xs[12];
+#pragma unroll
+  for (int i = 0; i < 12; ++i) {
+    const int k = 3 * g + i / 4;
+    xs[i] = k < 8 ? q_load8(qrow, live, c0 + 32 * k, i % 4) : q_load8(qrow, live, r0, i % 4);
+  }
+#pragma unroll
+  for (int kk = 0; kk < 3; ++kk) {  // 32 dims at a time: c_KV 0..7, rope 8
+    const int k = 3 * g + kk;
     const float f = k < 8 ? sc : sc * r_ratio;
     uint32_t hi[8], lo[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 x = k < 8 ? q_load8(qrow, live, c0 + 32 * k, i) : q_load8(qrow, live, r0, i);
+      const uint4 x = xs[4 * kk + i];
       const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
       for (int j = 0; j < 4; j += 2) {
@@ -265,6 +285,7 @@ KV_DEVI void build_q_e4m3(const uint16_t* qrow, bool live, uint32_t rank, float 
       *reinterpret_cast<uint4*>(row + ((pc ^ sw) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       *reinterpret_cast<uint4*>(row + (((pc + 1) ^ sw) << 4)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
     }
+  }
   }
 }
 
@@ -319,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
   constexpr int QF_BYTES = G::QF_BYTES, NQF = G::NQF, Q_BYTES = G::Q_BYTES;
   constexpr int VSTAGE = L::VSTAGE, VBOX = L::VBOX, OFF_QF = L::OFF_QF, OFF_QH = L::OFF_QH;
   constexpr int OFF_V = L::OFF_V, OFF_R = L::OFF_R, OFF_X = L::OFF_X, OFF_XS = L::OFF_XS;
-  constexpr int OFF_MX = L::OFF_MX, OFF_BAR = L::OFF_BAR;
+  constexpr int OFF_MX = L::OFF_MX, OFF_BAR = L::OFF_BAR, OFF_QSC = L::OFF_QSC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -613,6 +634,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           const uint16_t* qrow = p.q + (int64_t(sg.b) * p.h + r) * ROWW;
           const int e = q_row_exp(qrow, r < p.h, rank, p.r_ratio);
           part_scale = p.c_scale * __uint_as_float(uint32_t(127 - e) << 23);
+          // for the softmax warps, which read it after this sequence's Q barrier
+          reinterpret_cast<float*>(smem + OFF_QSC)[r] = part_scale;
           build_q_e4m3(qrow, r < p.h, rank, p.r_ratio, e, tmem + lane_off + TM_Q, smem + OFF_QF,
                        smem + OFF_QH, r);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -715,7 +738,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     const uint32_t xsent_peer = map_peer(smem_u32(&bars[kXSent0]), peer);
     Walker w{p.cum, 1, st, en};
     Seg sg;
-    uint32_t it = 0, received = 0;
+    uint32_t it = 0, received = 0, sgi = 0;
     bool ok = true;
     int nseg = 0, seg_unit[2] = {0, 0}, seg_slot[2] = {0, 0};   // this CTA's partials
     // Every wait result is made warp-uniform: the warp-collective TMEM
@@ -729,13 +752,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
       bool good = true;
       // E4M3: this rank's partial scores come out of the MMAs in c_KV code
-      // units times 2^e; the senders scale theirs the same way (q_row_exp)
+      // units times 2^e; the sender of this row wrote the factor back to
+      // score units before arriving on the sequence's Q barrier
       float part_scale = 1.f;
-      if constexpr (FP8)
-        part_scale = p.c_scale *
-                     __uint_as_float(uint32_t(127 - q_row_exp(p.q + (int64_t(sg.b) * p.h + r) * ROWW,
-                                                               r < p.h, rank, p.r_ratio))
-                                     << 23);
+      if constexpr (FP8) {
+        good = wait_all(&bars[kQTmem], sgi & 1);
+        part_scale = reinterpret_cast<const float*>(smem + OFF_QSC)[r];
+      }
+      ++sgi;
       for (uint32_t k = 0; k < n; ++k) {
         const uint32_t t = it + k;
         const uint32_t slot = t & 1;
