@@ -72,6 +72,8 @@ def _load():
             "kvo_mla_absorb_query": (None, [P, P, i32, i32, i32, P]),
             "kvo_mla_apply_wuv": (None, [P, P, i32, i32, i32, P]),
             "kvo_mla_explicit": (i32, [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, f64, P, P]),
+            "kvo_mla_prefill": (i32, [P, P, P, P, P, P, i64, i32, i32, i32, i32, i32, i32, f64, P,
+                                      P]),
             "kvo_lse_combine": (None, [P, P, i32, i32, i32, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -292,6 +294,27 @@ def mla_explicit(q_c, q_r, c, k_r, w_uk, w_uv, scale):
     if rc != 0:
         raise ValueError("kvo_mla_explicit: bad shape")
     return u, lse
+
+
+def mla_prefill(q_c, q_r, c, k_r, w_uk, w_uv, scale):
+    """Explicit-form MLA over the last q_len rows as new tokens, causal among
+    them.  q_c [q_len, h, d_hc], q_r [q_len, h, d_r], c [s, d_c], k_r [s, d_r],
+    w_uk [h, d_hc, d_c], w_uv [h, d_v, d_c] (float64 or anything numpy casts).
+    Returns (out [q_len, h, d_v], lse [q_len, h]) float64."""
+    arrs = [_c(a, np.float64) for a in (q_c, q_r, c, k_r, w_uk, w_uv)]
+    q_c, q_r, c, k_r, w_uk, w_uv = arrs
+    q_len, h, d_hc = q_c.shape
+    d_c = w_uk.shape[2]
+    d_v = w_uv.shape[1]
+    s, d_r = k_r.shape
+    assert q_r.shape == (q_len, h, d_r) and c.shape == (s, d_c) and w_uk.shape == (h, d_hc, d_c)
+    out = np.empty((q_len, h, d_v), dtype=np.float64)
+    lse = np.empty((q_len, h), dtype=np.float64)
+    rc = _load().kvo_mla_prefill(*[_ptr(a) for a in arrs], s, q_len, h, d_c, d_r, d_hc, d_v,
+                                 float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("kvo_mla_prefill: bad shape")
+    return out, lse
 
 
 def lse_combine(part_o, part_lse):

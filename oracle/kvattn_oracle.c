@@ -411,6 +411,82 @@ int kvo_mla_explicit(const double* q_c, const double* q_r, const double* c, cons
   return 0;
 }
 
+/* Explicit-form ("MHA mode") MLA over a chunk of q_len new tokens, causal
+ * among them: the sequence's cached rows are t = 0 .. s-1 and the new tokens
+ * are its last q_len rows, so token j sits at position s - q_len + j and, for
+ * each head i, attends to the rows t <= s - q_len + j with
+ *   k_t,i = [W_UK,i c_t | k_R,t],  q_j,i = [q^C_j,i | q^R_j,i],
+ *   score_t = scale * q_j,i . k_t,i,  out_j,i = sum_t softmax(score)_t W_UV,i c_t
+ * ([P2] "Low-Rank Joint Key-Value Compression", "The Decoupled RoPE
+ * Solution"; [P4] "MHA Mode", "Prefill 为什么未必使用与 Decode 相同的吸收方式":
+ * prefill expands k and v per head from the latent instead of absorbing).
+ * A token whose position is negative (s < q_len) sees nothing: out 0, lse -inf.
+ * q_c [q_len][h][d_hc], q_r [q_len][h][d_r], c [s][d_c], k_r [s][d_r],
+ * w_uk [h][d_hc][d_c], w_uv [h][d_v][d_c]; out [q_len][h][d_v], lse [q_len][h]. */
+int kvo_mla_prefill(const double* q_c, const double* q_r, const double* c, const double* k_r,
+                    const double* w_uk, const double* w_uv, int64_t s, int q_len, int h,
+                    int d_c, int d_r, int d_hc, int d_v, double scale, double* out, double* lse) {
+  if (s < 0 || q_len <= 0 || h <= 0 || d_c <= 0 || d_r < 0 || d_hc <= 0 || d_v <= 0) return -1;
+  int rc = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < h; ++i) {
+    /* this head's keys and values for every cached row */
+    double* kc = (double*)malloc(sizeof(double) * (size_t)((s > 0 ? s : 1) * d_hc));
+    double* vc = (double*)malloc(sizeof(double) * (size_t)((s > 0 ? s : 1) * d_v));
+    double* sc = (double*)malloc(sizeof(double) * (size_t)(s > 0 ? s : 1));
+    if (!kc || !vc || !sc) {
+      rc = -1;
+      free(kc);
+      free(vc);
+      free(sc);
+      continue;
+    }
+    for (int64_t t = 0; t < s; ++t) {
+      for (int j = 0; j < d_hc; ++j) {
+        double acc = 0.0;
+        for (int x = 0; x < d_c; ++x) acc += w_uk[((int64_t)i * d_hc + j) * d_c + x] * c[t * d_c + x];
+        kc[t * d_hc + j] = acc;
+      }
+      for (int j = 0; j < d_v; ++j) {
+        double acc = 0.0;
+        for (int x = 0; x < d_c; ++x) acc += w_uv[((int64_t)i * d_v + j) * d_c + x] * c[t * d_c + x];
+        vc[t * d_v + j] = acc;
+      }
+    }
+    for (int jt = 0; jt < q_len; ++jt) {
+      const int64_t n = s - q_len + jt + 1;   /* rows this token sees */
+      const double* qc = q_c + ((int64_t)jt * h + i) * d_hc;
+      const double* qr = q_r + ((int64_t)jt * h + i) * d_r;
+      double* o = out + ((int64_t)jt * h + i) * d_v;
+      for (int j = 0; j < d_v; ++j) o[j] = 0.0;
+      if (n <= 0) {
+        lse[(int64_t)jt * h + i] = -INFINITY;
+        continue;
+      }
+      double m = -INFINITY;
+      for (int64_t t = 0; t < n; ++t) {
+        double a = 0.0;
+        for (int j = 0; j < d_hc; ++j) a += qc[j] * kc[t * d_hc + j];
+        for (int j = 0; j < d_r; ++j) a += qr[j] * k_r[t * d_r + j];
+        sc[t] = scale * a;
+        if (sc[t] > m) m = sc[t];
+      }
+      double l = 0.0;
+      for (int64_t t = 0; t < n; ++t) {
+        const double p = exp(sc[t] - m);
+        l += p;
+        for (int j = 0; j < d_v; ++j) o[j] += p * vc[t * d_v + j];
+      }
+      for (int j = 0; j < d_v; ++j) o[j] /= l;
+      lse[(int64_t)jt * h + i] = m + log(l);
+    }
+    free(kc);
+    free(vc);
+    free(sc);
+  }
+  return rc;
+}
+
 /* Stable merge of split-KV partial results.  Split w covered a disjoint token
  * range and produced its own normalised output o_w and log-sum-exp lse_w.
  * With M = max_w lse_w:  o = sum_w e^(lse_w - M) o_w / sum_w e^(lse_w - M),

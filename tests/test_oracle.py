@@ -353,6 +353,75 @@ def test_mla_absorbed_equals_explicit(oracle, h, d_hc, d_c, d_r, d_v, s):
     np.testing.assert_allclose(sc_abs, sc_exp, rtol=1e-12, atol=1e-12)
 
 
+def _prefill_case(rng, h, d_hc, d_c, d_r, d_v, s, q_len):
+    q_c = rng.standard_normal((q_len, h, d_hc))
+    q_r = rng.standard_normal((q_len, h, d_r))
+    c = rng.standard_normal((s, d_c))
+    k_r = rng.standard_normal((s, d_r))
+    w_uk = rng.standard_normal((h, d_hc, d_c)) / math.sqrt(d_c)
+    w_uv = rng.standard_normal((h, d_v, d_c)) / math.sqrt(d_c)
+    return q_c, q_r, c, k_r, w_uk, w_uv, 1 / math.sqrt(d_hc + d_r)
+
+
+@pytest.mark.parametrize("h,d_hc,d_c,d_r,d_v,s,q_len",
+                         [(3, 16, 32, 8, 16, 9, 4), (2, 128, 512, 64, 128, 20, 5)])
+def test_mla_prefill_matches_causal_sdpa(oracle, h, d_hc, d_c, d_r, d_v, s, q_len):
+    """Explicit-form MLA prefill equals torch's float64 causal attention over
+    the keys [W_UK c | k_R] and values W_UV c expanded with matmuls."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    q_c, q_r, c, k_r, w_uk, w_uv, scale = _prefill_case(np.random.default_rng(s + q_len), h, d_hc,
+                                                       d_c, d_r, d_v, s, q_len)
+    out, lse = oracle.mla_prefill(q_c, q_r, c, k_r, w_uk, w_uv, scale)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    kc = torch.einsum("hjc,sc->hsj", T(w_uk), T(c))                        # [h, s, d_hc]
+    K = torch.cat([kc, T(k_r).unsqueeze(0).expand(h, s, d_r)], dim=2)      # [h, s, 192]
+    V = torch.einsum("hjc,sc->hsj", T(w_uv), T(c))                         # [h, s, d_v]
+    Q = torch.cat([T(q_c), T(q_r)], dim=2).transpose(0, 1)                 # [h, q_len, 192]
+    pos = torch.arange(s - q_len, s).unsqueeze(1)
+    mask = torch.arange(s).unsqueeze(0) <= pos                             # [q_len, s]
+    ref = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=scale)
+    np.testing.assert_allclose(out, ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
+    scores = (Q @ K.transpose(1, 2)) * scale
+    ref_lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=2).transpose(0, 1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12)
+
+
+def test_mla_prefill_last_token_equals_absorbed_decode(oracle):
+    """The last new token sees every row: its explicit result equals the
+    absorbed decode (q~ = W_UK^T q^C, latent weighted sum, W_UV afterwards)."""
+    h, d_hc, d_c, d_r, d_v, s, q_len = 4, 16, 32, 8, 16, 11, 3
+    q_c, q_r, c, k_r, w_uk, w_uv, scale = _prefill_case(np.random.default_rng(5), h, d_hc, d_c,
+                                                       d_r, d_v, s, q_len)
+    out, lse = oracle.mla_prefill(q_c, q_r, c, k_r, w_uk, w_uv, scale)
+    q_abs = np.concatenate([oracle.mla_absorb_query(q_c[-1], w_uk), q_r[-1]], axis=1)
+    u_tilde, lse_abs = oracle.mla_decode(q_abs, np.concatenate([c, k_r], axis=1), d_c, scale,
+                                         fmt=oracle.FMT_F64)
+    np.testing.assert_allclose(out[-1], oracle.mla_apply_wuv(u_tilde, w_uv), rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(lse[-1], lse_abs, rtol=1e-12)
+    # every earlier token equals the single-query explicit form over its prefix
+    for j in range(q_len):
+        n = s - q_len + j + 1
+        u, l = oracle.mla_explicit(q_c[j], q_r[j], c[:n], k_r[:n], w_uk, w_uv, scale)
+        np.testing.assert_allclose(out[j], u, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse[j], l, rtol=1e-12)
+
+
+def test_mla_prefill_short_sequence(oracle):
+    """More new tokens than rows: the first token has no position (zeros,
+    lse -inf); the second sees only row 0, so its output is W_UV c_0 exactly
+    and its lse the one score."""
+    h, d_hc, d_c, d_r, d_v = 2, 8, 16, 4, 8
+    q_c, q_r, c, k_r, w_uk, w_uv, scale = _prefill_case(np.random.default_rng(9), h, d_hc, d_c,
+                                                       d_r, d_v, 2, 3)
+    out, lse = oracle.mla_prefill(q_c, q_r, c, k_r, w_uk, w_uv, scale)
+    assert (out[0] == 0).all() and np.isneginf(lse[0]).all()
+    for i in range(h):
+        np.testing.assert_allclose(out[1, i], w_uv[i] @ c[0], rtol=1e-13)
+        score = scale * (q_c[1, i] @ (w_uk[i] @ c[0]) + q_r[1, i] @ k_r[0])
+        np.testing.assert_allclose(lse[1, i], score, rtol=1e-13)
+
+
 def test_mla_absorb_query_brute(oracle):
     rng = np.random.default_rng(2)
     q_c = rng.standard_normal((3, 4))
