@@ -273,6 +273,39 @@ KVATTN_API kvattn_status kvattn_mla_absorb_q(const void* q_nope, const void* q_r
 KVATTN_API kvattn_status kvattn_mla_up_v(const float* u_tilde, const void* w_uv, int batch, int h,
                                          int d_c, int d_v, float* v, int32_t* err, void* stream);
 
+/* Explicit-form ("MHA mode") MLA prefill over the paged latent: q_len new
+ * tokens per sequence, already appended (token j of sequence b sits at
+ * position s_b - q_len + j), attend causally to the cached rows with keys and
+ * values expanded per head from the latent,
+ *   k_t,i = [W_UK,i c_t | k_R,t],  v_t,i = W_UV,i c_t,
+ *   out_j,i = sum_{t <= s_b - q_len + j} softmax_t(scale * [q^C_j,i | q^R_j,i] . k_t,i) v_t,i
+ * ("MLA：为什么一份 Latent 可以代替多头 KV Cache", sections "MHA Mode" and "Prefill
+ * 为什么未必使用与 Decode 相同的吸收方式": prefill expands keys and values per
+ * head, decode absorbs W_UK into the query; the last new token's result equals
+ * the absorbed decode's followed by W_UV).  A token whose position would be
+ * negative (s_b < q_len) sees nothing: out 0, lse -inf.
+ *   q_nope:     device, [batch][q_len][h][d_hc] bf16 (q^C).
+ *   q_rope:     device, [batch][q_len][h][64] bf16 (q^R, already rotated).
+ *   cache:      host struct; kind MLA, bf16, d_c = 512, d_rope = 64, block 64.
+ *   block_table, seq_lens: as for kvattn_decode_mla (seq_lens include the new
+ *               tokens).
+ *   w_uk, w_uv: device, [h][d_hc][d_c] and [h][d_v][d_c] bf16 (row-major, d_c
+ *               fastest; the layouts of kvattn_mla_absorb_q and kvattn_mla_up_v).
+ *   scale:      softmax scale (1/sqrt(d_hc + d_rope)).
+ *   out:        device, [batch][q_len][h][d_v] float32;  lse: [batch][q_len][h].
+ * Built for d_hc = d_v = 128, h and batch at most 65535 (KVATTN_ERR_UNSUPPORTED
+ * otherwise).  Needs no workspace: the expanded keys and values of each tile
+ * of 128 cached rows live only in the SM that uses them (tensor memory, then
+ * shared memory).  One kernel on `stream`, one CTA per (128 new tokens, head,
+ * sequence); device errors as for kvattn_decode_mla. */
+KVATTN_API kvattn_status kvattn_mla_prefill(const void* q_nope, const void* q_rope,
+                                            const kvattn_cache* cache, const int32_t* block_table,
+                                            const int32_t* seq_lens, int batch,
+                                            int max_blocks_per_seq, int q_len, int h, int d_hc,
+                                            int d_v, const void* w_uk, const void* w_uv,
+                                            float scale, float* out, float* lse, int32_t* err,
+                                            void* stream);
+
 /* Split-KV log-sum-exp combine.
  *   Unit u owns split_count[u] consecutive partial slots starting at
  *   split_first[u]; each slot holds rows_per_unit rows of a normalised partial

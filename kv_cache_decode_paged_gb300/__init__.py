@@ -37,7 +37,7 @@ EXPORTED = [
     "kvattn_status_string", "kvattn_abi_version", "kvattn_page_bytes", "kvattn_cell_bytes",
     "kvattn_append", "kvattn_decode_workspace_bytes", "kvattn_default_num_ctas",
     "kvattn_decode_gqa", "kvattn_decode_mla", "kvattn_combine", "kvattn_decode_gqa_noalloc",
-    "kvattn_decode_gqa_multi", "kvattn_mla_absorb_q", "kvattn_mla_up_v",
+    "kvattn_decode_gqa_multi", "kvattn_mla_absorb_q", "kvattn_mla_up_v", "kvattn_mla_prefill",
 ]
 
 KVATTN_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -101,6 +101,8 @@ def load_library(build: bool = True) -> ctypes.CDLL:
                                               P, P, sz, i32, P, P]),
             "kvattn_mla_absorb_q": (i32, [P, P, P, i32, i32, i32, i32, i32, P, P, P]),
             "kvattn_mla_up_v": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
+            "kvattn_mla_prefill": (i32, [P, P, CP, P, P, i32, i32, i32, i32, i32, i32, P, P, f32,
+                                         P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -227,6 +229,20 @@ def kvattn_mla_up_v(u_tilde, w_uv, v, err=None, stream=None):
     _check("kvattn_mla_up_v", load_library().kvattn_mla_up_v(
         _ptr(u_tilde), _ptr(w_uv), int(batch), int(h), int(d_c), d_v, _ptr(v), _ptr(err),
         _stream(stream)))
+
+
+def kvattn_mla_prefill(q_nope, q_rope, cache: kvattn_cache, block_table, seq_lens, w_uk, w_uv,
+                       scale, out, lse, err=None, stream=None):
+    """Explicit-form MLA prefill of q_len new tokens per sequence (already in the
+    cache, causal among them): q_nope [B][q_len][h][128], q_rope [B][q_len][h][64]
+    bf16 bits, w_uk / w_uv [h][128][512] bf16 bits -> out [B][q_len][h][128],
+    lse [B][q_len][h] float32."""
+    batch, q_len, h, d_hc = q_nope.shape
+    d_v = int(w_uv.shape[1])
+    _check("kvattn_mla_prefill", load_library().kvattn_mla_prefill(
+        _ptr(q_nope), _ptr(q_rope), ctypes.byref(cache), _ptr(block_table), _ptr(seq_lens),
+        int(batch), int(block_table.shape[1]), int(q_len), int(h), int(d_hc), d_v, _ptr(w_uk),
+        _ptr(w_uv), float(scale), _ptr(out), _ptr(lse), _ptr(err), _stream(stream)))
 
 
 def kvattn_combine(part_out, part_lse, split_first, split_count, rows_per_unit, dv, out, lse,

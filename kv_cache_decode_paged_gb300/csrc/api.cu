@@ -279,6 +279,55 @@ extern "C" kvattn_status kvattn_mla_up_v(const float* u_tilde, const void* w_uv,
   return run_mla_up_v(a);
 }
 
+extern "C" kvattn_status kvattn_mla_prefill(const void* q_nope, const void* q_rope,
+                                            const kvattn_cache* cache, const int32_t* block_table,
+                                            const int32_t* seq_lens, int batch,
+                                            int max_blocks_per_seq, int q_len, int h, int d_hc,
+                                            int d_v, const void* w_uk, const void* w_uv,
+                                            float scale, float* out, float* lse, int32_t* err,
+                                            void* stream) {
+  if (!cache || cache->kind != KVATTN_MLA) return KVATTN_ERR_INVALID_ARG;
+  if (batch < 0 || max_blocks_per_seq <= 0 || q_len <= 0 || h <= 0 || d_hc <= 0 || d_v <= 0)
+    return KVATTN_ERR_INVALID_ARG;
+  if (cache->num_blocks <= 0 || cache->block_size <= 0 || cache->reserved != 0)
+    return KVATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || scale == INFINITY) return KVATTN_ERR_INVALID_ARG;
+  if (batch == 0) return KVATTN_OK;
+  if (!q_nope || !q_rope || !block_table || !seq_lens || !w_uk || !w_uv || !out || !lse ||
+      !cache->latent)
+    return KVATTN_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(q_rope, 16) || !aligned(w_uk, 16) || !aligned(w_uv, 16) ||
+      !aligned(out, 16) || !aligned(lse, 4) || !aligned(cache->latent, 16) ||
+      !aligned(block_table, 4) || !aligned(seq_lens, 4))
+    return KVATTN_ERR_INVALID_ARG;
+  if (cache->dtype != KVATTN_BF16) return KVATTN_ERR_UNSUPPORTED;
+  if (cache->d_c != 512 || cache->d_rope != 64 || cache->block_size != 64)
+    return KVATTN_ERR_UNSUPPORTED;
+  if (d_hc != 128 || d_v != 128) return KVATTN_ERR_UNSUPPORTED;
+  if (h > 65535 || batch > 65535 || cache->num_blocks >= INT_MAX / 64 ||
+      int64_t(max_blocks_per_seq) * 64 >= INT_MAX ||
+      int64_t(batch) * q_len * h >= INT_MAX / 128)
+    return KVATTN_ERR_UNSUPPORTED;
+  PrefillArgs a;
+  a.q_nope = q_nope;
+  a.q_rope = q_rope;
+  a.cache = cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.B = batch;
+  a.max_blocks = max_blocks_per_seq;
+  a.q_len = q_len;
+  a.h = h;
+  a.w_uk = w_uk;
+  a.w_uv = w_uv;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  a.err = err;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return run_mla_prefill(a);
+}
+
 extern "C" kvattn_status kvattn_combine(const float* part_out, const float* part_lse,
                                         const int32_t* split_first, const int32_t* split_count,
                                         int n_units, int rows_per_unit, int dv, float* out,

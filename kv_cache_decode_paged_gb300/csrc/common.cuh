@@ -9,14 +9,18 @@
 
 #define KV_DEVI __device__ __forceinline__
 
-// Iteration limit for every spin on an mbarrier.  mbarrier.try_wait may
-// suspend the thread for a hardware-defined interval per call, so this bound
-// is between tens of milliseconds and about a second of wall time: far beyond
-// any legitimate wait inside these kernels (each runs well under a
+// Time limit for every wait on an mbarrier, in nanoseconds of %globaltimer:
+// far beyond any legitimate wait inside these kernels (each runs well under a
 // millisecond), short enough that a protocol bug ends the kernel with
-// KVATTN_DEVERR_TIMEOUT quickly instead of hanging.
-#ifndef KV_MAX_SPIN
-#define KV_MAX_SPIN (1u << 20)
+// KVATTN_DEVERR_TIMEOUT instead of hanging the GPU.  Each mbarrier.try_wait
+// also carries a suspend-time hint (KV_WAIT_SLICE_NS): without one a thread
+// may stay suspended for a hardware-defined interval long enough that a bound
+// counted in iterations alone becomes minutes or hours.
+#ifndef KV_WAIT_NS
+#define KV_WAIT_NS 200000000ull   // 0.2 s
+#endif
+#ifndef KV_WAIT_SLICE_NS
+#define KV_WAIT_SLICE_NS 2000u
 #endif
 
 namespace kv {
@@ -55,16 +59,23 @@ KV_DEVI void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// try_wait suspends at most about KV_WAIT_SLICE_NS when the phase is not complete.
 KV_DEVI bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(KV_WAIT_SLICE_NS)
       : "memory");
   return ok != 0;
+}
+
+KV_DEVI uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
@@ -93,9 +104,11 @@ KV_DEVI bool mbar_test(uint64_t* bar, uint32_t parity) {
 // than a try_wait.
 KV_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_test(bar, parity)) return true;
-  for (uint32_t i = 0; i < KV_MAX_SPIN; ++i)
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if ((i & 7) == 0 && global_ns() - t0 > KV_WAIT_NS) return false;
+  }
 }
 
 // ---- TMA (cp.async.bulk.tensor) -----------------------------------------------
@@ -122,6 +135,16 @@ KV_DEVI void tma_load_3d_nohint(void* smem_dst, const CUtensorMap* map, int c0, 
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 4-D tiled load of one box, completing on `bar`.
+KV_DEVI void tma_load_4d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -330,18 +353,20 @@ KV_DEVI bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
         : "memory");
     if (ok) return true;
   }
-  for (uint32_t i = 0; i < KV_MAX_SPIN; ++i) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(KV_WAIT_SLICE_NS)
         : "memory");
     if (ok) return true;
+    if ((i & 7) == 0 && global_ns() - t0 > KV_WAIT_NS) return false;
   }
-  return false;
+
 }
 
 KV_DEVI void cluster_sync_all() {

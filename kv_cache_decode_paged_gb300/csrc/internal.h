@@ -117,6 +117,11 @@ bool encode_tensor_map_3d(void* map, CUtensorMapDataType dtype, const void* base
                           const uint64_t dims[3], const uint64_t strides_bytes[2],
                           const uint32_t box[3], CUtensorMapSwizzle swizzle);
 
+// The same for a 4-D tensor.
+bool encode_tensor_map_4d(void* map, CUtensorMapDataType dtype, const void* base,
+                          const uint64_t dims[4], const uint64_t strides_bytes[3],
+                          const uint32_t box[4], CUtensorMapSwizzle swizzle);
+
 struct GqaArgs {
   const void* q;
   const kvattn_cache* cache;
@@ -159,6 +164,24 @@ struct MlaArgs {
 };
 kvattn_status run_decode_mla(const MlaArgs& a);
 int mla_default_ctas(int h);
+
+// Explicit-form MLA prefill over the paged latent (prefill_mla.cu).
+struct PrefillArgs {
+  const void* q_nope;   // [B][q_len][h][128] bf16
+  const void* q_rope;   // [B][q_len][h][64] bf16
+  const kvattn_cache* cache;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int B, max_blocks, q_len, h;
+  const void* w_uk;     // [h][128][512] bf16
+  const void* w_uv;     // [h][128][512] bf16
+  float scale;
+  float* out;           // [B][q_len][h][128] f32
+  float* lse;           // [B][q_len][h] f32
+  int32_t* err;
+  cudaStream_t stream;
+};
+kvattn_status run_mla_prefill(const PrefillArgs& a);
 
 // Per-head projections around MLA decode (absorb.cu).
 struct AbsorbArgs {

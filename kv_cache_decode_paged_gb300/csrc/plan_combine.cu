@@ -403,6 +403,21 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+bool encode_tensor_map_4d(void* map, CUtensorMapDataType dtype, const void* base,
+                          const uint64_t dims[4], const uint64_t strides_bytes[3],
+                          const uint32_t box[4], CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t gstr[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(reinterpret_cast<CUtensorMap*>(map), dtype, 4, const_cast<void*>(base), gdim,
+                  gstr, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_tensor_map_3d(void* map, CUtensorMapDataType dtype, const void* base,
                           const uint64_t dims[3], const uint64_t strides_bytes[2],
                           const uint32_t box[3], CUtensorMapSwizzle swizzle) {

@@ -302,6 +302,18 @@ def mla_projections(B: int, h: int = 128, d_hc: int = 128, d_c: int = 512, d_rop
         w_uv=normal_bf16(rng_for(seed, "w_uv"), h * d_v * d_c, d_c ** -0.5).reshape(h, d_v, d_c))
 
 
+def prefill_queries(B: int, q_len: int, h: int = 128, d_hc: int = 128, d_rope: int = 64,
+                    seed: int = 0, q_scale: float = 1.0):
+    """Un-absorbed queries of q_len new tokens per sequence for the explicit-form
+    MLA prefill, spread like mla_projections' single-token queries:
+    q_nope [B][q_len][h][d_hc], q_rope [B][q_len][h][d_rope] bf16 bits."""
+    w = 512 + d_rope
+    q_nope = normal_bf16(rng_for(seed, f"pf_q_nope{q_len}"), B * q_len * h * d_hc, q_scale)
+    q_rope = normal_bf16(rng_for(seed, f"pf_q_rope{q_len}"), B * q_len * h * d_rope,
+                         q_scale * w ** -0.5)
+    return q_nope.reshape(B, q_len, h, d_hc), q_rope.reshape(B, q_len, h, d_rope)
+
+
 def plant_needle(wl: Workload, b: int, head: int, t: int, strength: float = 30.0):
     """Overwrite K[t] of sequence b (the KV head that ``head`` reads) with
     ``strength * q/|q|`` so that one key dominates the softmax of that head."""
