@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=0, help="0 = same as --steps")
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (GQA; > 1 runs the multi-token decode)")
+    ap.add_argument("--prefill", default="",
+                    help="B,S,Q: time only the explicit-form MLA prefill of Q new tokens over B "
+                         "sequences of S cached rows (DeepSeek-V3 heads) and print its JSON")
     ap.add_argument("--no-all-configs", action="store_true",
                     help="skip timing the decode call of every workload (the all_configs object)")
     ap.add_argument("--absorb", action="store_true",
@@ -530,6 +533,7 @@ def time_all_configs(args, sampler, headline, dev):
                  "gbs": kvb / cold / 1e3, "frac_of_measured_hbm": kvb / cold / 1e3 / peak,
                  "pct_of_8tbs": 100.0 * kvb / cold / 1e3 / NOMINAL_HBM_GBS,
                  "gbs_back_to_back": kvb / warm / 1e3, "target_frac": target,
+                 "traffic": recorded_traffic(wl, name),
                  "clocks": sampler.summary(t0, t1), "device_err_bits": g.err_bits()}
         if wl.kind == "gqa":
             entry["h_kv"] = wl.h_kv
@@ -540,11 +544,88 @@ def time_all_configs(args, sampler, headline, dev):
         if g is not headline:
             del g
         torch.cuda.empty_cache()
+    res["mla_prefill"] = time_prefill(args, sampler, dev, stream, flushed_by=(flush, n))
     res["how"] = ("decode call replayed from a CUDA graph %d times; us_decode_call = (flush + "
                   "decode replays - flush replays) / %d with an L2 flush (sum over a %d MB "
                   "buffer) before every decode; gbs, frac and pct use it" % (n, n,
                                                                              FLUSH_BYTES >> 20))
     return res
+
+
+def prefill_flops(S, q_len, h, B):
+    """FLOPs of one explicit-form MLA prefill call as the kernel performs them:
+    the expansion of every 128-row tile of keys and values each (128 new
+    tokens, head) visits (2 * 128 * 128 * 512 * 2 per tile), plus the causal
+    attention proper (2 * (192 + 128) per visible (token, row) pair), over all
+    heads and sequences."""
+    tiles = sum((S - q_len + min(q_len, 128 * qt + 128) + 127) // 128
+                for qt in range((q_len + 127) // 128))
+    expand = tiles * 128 * 128 * 512 * 2 * 2 * h * B
+    attend = sum(S - q_len + j + 1 for j in range(q_len)) * (192 + 128) * 2 * h * B
+    return expand, attend
+
+
+def time_prefill(args, sampler, dev, stream, flushed_by=None, B=4, S=4096, q_len=512):
+    """Explicit-form MLA prefill at DeepSeek-V3 shapes: B sequences of S cached
+    rows (the last q_len of them new), 128 heads, replayed from a CUDA graph
+    after an L2 flush like the decode calls."""
+    import torch
+
+    import kv_cache_decode_paged_gb300 as kv
+    from kv_cache_decode_paged_gb300 import inputs
+    from kv_cache_decode_paged_gb300.device import GpuWorkload, dev_bits
+
+    if flushed_by is None:
+        flush_buf = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        sink = torch.empty((), dtype=torch.int64, device=dev)
+
+        def flush():
+            torch.sum(flush_buf, dim=0, dtype=torch.int64, out=sink)
+        n = max(50, args.steps)
+    else:
+        flush, n = flushed_by
+    wl = inputs.make_workload("deepseek_v3_mla", seed=args.seed, lens=[S] * B)
+    g = GpuWorkload(wl, poison=False, device=dev)
+    h = 128
+    qn, qr = inputs.prefill_queries(B, q_len, h=h, seed=args.seed)
+    pj = inputs.mla_projections(1, h=h, seed=args.seed)
+    qn, qr = dev_bits(qn, dev), dev_bits(qr, dev)
+    wk, wv = dev_bits(pj.w_uk, dev), dev_bits(pj.w_uv, dev)
+    out = torch.empty((B, q_len, h, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, q_len, h), dtype=torch.float32, device=dev)
+    desc = g.cache.descriptor()
+
+    def run():
+        kv.kvattn_mla_prefill(qn, qr, desc, g.bt, g.seq_lens, wk, wv, wl.scale, out, lse,
+                              err=g.err)
+
+    def flushed():
+        flush()
+        run()
+
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    reps = max(10, n // 5)
+    warm = replay_us(torch, run, reps, stream)
+    both = replay_us(torch, flushed, reps, stream)
+    alone = replay_us(torch, flush, reps, stream)
+    t1 = time.monotonic()
+    cold = max(both - alone, 1e-3)
+    expand, attend = prefill_flops(S, q_len, h, B)
+    peak = 1928.9
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    tf = (expand + attend) / cold / 1e6
+    return {"kernel": "explicit-form MLA prefill (keys and values expanded per tile on the SM)",
+            "batch": B, "cached_rows": S, "q_len": q_len, "h": h, "us": cold,
+            "us_back_to_back": warm, "flop_expand": expand, "flop_attention": attend,
+            "tflops": tf, "roofline": {"bound": "tensor", "achieved": tf, "peak": peak,
+                                       "unit": "TFLOP/s", "frac": tf / peak,
+                                       "peak_source": "MEASURED_PEAKS.json bf16_tflops (burst)"},
+            "clocks": sampler.summary(t0, t1), "device_err_bits": g.err_bits()}
 
 
 # -------------------------------------------------------------------------- ours
@@ -824,9 +905,29 @@ def run_ours(args, wl, rank, world, local):
         dist.destroy_process_group()
 
 
+def run_prefill_only(args):
+    import torch
+    torch.cuda.set_device(0)
+    import kv_cache_decode_paged_gb300 as kv
+    kv.load_library()
+    B, S, Q = (int(x) for x in args.prefill.split(","))
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(0).uuid).replace("GPU-", "")
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    res = time_prefill(args, sampler, "cuda:0", torch.cuda.current_stream(), B=B, S=S, q_len=Q)
+    sampler.stop()
+    print(json.dumps({"metric": "explicit-form MLA prefill TFLOP/s", "value": res["tflops"],
+                      "unit": "TFLOP/s", "n_gpus": 1, "higher_is_better": True,
+                      "dtype": "bf16", "data": "synthetic", "prefill": res}), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = env_ranks()
+    if args.prefill and args.impl == "ours":
+        if rank == 0:
+            run_prefill_only(args)
+        return
     from kv_cache_decode_paged_gb300 import inputs
     batch = args.batch or None
     if args.impl == "reference":
