@@ -78,38 +78,44 @@ def load_library(build: bool = True) -> ctypes.CDLL:
             _build.build()
         if not os.path.exists(_build.LIB):
             raise RuntimeError(f"libkvattn.so not found at {_build.LIB}; run __graft_entry__.build()")
-        lib = ctypes.CDLL(_build.LIB)
-        P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
-                                ctypes.c_size_t)
-        CP = ctypes.POINTER(kvattn_cache)
-        sig = {
-            "kvattn_status_string": (ctypes.c_char_p, [i32]),
-            "kvattn_abi_version": (i32, []),
-            "kvattn_page_bytes": (i64, [CP]),
-            "kvattn_cell_bytes": (i64, [i32, i32, i32, i32, i32, i32, i32]),
-            "kvattn_append": (i32, [CP, P, P, i64, P, P, P, i32, i32, P, P]),
-            "kvattn_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
-            "kvattn_default_num_ctas": (i32, [i32, i32, i32, i32, i32]),
-            "kvattn_decode_gqa": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz,
-                                        i32, P, P]),
-            "kvattn_decode_mla": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz,
-                                        i32, P, P]),
-            "kvattn_combine": (i32, [P, P, P, P, i32, i32, i32, P, P, P]),
-            "kvattn_decode_gqa_noalloc": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P,
-                                                i32, P, P]),
-            "kvattn_decode_gqa_multi": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, i32, f32, P,
-                                              P, P, sz, i32, P, P]),
-            "kvattn_mla_absorb_q": (i32, [P, P, P, i32, i32, i32, i32, i32, P, P, P]),
-            "kvattn_mla_up_v": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
-            "kvattn_mla_prefill": (i32, [P, P, CP, P, P, i32, i32, i32, i32, i32, i32, P, P, f32,
-                                         P, P, P, P]),
-        }
-        for name, (res, args) in sig.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
-        return lib
+        _lib = open_library(_build.LIB)
+        return _lib
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """Load a build of the library at `path` with every entry point's ctypes
+    signature set (load_library() does this for libkvattn.so)."""
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    CP = ctypes.POINTER(kvattn_cache)
+    sig = {
+        "kvattn_status_string": (ctypes.c_char_p, [i32]),
+        "kvattn_abi_version": (i32, []),
+        "kvattn_page_bytes": (i64, [CP]),
+        "kvattn_cell_bytes": (i64, [i32, i32, i32, i32, i32, i32, i32]),
+        "kvattn_append": (i32, [CP, P, P, i64, P, P, P, i32, i32, P, P]),
+        "kvattn_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "kvattn_default_num_ctas": (i32, [i32, i32, i32, i32, i32]),
+        "kvattn_decode_gqa": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz,
+                                    i32, P, P]),
+        "kvattn_decode_mla": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P, P, sz,
+                                    i32, P, P]),
+        "kvattn_combine": (i32, [P, P, P, P, i32, i32, i32, P, P, P]),
+        "kvattn_decode_gqa_noalloc": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, f32, P, P,
+                                            i32, P, P]),
+        "kvattn_decode_gqa_multi": (i32, [P, CP, P, P, i32, i32, i32, i32, i32, i32, f32, P,
+                                          P, P, sz, i32, P, P]),
+        "kvattn_mla_absorb_q": (i32, [P, P, P, i32, i32, i32, i32, i32, P, P, P]),
+        "kvattn_mla_up_v": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
+        "kvattn_mla_prefill": (i32, [P, P, CP, P, P, i32, i32, i32, i32, i32, i32, P, P, f32,
+                                     P, P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
 
 
 def _ptr(t) -> Optional[int]:

@@ -39,24 +39,41 @@ def _inputs():
     return files
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB):
+# Test-only variant: every mbarrier wait gives up after 2 ms, and CTA 0 of the
+# GQA decode never signals chunk 3 of its walk, so that a wait runs out on the
+# GPU and the abort path can be checked there.  Built on demand by its test,
+# never by build().
+WAIT_TEST_LIB = os.path.join(BUILD, "wait_test", "libkvattn_wait_test.so")
+WAIT_TEST_DEFINES = ["-DKV_WAIT_NS=2000000ull", "-DKV_TEST_DROP_CHUNK=3"]
+
+
+def is_stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not is_stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    exe = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
     # extra nvcc flags for tuning sweeps (e.g. -D overrides of kernel constants)
-    extra += os.environ.get("KVATTN_NVCC_EXTRA", "").split()
+    extra = os.environ.get("KVATTN_NVCC_EXTRA", "").split()
+    return _build_lib(LIB, BUILD, extra, force, verbose, ptxas_info)
+
+
+def build_wait_test(force: bool = False) -> str:
+    return _build_lib(WAIT_TEST_LIB, os.path.dirname(WAIT_TEST_LIB), WAIT_TEST_DEFINES, force)
+
+
+def _build_lib(lib: str, build_dir: str, extra: list, force: bool = False, verbose: bool = False,
+               ptxas_info: bool = False) -> str:
+    if not force and not is_stale(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
+    exe = nvcc()
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + list(extra)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [exe, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,13 +86,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log:
                 print(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [exe, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -28,6 +28,17 @@
 #include "internal.h"
 #include "walk.cuh"
 
+// Test builds only (-DKV_TEST_DROP_CHUNK=n, with a short KV_WAIT_NS): CTA 0's
+// producer neither signals nor loads chunk n of its walk, as a copy that never
+// lands would, so that the consumer's bounded wait on that stage runs out and
+// the abort path (error bit, stop, drain, exit) runs on the GPU.  The library
+// is built without it.
+#ifdef KV_TEST_DROP_CHUNK
+#define KV_TEST_DROPS_CHUNK(ic) (blockIdx.x == 0 && (ic) == uint32_t(KV_TEST_DROP_CHUNK))
+#else
+#define KV_TEST_DROPS_CHUNK(ic) false
+#endif
+
 namespace kv {
 
 struct GqaParams {
@@ -177,14 +188,15 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
         for (int c0 = 0; c0 < nchunk && ok; c0 += C::GROUP) {
           const int cl = c0 + lane;
           const int pg = __shfl_sync(0xffffffffu, page, min(cl / cpp, 31));
-          bool lok = true;
+          bool lok = true, issued = false;
+          const uint32_t ic = it + uint32_t(cl);
           if (lane < C::GROUP && cl < nchunk) {
-            const uint32_t ic = it + uint32_t(cl);
             const int s = ic % C::NSTAGE;
             const int sub = cl % cpp;
             if (!mbar_wait(&empty[s], ((ic / C::NSTAGE) & 1) ^ 1)) {
               lok = false;
-            } else {
+            } else if (!KV_TEST_DROPS_CHUNK(ic)) {
+              issued = true;
               mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
               uint8_t* dst = stages + s * C::STAGE_BYTES;
 #pragma unroll
@@ -198,18 +210,33 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
           }
           lok = lok && *reinterpret_cast<volatile int*>(abort_flag) == 0;
           ok = __all_sync(0xffffffffu, lok) != 0;
-          if (!ok && lane == 0) {
-            report(p.err, KVATTN_DEVERR_TIMEOUT);
-            *reinterpret_cast<volatile int*>(abort_flag) = 1;
+          if (!ok) {
+            if (lane == 0) {
+              report(p.err, KVATTN_DEVERR_TIMEOUT);
+              *reinterpret_cast<volatile int*>(abort_flag) = 1;
+            }
+            // Drain before exiting: wait (bounded) for the last copy issued
+            // into each stage, which may still be landing in this CTA's shared
+            // memory.  Chunks before this group were all issued, and the last
+            // NSTAGE - GROUP of them hold stages that no chunk of this group
+            // touched; each of this group's lanes covers the stage of its own
+            // chunk: that chunk if it issued it, else the one NSTAGE before.
+            const uint32_t base = it + uint32_t(c0);
+            const uint32_t span = uint32_t(C::NSTAGE - C::GROUP);
+            if (lane == 0)
+              for (uint32_t k = base > span ? base - span : 0u; k < base; ++k)
+                mbar_wait(&full[k % C::NSTAGE], (k / C::NSTAGE) & 1);
+            if (lane < C::GROUP) {
+              if (issued)
+                mbar_wait(&full[ic % C::NSTAGE], (ic / C::NSTAGE) & 1);
+              else if (ic >= uint32_t(C::NSTAGE))
+                mbar_wait(&full[(ic - C::NSTAGE) % C::NSTAGE], ((ic - C::NSTAGE) / C::NSTAGE) & 1);
+            }
+            __syncwarp();
           }
         }
         it += uint32_t(nchunk);
       }
-    }
-    if (!ok && lane == 0) {
-      // Drain: wait (bounded) for the copies still in flight before exiting.
-      const uint32_t lo = it > uint32_t(C::NSTAGE) ? it - C::NSTAGE : 0;
-      for (uint32_t k = lo; k < it; ++k) mbar_wait(&full[k % C::NSTAGE], (k / C::NSTAGE) & 1);
     }
     return;
   }
