@@ -33,8 +33,9 @@
  *   - CUDA graphs: the first call of an entry point on a device does one-time
  *     host set-up (kernel attributes, occupancy queries, the tensor-map
  *     encoder's address); make it outside any stream capture.  After it,
- *     kvattn_append, kvattn_decode_gqa, kvattn_decode_mla, kvattn_mla_absorb_q
- *     and kvattn_mla_up_v only enqueue kernels on `stream`, so they can be
+ *     kvattn_append, kvattn_decode_gqa, kvattn_decode_gqa_multi,
+ *     kvattn_decode_mla, kvattn_mla_absorb_q, kvattn_mla_up_v and
+ *     kvattn_mla_prefill only enqueue kernels on `stream`, so they can be
  *     captured in a CUDA graph and replayed.  Replays read the buffers the
  *     captured call was given, whatever they hold at replay time; the host
  *     struct and scalars are fixed at capture.
@@ -42,8 +43,9 @@
  *     KVATTN_ERR_INVALID_ARG or KVATTN_ERR_UNSUPPORTED and nothing is
  *     enqueued.  KVATTN_ERR_CUDA means a CUDA call or launch failed.
  *     Data-dependent faults found on the device (a block id outside the pool,
- *     a length longer than the block table row, a bounded wait that gave up)
- *     never trap: the kernel skips or zero-fills the access and ORs a
+ *     a length longer than the block table row, a wait inside a kernel that
+ *     gave up after its time limit of 0.2 s) never trap: the kernel skips or
+ *     zero-fills the access, or stops and drains its copies, and ORs a
  *     KVATTN_DEVERR_* bit into *err (a device int32 the caller zeroes; err may
  *     be NULL).  Outputs touched by such a fault are unspecified but finite.
  *   - Layouts are row-major and densely packed unless stated.
@@ -93,8 +95,11 @@ typedef enum kvattn_dtype { KVATTN_BF16 = 0, KVATTN_FP8_E4M3 = 1 } kvattn_dtype;
  *   MLA: one pool [num_blocks][block_size][d_c + d_rope], each row
  *        [c_KV | k_R] ("page / token i: [c_KV | k_R]", "MLA：为什么一份
  *        Latent ...", section "Paged KV Cache 的 Block 里放什么").
- *   Element type: bf16, or (GQA only) FP8-E4M3 codes whose value is
- *   code * k_scale (K) or code * v_scale (V), one scale per tensor.
+ *   Element type: bf16, or FP8-E4M3 codes with one scale per tensor: GQA
+ *   code * k_scale (K) or code * v_scale (V); MLA code * k_scale for the c_KV
+ *   part of a row and code * v_scale for its k_R part (c_KV and k_R are
+ *   quantised separately: "MLA：为什么一份 Latent ...", section "MLA 与 KV Cache
+ *   量化可以叠加").
  * Pools must be 16-byte aligned; 256-byte alignment is recommended. */
 typedef struct kvattn_cache {
   int32_t kind;        /* kvattn_kind                                   */
@@ -105,8 +110,8 @@ typedef struct kvattn_cache {
   int32_t d_h;         /* GQA: head dim (MLA: ignored)                  */
   int32_t d_c;         /* MLA: latent width c_KV (512)                  */
   int32_t d_rope;      /* MLA: decoupled RoPE key width (64)            */
-  float k_scale;       /* FP8 dequant scale of K (1.0 for bf16)         */
-  float v_scale;       /* FP8 dequant scale of V (1.0 for bf16)         */
+  float k_scale;       /* FP8 dequant scale of K / MLA c_KV (1.0 bf16)  */
+  float v_scale;       /* FP8 dequant scale of V / MLA k_R (1.0 bf16)   */
   int32_t reserved;    /* must be 0                                     */
   void* k;             /* GQA K pool (device)                           */
   void* v;             /* GQA V pool (device)                           */
@@ -142,7 +147,9 @@ KVATTN_API int64_t kvattn_cell_bytes(int kind, int num_layers, int h_kv, int d_h
  *        nearest even and saturated to +-448.
  *   MLA: k_or_ckv = c_KV [n_tokens][d_c] bf16, v_or_kr = k_R [n_tokens][d_rope]
  *        bf16 (already rotated by the caller); the row becomes [c_KV | k_R]
- *        ("MLA：为什么一份 Latent ...": "cache_j = [c_j^KV ; k_j^R]").
+ *        ("MLA：为什么一份 Latent ...": "cache_j = [c_j^KV ; k_j^R]").  An
+ *        FP8 pool stores c_KV as e4m3(x / k_scale) and k_R as
+ *        e4m3(x / v_scale), rounded as for GQA.
  *   All pointers except cache are device pointers.  Tokens whose (seq, pos)
  *   falls outside the table or whose block id is outside the pool are skipped
  *   and flagged in *err.  Two tokens with the same slot race. */
@@ -215,7 +222,9 @@ KVATTN_API kvattn_status kvattn_decode_gqa_multi(const void* q, const kvattn_cac
 /* MLA absorbed decode.
  *   q_absorbed:  device, [batch][h][d_c + d_rope] bf16: [W_UK^T q^C | q^R] per
  *                head ("Let us define the absorbed query vector").
- *   cache:       host struct; kind MLA, bf16, d_c = 512, d_rope = 64.
+ *   cache:       host struct; kind MLA, bf16 or FP8-E4M3 (k_scale, v_scale >
+ *                0), block_size 64, d_c = 512, d_rope = 64; other shapes
+ *                return KVATTN_ERR_UNSUPPORTED.
  *   h:           query heads, 1..128.
  *   scale:       softmax scale (1/sqrt(d_h^C + d_r) = 1/sqrt(192) for
  *                DeepSeek-V3 -- not 1/sqrt of the row width).

@@ -39,10 +39,10 @@ def _inputs():
     return files
 
 
-# Test-only variant: every mbarrier wait gives up after 2 ms, and CTA 0 of the
-# GQA decode never signals chunk 3 of its walk, so that a wait runs out on the
-# GPU and the abort path can be checked there.  Built on demand by its test,
-# never by build().
+# Test-only variant: every main-loop mbarrier wait gives up after 2 ms (the
+# exit-path drains keep their full limit), and CTA 0 of the GQA decode never
+# signals chunk 3 of its walk, so that a wait runs out on the GPU and the abort
+# path can be checked there.  Built on demand by its test, never by build().
 WAIT_TEST_LIB = os.path.join(BUILD, "wait_test", "libkvattn_wait_test.so")
 WAIT_TEST_DEFINES = ["-DKV_WAIT_NS=2000000ull", "-DKV_TEST_DROP_CHUNK=3"]
 

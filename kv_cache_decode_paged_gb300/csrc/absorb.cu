@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(absorb::THREADS)
   if (warp == 0 && !ok) {   // no MMA may still write TMEM when it is released
     if (lane == 0) umma_commit(drain);
     __syncwarp();
-    mbar_wait(drain, 0);
+    mbar_wait(drain, 0, KV_DRAIN_WAIT_NS);
   }
   __syncwarp();
   tc_fence_before();
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(absorb::THREADS)
   if (warp == 0 && !ok) {   // no MMA may still write TMEM when it is released
     if (lane == 0) umma_commit(drain);
     __syncwarp();
-    mbar_wait(drain, 0);
+    mbar_wait(drain, 0, KV_DRAIN_WAIT_NS);
   }
   tc_fence_before();
   __syncthreads();

@@ -22,6 +22,10 @@
 #ifndef KV_WAIT_SLICE_NS
 #define KV_WAIT_SLICE_NS 2000u
 #endif
+// Waits on the exit path (copies and MMAs that may still be landing in this
+// CTA's memory, the peer's last signals) keep this limit even in a build with
+// a shorter KV_WAIT_NS.
+#define KV_DRAIN_WAIT_NS 200000000ull
 
 namespace kv {
 
@@ -102,12 +106,12 @@ KV_DEVI bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  A phase that
 // has already completed is seen by the non-blocking test, which is cheaper
 // than a try_wait.
-KV_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity) {
+KV_DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = KV_WAIT_NS) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 7) == 0 && global_ns() - t0 > KV_WAIT_NS) return false;
+    if ((i & 7) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -341,7 +345,8 @@ KV_DEVI void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
 }
 
 // Bounded wait that acquires at cluster scope (sees the peer's released writes).
-KV_DEVI bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+KV_DEVI bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                uint64_t limit_ns = KV_WAIT_NS) {
   {
     uint32_t ok;
     asm volatile(
@@ -364,7 +369,7 @@ KV_DEVI bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity), "r"(KV_WAIT_SLICE_NS)
         : "memory");
     if (ok) return true;
-    if ((i & 7) == 0 && global_ns() - t0 > KV_WAIT_NS) return false;
+    if ((i & 7) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 
 }

@@ -225,12 +225,13 @@ __global__ void __launch_bounds__(GqaCfg<D, MT, FP8>::THREADS)
             const uint32_t span = uint32_t(C::NSTAGE - C::GROUP);
             if (lane == 0)
               for (uint32_t k = base > span ? base - span : 0u; k < base; ++k)
-                mbar_wait(&full[k % C::NSTAGE], (k / C::NSTAGE) & 1);
+                mbar_wait(&full[k % C::NSTAGE], (k / C::NSTAGE) & 1, KV_DRAIN_WAIT_NS);
             if (lane < C::GROUP) {
               if (issued)
-                mbar_wait(&full[ic % C::NSTAGE], (ic / C::NSTAGE) & 1);
+                mbar_wait(&full[ic % C::NSTAGE], (ic / C::NSTAGE) & 1, KV_DRAIN_WAIT_NS);
               else if (ic >= uint32_t(C::NSTAGE))
-                mbar_wait(&full[(ic - C::NSTAGE) % C::NSTAGE], ((ic - C::NSTAGE) / C::NSTAGE) & 1);
+                mbar_wait(&full[(ic - C::NSTAGE) % C::NSTAGE], ((ic - C::NSTAGE) / C::NSTAGE) & 1,
+                          KV_DRAIN_WAIT_NS);
             }
             __syncwarp();
           }

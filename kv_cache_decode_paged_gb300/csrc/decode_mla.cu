@@ -459,9 +459,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       }
       // Every load this thread issued lands before the CTA can exit (on the
       // normal path the consumers have waited for all of them already).
-      if (!FP8 && seg > 0) mbar_wait(&bars[kQFull], (seg - 1) & 1);
+      if (!FP8 && seg > 0) mbar_wait(&bars[kQFull], (seg - 1) & 1, KV_DRAIN_WAIT_NS);
       for (uint32_t k = it > uint32_t(NSTAGE) ? it - NSTAGE : 0; k < it; ++k)
-        mbar_wait(&bars[kKVFull0 + k % NSTAGE], (k / NSTAGE) & 1);
+        mbar_wait(&bars[kKVFull0 + k % NSTAGE], (k / NSTAGE) & 1, KV_DRAIN_WAIT_NS);
     }
   } else if (warp == 1 || warp == PV_WARP) {
     // ------------------------------------------ MMA issuers: S (warp 1), P.V
@@ -606,7 +606,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       }
       // no MMA of this thread may still write TMEM when it is released
       umma_commit(&bars[kMmaDrain + (warp == 1 ? 0 : 1)]);
-      mbar_wait(&bars[kMmaDrain + (warp == 1 ? 0 : 1)], 0);
+      mbar_wait(&bars[kMmaDrain + (warp == 1 ? 0 : 1)], 0, KV_DRAIN_WAIT_NS);
     }
   } else if (warp >= SEND0 / 32) {   // (warps SEND0/32 .. PV_WARP-1)
     // ---------------------------------------------------------------- senders
@@ -723,8 +723,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
     // Drain: the peer's last arrivals on this CTA's barriers (received / read)
     // for the last partials pushed
     for (uint32_t k = u > uint32_t(NX) ? u - NX : 0; k < u; ++k) {
-      mbar_wait_cluster(&bars[kXSent0 + k % NX], (k / NX) & 1);
-      mbar_wait_cluster(&bars[kXEmpty0 + k % NX], (k / NX) & 1);
+      mbar_wait_cluster(&bars[kXSent0 + k % NX], (k / NX) & 1, KV_DRAIN_WAIT_NS);
+      mbar_wait_cluster(&bars[kXEmpty0 + k % NX], (k / NX) & 1, KV_DRAIN_WAIT_NS);
     }
   } else {
     // ------------------------------------------ softmax / epilogue warps (2..9)
@@ -1027,7 +1027,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
       Seg s2;
       while (w2.next(s2)) total += uint32_t(s2.j1 - s2.j0);
       for (uint32_t k = received; k < total && k < received + NX; ++k)
-        mbar_wait_cluster(&bars[kXFull0 + k % NX], (k / NX) & 1);
+        mbar_wait_cluster(&bars[kXFull0 + k % NX], (k / NX) & 1, KV_DRAIN_WAIT_NS);
     } else {
       // Publish this rank's halves of the partials it wrote and merge the
       // groups and sequences they complete (merge.cuh): each rank merges its

@@ -184,10 +184,10 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         *abort_flag = 1;
       }
       // every load issued lands before the CTA can exit
-      mbar_wait(&bars[pQ], 0);
-      if (nkr > 0) mbar_wait(&bars[pKR], (nkr - 1) & 1);
+      mbar_wait(&bars[pQ], 0, KV_DRAIN_WAIT_NS);
+      if (nkr > 0) mbar_wait(&bars[pKR], (nkr - 1) & 1, KV_DRAIN_WAIT_NS);
       for (uint32_t k = g > uint32_t(NCH) ? g - NCH : 0; k < g; ++k)
-        mbar_wait(&bars[pChFull0 + k % NCH], (k / NCH) & 1);
+        mbar_wait(&bars[pChFull0 + k % NCH], (k / NCH) & 1, KV_DRAIN_WAIT_NS);
     }
   } else if (warp == 5) {
     // ---------------------------------------------------------------- MMA issuer
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
         *abort_flag = 1;
       }
       umma_commit(&bars[pDrain]);
-      mbar_wait(&bars[pDrain], 0);
+      mbar_wait(&bars[pDrain], 0, KV_DRAIN_WAIT_NS);
     }
   } else {
     // ---------------------------------------------------------------- compute

@@ -5,7 +5,8 @@ reports KVATTN_DEVERR_TIMEOUT in the caller's error word and ends the kernel
 (stop issuing, wait for the copies still landing, exit), so that a lost copy or
 a protocol bug costs one wrong result instead of a hung GPU.  The library's
 own build never takes that path, so this test builds a variant of it
-(`_build.build_wait_test`): every wait gives up after 2 ms, and the producer
+(`_build.build_wait_test`): every main-loop wait gives up after 2 ms (the
+drains on the way out keep their full limit), and the producer
 of CTA 0 neither loads nor signals chunk 3 of its walk, as if that copy never
 landed.  Nothing faults and nothing waits without a limit: the consumer's wait
 on that stage runs out, and the rest of CTA 0 follows the abort path.
