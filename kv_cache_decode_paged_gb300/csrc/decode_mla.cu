@@ -72,9 +72,13 @@ constexpr int BS = 64;                 // tokens per page = tokens per tile
 constexpr int NROPE = 2;               // rope ring
 constexpr int XROW = BS * 2;           // a row of a partial tile, f16
 constexpr int XBYTES = 128 * XROW;     // 16 KB
-constexpr int NX = 2;                  // exchange ring depth
+#ifndef KV_MLA_NX
+#define KV_MLA_NX 1
+#endif
+constexpr int NX = KV_MLA_NX;          // exchange ring depth (staging and receive slots)
+static_assert(NX >= 1 && NX <= 2, "two barrier slots per exchange ring");
 constexpr int NBARS = 48;
-constexpr int NSTAGE_MAX = 8;          // barrier slots reserved per value stage ring
+constexpr int NSTAGE_MAX = 10;         // barrier slots reserved per value stage ring
 constexpr int NSW = 256;               // softmax warps: two threads per head row
 constexpr int NSEND = 128;             // sender warps: one thread per head row
 constexpr int SW0 = 64, SEND0 = 64 + NSW;
@@ -91,7 +95,7 @@ constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units: rescale O only when the
 #define KV_MLA_NQT 12
 #endif
 #ifndef KV_MLA_NSTAGE
-#define KV_MLA_NSTAGE 4
+#define KV_MLA_NSTAGE 5
 #endif
 #ifndef KV_MLA_NSTAGE_FP8
 #define KV_MLA_NSTAGE_FP8 7
@@ -185,6 +189,7 @@ struct MlaParams {
   float c_scale;           // E4M3 cache: value of a c_KV code unit (1 for bf16)
   float r_ratio;           // E4M3 cache: k_R scale / c_KV scale (1 for bf16)
   int32_t* err;
+  uint32_t zero;           // always 0: a mask the compiler cannot fold (see the receive-slot release)
 };
 
 // E4M3 query of one head row for one rank of the pair: the rank's 256 c_KV
@@ -412,47 +417,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      Walker w{p.cum, 1, st, en};
-      Seg sg;
-      uint32_t it = 0, seg = 0;
-      bool ok = true;
-      while (ok && w.next(sg)) {
-        if constexpr (!FP8) {
-          // bf16: the shared-memory part of Q is loaded as it is (the E4M3
-          // form is built by the sender warps)
-          if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
-          for (int i = 0; i < NQF; ++i)
-            tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 16 * G::NQT + 64 * i, 0,
-                               sg.b, &bars[kQFull]);
-          tma_load_3d_nohint(smem + OFF_QH, &tmQH, rx, 0, sg.b, &bars[kQFull]);
-        }
-        const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
-        for (int j = sg.j0; j < sg.j1 && ok; ++j, ++it) {
-          const int s = it % NSTAGE, q = it & 1;
-          if (!mbar_wait(&bars[kKVEmpty0 + s], ((it / NSTAGE) & 1) ^ 1) ||
-              !mbar_wait(&bars[kRopeEmpty0 + q], ((it >> 1) & 1) ^ 1)) {
+    // The whole warp walks the segments; lane 0 waits and issues, and the
+    // block ids are read 32 at a time, one per lane, before the waits that
+    // precede their tiles (a block id read right after a stage frees would
+    // add an L2 round trip to every stage's lifetime, and at a sequence's
+    // start one round trip per tile).
+    const uint64_t pol = policy_evict_first();
+    Walker w{p.cum, 1, st, en};
+    Seg sg;
+    uint32_t it = 0, seg = 0;
+    bool ok = true;
+    while (ok && w.next(sg)) {
+      if constexpr (!FP8) {
+        // bf16: the shared-memory part of Q is loaded as it is (the E4M3
+        // form is built by the sender warps)
+        if (lane == 0) {
+          if (seg > 0 && !mbar_wait(&bars[kQEmpty], (seg - 1) & 1)) {
             ok = false;
-            break;
+          } else {
+            mbar_arrive_expect_tx(&bars[kQFull], Q_BYTES);
+            for (int i = 0; i < NQF; ++i)
+              tma_load_3d_nohint(smem + OFF_QF + i * QF_BYTES, &tmQF, vx0 + 16 * G::NQT + 64 * i, 0,
+                                 sg.b, &bars[kQFull]);
+            tma_load_3d_nohint(smem + OFF_QH, &tmQH, rx, 0, sg.b, &bars[kQFull]);
           }
-          const int blk = row[j];
-          int page = int(p.num_blocks);  // out of range: zero fill
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
+      for (int jb = sg.j0; jb < sg.j1 && ok; jb += 32) {
+        int page = int(p.num_blocks);  // out of range: zero fill
+        if (jb + lane < sg.j1) {
+          const int blk = row[jb + lane];
           if (blk < 0 || int64_t(blk) >= p.num_blocks)
             report(p.err, KVATTN_DEVERR_BLOCK_ID);
           else
             page = blk;
-          uint8_t* stg = smem + OFF_V + s * VF_BYTES;
-          mbar_arrive_expect_tx(&bars[kKVFull0 + s], uint32_t(VSTAGE + RH_BYTES));
-          for (int i = 0; i < G::NVB; ++i)
-            tma_load_3d(stg + i * VBOX, &tmLF, vx0 + G::BOX_DIMS * i, 0, page, &bars[kKVFull0 + s],
-                        pol);
-          tma_load_3d(smem + OFF_R + q * RH_BYTES, &tmLH, rx, 0, page, &bars[kKVFull0 + s], pol);
-          if (*abort_flag) ok = false;
         }
-        ++seg;
+        const int cnt = min(32, sg.j1 - jb);
+        for (int i = 0; i < cnt && ok; ++i) {
+          const int pg = __shfl_sync(0xffffffffu, page, i);
+          int issued = 0;
+          if (lane == 0) {
+            const int s = it % NSTAGE, q = it & 1;
+            if (!mbar_wait(&bars[kKVEmpty0 + s], ((it / NSTAGE) & 1) ^ 1) ||
+                !mbar_wait(&bars[kRopeEmpty0 + q], ((it >> 1) & 1) ^ 1)) {
+              ok = false;
+            } else {
+              uint8_t* stg = smem + OFF_V + s * VF_BYTES;
+              mbar_arrive_expect_tx(&bars[kKVFull0 + s], uint32_t(VSTAGE + RH_BYTES));
+              for (int b = 0; b < G::NVB; ++b)
+                tma_load_3d(stg + b * VBOX, &tmLF, vx0 + G::BOX_DIMS * b, 0, pg,
+                            &bars[kKVFull0 + s], pol);
+              tma_load_3d(smem + OFF_R + q * RH_BYTES, &tmLH, rx, 0, pg, &bars[kKVFull0 + s], pol);
+              issued = 1;
+              if (*abort_flag) ok = false;
+            }
+          }
+          // it counts the tiles issued (the exit drain waits for their loads)
+          it += uint32_t(__shfl_sync(0xffffffffu, issued, 0));
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
       }
+      ++seg;
+    }
+    if (lane == 0) {
       if (!ok) {
         report(p.err, KVATTN_DEVERR_TIMEOUT);
         *abort_flag = 1;
@@ -760,28 +790,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
         part_scale = reinterpret_cast<const float*>(smem + OFF_QSC)[r];
       }
       ++sgi;
+      // This rank's own partial of tile t (f16 pairs of this thread's 32
+      // tokens), read out of S slot t % 2, which is then released.  The next
+      // tile's partial is read in the middle of this tile's step, as soon as
+      // the exchange has delivered this tile's peer partial: the score MMAs
+      // of tile t + 2 wait for that slot, and with it the senders and the
+      // exchange of tile t + 2, which the softmax of tile t + 2 waits for.
+      uint32_t own[16];
+      auto read_own = [&](uint32_t t) {
+        const uint32_t slot = t & 1;
+        if (!wait_all(&bars[kSFull0 + slot], (t >> 1) & 1)) return false;
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + TM_S + BS * slot + 32 * hh, v);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
+        if constexpr (FP8) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * part_scale);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) own[j] = partial_pair(v[2 * j], v[2 * j + 1]);
+        return true;
+      };
+      if (n > 0) good = good && read_own(it);
       for (uint32_t k = 0; k < n; ++k) {
         const uint32_t t = it + k;
         const uint32_t slot = t & 1;
-        // This rank's own partial is ready well before the peer's arrives:
-        // read it first, so that only the addition waits for the exchange.
-        good = good && wait_all(&bars[kSFull0 + slot], (t >> 1) & 1);
-        uint32_t own[16];
-        if (good) {
-          tc_fence_after();
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + TM_S + BS * slot + 32 * hh, v);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars[kSRead0 + slot]);
-          if constexpr (FP8) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * part_scale);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) own[j] = partial_pair(v[2 * j], v[2 * j + 1]);
-        }
         // The peer's bulk copy writes this CTA's shared memory and completes on
         // this CTA's barrier: observing the phase makes the bytes visible.
         const uint32_t xs = t % NX;
@@ -803,11 +840,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           uint4 pv[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) pv[c] = xr[(4 * hh + c) ^ (r & 7)];
-          // Once every lane's loads have been performed the warp releases its
-          // share of the receive slot, so that the peer can push the next
-          // partial while this tile's softmax goes on.
-          __syncwarp();
-          if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer + xs * 8u);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             hs[4 * c] = hadd2_u32(own[4 * c], pv[c].x);
@@ -815,6 +847,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             hs[4 * c + 2] = hadd2_u32(own[4 * c + 2], pv[c].z);
             hs[4 * c + 3] = hadd2_u32(own[4 * c + 3], pv[c].w);
           }
+          // Once every lane's loads have returned, the warp releases its share
+          // of the receive slot, so that the peer can push the next partial
+          // while this tile's softmax goes on.  The arrive is relaxed (a
+          // release-ordered remote arrive costs about a microsecond), so it is
+          // ordered after the loads by data: its address adds a value derived
+          // from every lane's four loaded words, masked by p.zero (0 at run
+          // time, unknown to the compiler), so it cannot issue before they
+          // have returned.
+          const uint32_t dep = __reduce_or_sync(0xffffffffu, pv[0].x ^ pv[1].y ^ pv[2].z ^ pv[3].w);
+          if (lane == 0) mbar_arrive_remote_relaxed(xempty_peer + xs * 8u + (dep & p.zero));
           if (valid < 32) {   // tokens past the end of the sequence score -inf
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -828,6 +870,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
           const float2 m2 = __half22float2(*reinterpret_cast<const __half2*>(&hm));
           mx = fmaxf(m2.x, m2.y) * p.scale_log2;   // log2 units (scale > 0 keeps the order)
         }
+        if (k + 1 < n) good = good && read_own(t + 1);
         // One barrier per tile in the common case: every thread has read the
         // receive slot, and no row's max has outgrown its reference by the
         // threshold.  Otherwise the two halves of each row exchange maxima.
@@ -1193,6 +1236,7 @@ kvattn_status run_decode_mla(const MlaArgs& a) {
   prm.c_scale = fp8 ? cc->k_scale : 1.f;
   prm.r_ratio = fp8 ? cc->v_scale / cc->k_scale : 1.f;
   prm.err = a.err;
+  prm.zero = 0u;
   // the kernel fixes its cluster shape (a CTA pair) at compile time
   const cudaError_t e =
       fp8 ? launch_pdl(mla_decode_kernel<true>, dim3(2 * G), dim3(mla::THREADS),
