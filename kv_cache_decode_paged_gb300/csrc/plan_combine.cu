@@ -199,6 +199,9 @@ constexpr int kCombineMaxCols = 4;   // float4 columns per lane: dv <= 512
 // COLS float4 columns per lane (dv <= 128 COLS); each warp loads BATCH splits
 // (its splits w, w + 8, ...) before merging them, so that a row split many
 // ways waits for a few batches of loads rather than one load per split.
+#ifndef KV_COMBINE_BATCH
+#define KV_COMBINE_BATCH 8
+#endif
 template <int COLS, int BATCH>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse,
@@ -362,7 +365,7 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, const i
   if (items > 0x7fffffff) return cudaErrorInvalidValue;
   using CombineFn = void (*)(const float*, const float*, const int32_t*, const int32_t*, int, int,
                              float*, float*, int, RowMap);
-  const CombineFn k = dv <= 128 ? CombineFn(&combine_kernel<1, 8>)
+  const CombineFn k = dv <= 128 ? CombineFn(&combine_kernel<1, KV_COMBINE_BATCH>)
                     : dv <= 256 ? CombineFn(&combine_kernel<2, 4>)
                                 : CombineFn(&combine_kernel<4, 2>);
   return launch_pdl(k, dim3(unsigned(items)), dim3(kCombineThreads), 0, s, part_out, part_lse, first,
