@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvattn.so")
-SOURCES = ["api.cu", "append.cu", "plan_combine.cu", "decode_gqa.cu", "decode_mla.cu", "noalloc.cu",
-           "absorb.cu", "prefill_mla.cu"]
+SOURCES = ["api.cu", "append.cu", "plan_combine.cu", "decode_gqa.cu", "decode_gqa_tc.cu",
+           "decode_mla.cu", "noalloc.cu", "absorb.cu", "prefill_mla.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

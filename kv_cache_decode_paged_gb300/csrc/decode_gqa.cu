@@ -41,24 +41,6 @@
 
 namespace kv {
 
-struct GqaParams {
-  const uint16_t* q;
-  const int32_t* bt;
-  const int32_t* seq_lens;
-  const int64_t* cum;
-  const int4* cta_start;
-  float* out;
-  float* lse;
-  float* part_out;
-  float* part_lse;
-  int B, h, hkv, g, bs, max_blocks;
-  int qlen;   // new tokens per sequence (1: plain decode)
-  int rows;   // rows per unit: qlen * g, ordered (token j, head in group)
-  int64_t num_blocks;
-  float qk_scale_log2;  // softmax scale * log2(e), times k_scale for FP8
-  float v_mult;         // 1, or v_scale for FP8
-  int32_t* err;
-};
 
 template <int D, int MT, bool FP8>
 struct GqaCfg {
@@ -637,6 +619,7 @@ static int default_ctas_mt(int g) {
 int gqa_default_ctas(int dtype, int h, int h_kv, int d) {
   if (h_kv <= 0 || h % h_kv) return -1;
   const int g = h / h_kv;
+  if (gqa_tc_applies(dtype, g, d)) return gqa_tc_ctas();
   if (dtype == KVATTN_FP8_E4M3) return d == 128 ? default_ctas_mt<128, true>(g) : -1;
   if (d == 64) return default_ctas_mt<64, false>(g);
   if (d == 128) return default_ctas_mt<128, false>(g);
@@ -700,7 +683,9 @@ kvattn_status run_decode_gqa(const GqaArgs& a) {
   prm.v_mult = fp8 ? cc->v_scale : 1.f;
   prm.err = a.err;
   kvattn_status st;
-  if (fp8)
+  if (gqa_tc_applies(cc->dtype, rows, a.d))
+    st = launch_gqa_tc(a, prm, G);
+  else if (fp8)
     st = dispatch_mt<128, true>(a, prm, G);
   else if (a.d == 64)
     st = dispatch_mt<64, false>(a, prm, G);

@@ -1,0 +1,542 @@
+// decode_gqa_tc.cu -- GQA decode on tcgen05 for units of many rows.
+//
+// The same computation as decode_gqa.cu ("MHA → MQA → GQA → MLA", the grouped
+// attention of one KV head; "MLA：为什么一份 Latent 可以代替多头 KV Cache",
+// section "Prefill 为什么未必使用与 Decode 相同的吸收方式", several new tokens
+// verified per pass, causal among themselves): for each unit (sequence b, KV
+// head), its rows r = (new token j, head i of the group), r = j * g + i, attend
+// to the cached positions [0, s_b - (q_len - 1 - j)).
+//
+// When a unit has more than 32 rows the mma.sync kernel runs every 16-row
+// m-tile of a chunk through its own warps, and its fixed-latency MMA chains
+// cap it at 190-250 TFLOP/s whatever the bytes.  Here the unit's rows are the
+// M dimension of tcgen05 MMAs (M = 128; rows past q_len * g are padding that
+// no thread writes out):
+//   S = Q K^T   M = 128 rows, N = 64 tokens, K = 128 dims: 8 MMAs per tile
+//   O += P V    M = 128 rows, N = 128 dims, K = 64 tokens: 4 MMAs, P from TMEM
+// with S, P and O in tensor memory.  Thread r of the four softmax warps owns
+// TMEM lane r, i.e. row r, so the online softmax (lazy rescale of O when a
+// row's max grows by more than 2^8) needs no exchange between threads.
+//
+// A tile is 64 tokens = four 16-token chunks; a chunk of K (or V) arrives as
+// two TMA boxes [16 tokens x 64 dims] (128-byte swizzle) at row 16c of the
+// tile's two 64-dim halves, which makes each half one swizzled [64 x 64]
+// operand.  Chunks past the CTA's range are loaded from an out-of-range page
+// (zero fill); cached rows past the sequence's length are zeroed in shared
+// memory by the softmax warps before P.V reads them (P is 0 there, but 0 * NaN
+// would be NaN).  The planner, the partial slots and the combine are those of
+// the mma.sync kernel.
+//   warps 0, 6-8  TMA producers: warp 0 loads the unit's Q per segment (a 4-D
+//              box [q_len][g][64 dims], twice) and arms each tile's barrier;
+//              each producer warp issues one chunk's four boxes per tile (one
+//              warp issuing all 16 boxes of a tile serialises them at ~120
+//              cycles apiece, ~1 us per tile: the HBM needs one per ~0.7 us)
+//   warp 1     TMEM owner and S issuer: S(t) into one of two S slots
+//   warp 9     P.V issuer (one thread issuing both MMA chains, ~100 cycles
+//              per tcgen05.mma, set a period of ~1 us per tile)
+//   warps 2-5, 10-13  softmax and epilogue, two threads per row
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+#include "walk.cuh"
+
+namespace kv {
+
+namespace gtc {
+constexpr int D = 128;
+constexpr int TT = 64;                  // tokens per tile
+constexpr int HALF = TT * 128;          // one 64-dim half of K or V: [64 tokens x 128 B]
+constexpr int STAGE = 4 * HALF;         // K half 0, K half 1, V half 0, V half 1 (32 KB)
+constexpr int NSTAGE = 5;
+constexpr int NSTAGE_MAX = 8;
+constexpr int QHALF = 128 * 128;        // Q half [128 rows x 64 dims]
+constexpr int OFF_Q = 0;
+constexpr int OFF_ST = 2 * QHALF;
+constexpr int OFF_ML = OFF_ST + NSTAGE * STAGE;    // the epilogue's row max / sum exchange
+constexpr int OFF_BAR = OFF_ML + 4 * 128 * 4;
+constexpr int NBARS = 32;
+constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
+constexpr int THREADS = 448;
+constexpr int PV_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TM_S = 0;            // two S slots of 64 columns
+constexpr uint32_t TM_P = 128;          // two P slots of 32 columns (bf16 pairs)
+constexpr int NP = 2;                   // P slots: the softmax of tile t waits for P.V(t - 2)
+constexpr uint32_t TM_O = 256;          // O of tokens 0-31 of each tile, then of tokens 32-63
+constexpr float RESCALE = 8.f;          // log2 units
+static_assert(SMEM <= 232448, "shared memory");
+static_assert(NSTAGE <= NSTAGE_MAX, "barrier slots");
+}  // namespace gtc
+
+enum : int {
+  gQFull = 0, gQEmpty = 1, gOFree = 2,
+  gSFull0 = 3,    // 2
+  gSRead0 = 5,    // 2: the softmax warps have read S slot t % 2
+  gPFull0 = 7,    // NP: P(t) is in P slot t % NP (and the tile's tail rows zeroed)
+  gPVDone0 = 10,  // NP: P.V(t) has completed (P slot t % NP free)
+  gDrain = 13,
+  gFull0 = 14,                              // NSTAGE: the tile's K and V landed
+  gEmpty0 = gFull0 + gtc::NSTAGE_MAX,       // NSTAGE: P.V finished with the stage
+  gAbort = gEmpty0 + gtc::NSTAGE_MAX,       // an int flag in this slot
+  gDrain2 = gAbort + 1,                     // the P.V issuer's last MMAs completed
+  gNumBars = gDrain2 + 1
+};
+static_assert(gNumBars <= gtc::NBARS, "barrier slots");
+
+template <bool MQ>
+__global__ void __launch_bounds__(gtc::THREADS, 1)
+    gqa_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
+  using namespace gtc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + gAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[gQFull], 1);
+    mbar_init(&bars[gQEmpty], 1);
+    mbar_init(&bars[gOFree], 8);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[gSFull0 + i], 1);
+      mbar_init(&bars[gSRead0 + i], 8);
+    }
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(&bars[gPFull0 + i], 8);
+      mbar_init(&bars[gPVDone0 + i], 1);
+    }
+    mbar_init(&bars[gDrain], 1);
+    mbar_init(&bars[gDrain2], 1);
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&bars[gFull0 + i], 1);
+      mbar_init(&bars[gEmpty0 + i], 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  __syncwarp();
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // Launched right behind the planner: wait for its plan, and let the combine
+  // that follows get scheduled while this grid runs.
+  pdl_wait();
+  pdl_launch_dependents();
+  const int4 st = p.cta_start[c], en = p.cta_start[c + 1];
+  const uint32_t tmem = *tmem_slot;
+  const int cpp = p.bs >> 4;  // 16-token chunks per page
+
+  if (pos_less(st, en)) {
+    if (warp == 0 || (warp >= 6 && warp < PV_WARP)) {
+      // ------------------------------------------------------------- producers
+      const int pc = warp == 0 ? 0 : warp - 5;   // the chunk of each tile this warp loads
+      const uint64_t pol = policy_evict_first();
+      const int oob_page = int(p.num_blocks * p.hkv);  // past the end: zero fill
+      Walker w{p.cum, p.hkv, st, en};
+      Seg sg;
+      uint32_t t = 0, seg = 0;
+      bool ok = true;
+      while (ok && w.next(sg)) {
+        if (warp == 0 && lane == 0) {
+          if (seg > 0 && !mbar_wait(&bars[gQEmpty], (seg - 1) & 1)) {
+            ok = false;
+          } else {
+            // rows j * g + i: the box [q_len][g][64 dims] at head kvh * g
+            mbar_arrive_expect_tx(&bars[gQFull], uint32_t(2 * 128 * p.rows));
+            tma_load_4d(smem + OFF_Q, &tmQ, 0, sg.kvh * p.g, 0, sg.b, &bars[gQFull]);
+            tma_load_4d(smem + OFF_Q + QHALF, &tmQ, 64, sg.kvh * p.g, 0, sg.b, &bars[gQFull]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++seg;
+        const int32_t* row = p.bt + int64_t(sg.b) * p.max_blocks;
+        const int nch = (sg.j1 - sg.j0) * cpp;
+        for (int pb = sg.j0; pb < sg.j1 && ok; pb += 32) {
+          // block ids of pages pb .. pb + 31, one per lane
+          int page = oob_page;
+          if (pb + lane < sg.j1) {
+            const int blk = row[pb + lane];
+            if (blk < 0 || int64_t(blk) >= p.num_blocks)
+              report(p.err, KVATTN_DEVERR_BLOCK_ID);
+            else
+              page = blk * p.hkv + sg.kvh;
+          }
+          // tiles of four chunks; a tile never straddles two groups of 32 pages
+          const int c0 = (pb - sg.j0) * cpp;
+          const int c1 = min(pb + 32 - sg.j0, sg.j1 - sg.j0) * cpp;
+          for (int cc = c0; cc < c1 && ok; cc += 4) {
+            const int s = int(t % NSTAGE);
+            int lok = 1;
+            if (lane == 0) {
+              lok = mbar_wait(&bars[gEmpty0 + s], ((t / NSTAGE) & 1) ^ 1) ? 1 : 0;
+              // one arrival, and the tile's bytes from all four warps' loads
+              if (lok && warp == 0) mbar_arrive_expect_tx(&bars[gFull0 + s], uint32_t(STAGE));
+            }
+            lok = __shfl_sync(0xffffffffu, lok, 0);
+            if (!lok) {
+              ok = false;
+              break;
+            }
+            const int ci = cc + pc;                                    // this warp's chunk
+            const int src = min(max(ci / cpp - (pb - sg.j0), 0), 31);  // lane holding its page
+            const int pg_l = __shfl_sync(0xffffffffu, page, src);
+            if (lane == 0) {
+              const int pg = ci < nch ? pg_l : oob_page;
+              const int sub = ci % cpp;
+              uint8_t* dst = smem + OFF_ST + s * STAGE + pc * (16 * 128);
+              tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+              tma_load_3d(dst + HALF, &tmK, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+              tma_load_3d(dst + 2 * HALF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+              tma_load_3d(dst + 3 * HALF, &tmV, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+            }
+            ++t;   // issued: the exit drain waits for it
+            ok = __shfl_sync(0xffffffffu, lane == 0 ? (*abort_flag == 0) : true, 0);
+          }
+        }
+      }
+      if (lane == 0) {
+        if (!ok) {
+          report(p.err, KVATTN_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        // every load issued lands before the CTA exits
+        if (warp == 0 && seg > 0) mbar_wait(&bars[gQFull], (seg - 1) & 1, KV_DRAIN_WAIT_NS);
+        for (uint32_t k = t > uint32_t(NSTAGE) ? t - NSTAGE : 0u; k < t; ++k)
+          mbar_wait(&bars[gFull0 + k % NSTAGE], (k / NSTAGE) & 1, KV_DRAIN_WAIT_NS);
+      }
+    } else if (warp == 1 || warp == PV_WARP) {
+      // ---------------------------------------------- MMA issuers: S, and P.V
+      if (lane == 0) {
+        const uint32_t st0 = smem_u32(smem + OFF_ST);
+        Walker w{p.cum, p.hkv, st, en};
+        Seg sg;
+        uint32_t t = 0, seg = 0;
+        bool ok = true;
+        if (warp == 1) {
+          const uint32_t id_s = idesc_bf16(128, TT, false);
+          const uint64_t qa0 = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
+          while (ok && w.next(sg)) {
+            const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
+            if (!mbar_wait(&bars[gQFull], seg & 1)) {
+              ok = false;
+              break;
+            }
+            for (int k = 0; k < ntile && ok; ++k, ++t) {
+              // the tile's K and V, and its S slot: the softmax has read S(t - 2)
+              if ((t >= 2 && !mbar_wait(&bars[gSRead0 + (t & 1)], ((t - 2) >> 1) & 1)) ||
+                  !mbar_wait(&bars[gFull0 + t % NSTAGE], (t / NSTAGE) & 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t kd = sdesc_sw128(st0 + (t % NSTAGE) * STAGE, 16, 1024);
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;     // K: half, 16 dims
+                const uint32_t qoff = (kk >> 2) * QHALF + (kk & 3) * 32;   // Q: same dims
+                umma_ss(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t(qoff >> 4),
+                        kd + uint64_t(off >> 4), id_s, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(&bars[gSFull0 + (t & 1)]);
+              if (k == ntile - 1) umma_commit(&bars[gQEmpty]);   // every S of the segment issued
+              if (*abort_flag) ok = false;
+            }
+            ++seg;
+          }
+        } else {
+          const uint32_t id_o = idesc_bf16(128, D, true);
+          while (ok && w.next(sg)) {
+            const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
+            for (int k = 0; k < ntile && ok; ++k, ++t) {
+              // O (+)= P(t) V(t): the first tile of a segment overwrites O, once
+              // the previous segment's epilogue has read it
+              if ((k == 0 && seg > 0 && !mbar_wait(&bars[gOFree], (seg - 1) & 1)) ||
+                  !mbar_wait(&bars[gPFull0 + t % NP], (t / NP) & 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint64_t vd = sdesc_sw128(st0 + (t % NSTAGE) * STAGE + 2 * HALF, HALF, 1024);
+              // tokens 0-31 into O_0, tokens 32-63 into O_1 (the two softmax halves)
+#pragma unroll
+              for (int kk = 0; kk < TT / 16; ++kk)
+                umma_ts(tmem + TM_O + 128 * (kk >> 1), tmem + TM_P + 32 * (t % NP) + 8 * kk,
+                        vd + uint64_t((kk * 16 * 128) >> 4), id_o,
+                        (k == 0 && (kk & 1) == 0) ? 0u : 1u);
+              umma_commit(&bars[gEmpty0 + t % NSTAGE]);
+              umma_commit(&bars[gPVDone0 + t % NP]);
+              if (*abort_flag) ok = false;
+            }
+            ++seg;
+          }
+        }
+        if (!ok) {
+          report(p.err, KVATTN_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        // no MMA of this thread may still write TMEM when it is released
+        uint64_t* drain = &bars[warp == 1 ? gDrain : gDrain2];
+        umma_commit(drain);
+        mbar_wait(drain, 0, KV_DRAIN_WAIT_NS);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------- softmax / epilogue
+      // Two threads per row: warps 2-5 take tokens 0-31 of each tile (hh = 0),
+      // warps 10-13 tokens 32-63 (hh = 1).  Each half keeps its own running
+      // max, sum and O accumulator (O_hh += P[:, half] V[half, :]), so the two
+      // threads of a row never wait for each other inside a segment; the
+      // epilogue merges the halves.  With one thread per row the softmax of a
+      // 64-token tile, one warp per SM sub-partition with nothing to hide its
+      // latencies, set the kernel's pace at ~1 us per tile.
+      const int r = 32 * (warp & 3) + lane;                 // row = TMEM lane
+      const int hh = warp >= 10 ? 1 : 0;
+      const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
+      const int tid = hh * 128 + r;                         // 0..255
+      const uint32_t tm_oh = TM_O + 128 * hh;               // this half's O
+      const bool row_ok = r < p.rows;
+      // causal limit among the new tokens: row r's token is r / g
+      const int back = MQ ? p.qlen - 1 - min(r, p.rows - 1) / p.g : 0;
+      float* ml_s = reinterpret_cast<float*>(smem + OFF_ML);   // [2 halves][2][128]: m, l
+      // every wait result is warp-uniform: the TMEM instructions that follow
+      // are warp-collective
+      auto wait_all = [](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
+      };
+      Walker w{p.cum, p.hkv, st, en};
+      Seg sg;
+      uint32_t t = 0, seg = 0;
+      bool good = true;
+      while (w.next(sg)) {
+        int len = p.seq_lens[sg.b];
+        len = max(0, min(len, sg.n * p.bs));
+        const int lim = row_ok ? len - back : 0;            // this row sees tokens [0, lim)
+        const int tok_beg = sg.j0 * p.bs, tok_end = sg.j1 * p.bs;
+        const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
+        float m_ref = -INFINITY, l = 0.f;
+        for (int k = 0; k < ntile && good; ++k, ++t) {
+          good = wait_all(&bars[gSFull0 + (t & 1)], (t >> 1) & 1);
+          if (!good) break;
+          tc_fence_after();
+          uint32_t sv[32];
+          tmem_ld32(tmem + lane_off + TM_S + 64 * (t & 1) + 32 * hh, sv);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[gSRead0 + (t & 1)]);
+          const int t0 = tok_beg + TT * k + 32 * hh;          // this half's first token
+          const int nv = min(lim, tok_end) - t0;            // tokens n < nv are seen
+          float mx = -INFINITY;
+#pragma unroll
+          for (int n = 0; n < 32; ++n)
+            if (n < nv) mx = fmaxf(mx, __uint_as_float(sv[n]));
+          mx *= p.qk_scale_log2;
+          const bool grow = mx > m_ref + RESCALE;
+          if (__any_sync(0xffffffffu, grow)) {
+            const float m_new = grow ? mx : m_ref;
+            const float alpha = grow ? exp2_approx(m_ref - m_new) : 1.f;   // 0 while m_ref = -inf
+            if (k > 0) {
+              // O_hh holds this segment's earlier tiles: rescale this row once
+              // P.V(t - 1) has landed
+              good = wait_all(&bars[gPVDone0 + (t - 1) % NP], ((t - 1) / NP) & 1);
+              if (!good) break;
+              tc_fence_after();
+#pragma unroll 1
+              for (int cb = 0; cb < D; cb += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + tm_oh + cb, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                tmem_st32(tmem + lane_off + tm_oh + cb, o);
+              }
+              tmem_st_wait();
+            }
+            l = k > 0 ? l * alpha : 0.f;
+            m_ref = m_new;
+          }
+          // the P slot was last read by P.V(t - NP)
+          good = t < uint32_t(NP) || wait_all(&bars[gPVDone0 + t % NP], ((t - NP) / NP) & 1);
+          if (!good) break;
+          tc_fence_after();
+          uint32_t pk[16];
+          float ls = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = 2 * j < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j]), p.qk_scale_log2, -m_ref)) : 0.f;
+            const float a1 = 2 * j + 1 < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j + 1]), p.qk_scale_log2, -m_ref)) : 0.f;
+            ls += a0 + a1;
+            pk[j] = pack_bf16(a0, a1);
+          }
+          l += ls;
+          tmem_st16(tmem + lane_off + TM_P + 32 * (t % NP) + 16 * hh, pk);
+          tmem_st_wait();
+          const int vt = len - (tok_beg + TT * k);   // cached rows of the tile that hold tokens
+          if (vt < TT) {
+            // Zero the V rows past the sequence's end (stale or never-written
+            // slots of its last page); rows past the CTA's range came from
+            // the out-of-range page and are zero already.
+            uint8_t* vb = smem + OFF_ST + (t % NSTAGE) * STAGE + 2 * HALF;
+            const int v0 = max(vt, 0);
+            for (int idx = tid; idx < (TT - v0) * 16; idx += 256) {
+              const int row = v0 + (idx >> 4), piece = idx & 15;
+              *reinterpret_cast<uint4*>(vb + (piece >> 3) * HALF + row * 128 + (piece & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[gPFull0 + t % NP]);
+        }
+        // ---- epilogue: merge the two halves of each row.  Every softmax warp
+        // arrives here once per segment, failed or not, and they decide
+        // together (a bounded barrier would be needed otherwise).
+        const uint32_t last = t - 1;
+        good = good && wait_all(&bars[gPVDone0 + last % NP], (last / NP) & 1);
+        ml_s[(hh * 2) * 128 + r] = m_ref;
+        ml_s[(hh * 2 + 1) * 128 + r] = l;
+        if (!named_bar_and(1, 256, good)) {
+          good = false;
+          break;
+        }
+        tc_fence_after();
+        const float m0 = ml_s[r], l0 = ml_s[128 + r], m1 = ml_s[256 + r], l1 = ml_s[384 + r];
+        const float M = fmaxf(m0, m1);
+        const float a0 = m0 == -INFINITY ? 0.f : exp2_approx(m0 - M);
+        const float a1 = m1 == -INFINITY ? 0.f : exp2_approx(m1 - M);
+        const float L = l0 * a0 + l1 * a1;
+        float* dst;
+        float* dl;
+        if (sg.full) {
+          int64_t orow;
+          if constexpr (MQ) {
+            const int rr = min(r, p.rows - 1), j = rr / p.g, i = rr - j * p.g;
+            orow = (int64_t(sg.b) * p.qlen + j) * p.h + sg.kvh * p.g + i;
+          } else {
+            orow = int64_t(sg.b) * p.h + sg.kvh * p.g + min(r, p.rows - 1);
+          }
+          dst = p.out + orow * D;
+          dl = p.lse + orow;
+        } else {
+          // row r of this CTA's partial slot for the unit (slot u + c)
+          const int64_t slot = int64_t(sg.b) * p.hkv + sg.kvh + c;
+          dst = p.part_out + (slot * p.rows + min(r, p.rows - 1)) * D;
+          dl = p.part_lse + slot * p.rows + min(r, p.rows - 1);
+        }
+        const float inv = L > 0.f ? p.v_mult / L : 0.f;
+        const float f0 = a0 * inv, f1 = a1 * inv;
+        // this thread writes columns 64 hh .. 64 hh + 63 of the merged row
+#pragma unroll 1
+        for (int cb = 64 * hh; cb < 64 * hh + 64; cb += 32) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tmem + lane_off + TM_O + cb, o0);
+          tmem_ld32(tmem + lane_off + TM_O + 128 + cb, o1);
+          tmem_ld_wait();
+          if (row_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dst + cb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d4[j] = make_float4(
+                  __uint_as_float(o0[4 * j]) * f0 + __uint_as_float(o1[4 * j]) * f1,
+                  __uint_as_float(o0[4 * j + 1]) * f0 + __uint_as_float(o1[4 * j + 1]) * f1,
+                  __uint_as_float(o0[4 * j + 2]) * f0 + __uint_as_float(o1[4 * j + 2]) * f1,
+                  __uint_as_float(o0[4 * j + 3]) * f0 + __uint_as_float(o1[4 * j + 3]) * f1);
+          }
+        }
+        if (row_ok && hh == 0) *dl = L > 0.f ? (M + log2_approx(L)) * kLn2 : -INFINITY;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[gOFree]);
+        ++seg;
+      }
+      if (!good) {
+        report(p.err, KVATTN_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  }
+  // every warp is done with TMEM and with its waits
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+// Up to 32 rows the mma.sync kernel measured faster (Llama-3-70B shapes, 4 new
+// tokens: 175 against 196 us per call); from 64 rows on this one (8 new
+// tokens: 200 against 277 us).
+bool gqa_tc_applies(int dtype, int rows, int d) {
+  return dtype == KVATTN_BF16 && d == gtc::D && rows > 32 && rows <= 128;
+}
+
+int gqa_tc_ctas() {
+  static int cache[64];
+  static std::once_flag flags[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::call_once(flags[dev], [dev] {
+    cudaFuncSetAttribute(gqa_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         gtc::SMEM);
+    cudaFuncSetAttribute(gqa_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         gtc::SMEM);
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_tc_kernel<false>, gtc::THREADS,
+                                                      gtc::SMEM) != cudaSuccess)
+      n = 0;
+    const int sms = device_sm_count();
+    cache[dev] = (n > 0 && sms > 0) ? n * sms : -1;
+  });
+  return cache[dev];
+}
+
+kvattn_status launch_gqa_tc(const GqaArgs& a, const GqaParams& prm, int G) {
+  using namespace gtc;
+  if (gqa_tc_ctas() <= 0) return KVATTN_ERR_CUDA;   // also sets the shared-memory attribute
+  const kvattn_cache* cc = a.cache;
+  alignas(64) CUtensorMap tmQ, tmK, tmV;
+  // q [B][q_len][h][d] as (d, h, q_len, B); a box is one unit's rows
+  const uint64_t qdims[4] = {uint64_t(D), uint64_t(prm.h), uint64_t(prm.qlen), uint64_t(prm.B)};
+  const uint64_t qstr[3] = {uint64_t(D) * 2, uint64_t(prm.h) * D * 2,
+                            uint64_t(prm.qlen) * prm.h * D * 2};
+  const uint32_t qbox[4] = {64u, uint32_t(prm.g), uint32_t(prm.qlen), 1u};
+  const uint64_t dims[3] = {uint64_t(D), uint64_t(cc->block_size),
+                            uint64_t(cc->num_blocks) * uint64_t(cc->h_kv)};
+  const uint64_t strides[2] = {uint64_t(D) * 2, uint64_t(D) * 2 * uint64_t(cc->block_size)};
+  const uint32_t box[3] = {64u, 16u, 1u};
+  if (!encode_tensor_map_4d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, qdims, qstr, qbox,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_3d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->k, dims, strides, box,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->v, dims, strides, box,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+    return KVATTN_ERR_CUDA;
+  const cudaError_t e =
+      prm.qlen > 1 ? launch_pdl(gqa_tc_kernel<true>, dim3(G), dim3(THREADS), SMEM, a.stream, tmQ,
+                                tmK, tmV, prm)
+                   : launch_pdl(gqa_tc_kernel<false>, dim3(G), dim3(THREADS), SMEM, a.stream, tmQ,
+                                tmK, tmV, prm);
+  return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA;
+}
+
+}  // namespace kv

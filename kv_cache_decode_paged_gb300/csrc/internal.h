@@ -139,6 +139,30 @@ struct GqaArgs {
   cudaStream_t stream;
 };
 kvattn_status run_decode_gqa(const GqaArgs& a);
+// Kernel parameters of the GQA decode kernels (decode_gqa.cu, decode_gqa_tc.cu).
+struct GqaParams {
+  const uint16_t* q;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  const int64_t* cum;
+  const int4* cta_start;
+  float* out;
+  float* lse;
+  float* part_out;
+  float* part_lse;
+  int B, h, hkv, g, bs, max_blocks;
+  int qlen;   // new tokens per sequence (1: plain decode)
+  int rows;   // rows per unit: qlen * g, ordered (token j, head in group)
+  int64_t num_blocks;
+  float qk_scale_log2;  // softmax scale * log2(e), times k_scale for FP8
+  float v_mult;         // 1, or v_scale for FP8
+  int32_t* err;
+};
+// The tcgen05 form for units of many rows (decode_gqa_tc.cu): bf16 cache,
+// d_h 128, 32 < rows <= 128.  gqa_tc_ctas: its default grid (one CTA per SM).
+bool gqa_tc_applies(int dtype, int rows, int d);
+int gqa_tc_ctas();
+kvattn_status launch_gqa_tc(const GqaArgs& a, const GqaParams& prm, int G);
 // Host validation of a GQA decode call (api.cu); KVATTN_OK with *nothing set
 // for an empty batch.
 kvattn_status check_gqa_args(const void* q, const kvattn_cache* cache, const int32_t* block_table,

@@ -98,7 +98,10 @@ def _gqa_cache(**kw):
     (dict(scale=0.0), {}, kv.KVATTN_ERR_INVALID_ARG),
     (dict(maxb=0), {}, kv.KVATTN_ERR_INVALID_ARG),
     (dict(d=96), dict(d_h=96), kv.KVATTN_ERR_UNSUPPORTED),              # head dim not built
-    (dict(h=130, h_kv=1), dict(h_kv=1), kv.KVATTN_ERR_UNSUPPORTED),     # g > 64
+    (dict(h=130, h_kv=1), dict(h_kv=1), kv.KVATTN_ERR_UNSUPPORTED),     # g > 128
+    (dict(h=80, h_kv=1), dict(h_kv=1, dtype=kv.KVATTN_FP8_E4M3),
+     kv.KVATTN_ERR_UNSUPPORTED),                                        # FP8: g > 64
+    (dict(h=80, h_kv=1, d=64), dict(h_kv=1, d_h=64), kv.KVATTN_ERR_UNSUPPORTED),  # d 64: g > 64
     ({}, dict(block_size=8), kv.KVATTN_ERR_UNSUPPORTED),
     ({}, dict(block_size=40), kv.KVATTN_ERR_UNSUPPORTED),             # not whole 16-token chunks
     ({}, dict(block_size=512), kv.KVATTN_ERR_UNSUPPORTED),            # more than 16 chunks
@@ -156,7 +159,7 @@ def test_gqa_multi_host_validation(lib):
 
     assert call(q_len=0) == kv.KVATTN_ERR_INVALID_ARG
     assert call(q_len=-3) == kv.KVATTN_ERR_INVALID_ARG
-    assert call(h=32, q_len=5) == kv.KVATTN_ERR_UNSUPPORTED     # 16 heads x 5 tokens > 64 rows
+    assert call(h=32, q_len=9) == kv.KVATTN_ERR_UNSUPPORTED     # 16 heads x 9 tokens > 128 rows
     assert call(h=7) == kv.KVATTN_ERR_INVALID_ARG                # h % h_kv != 0
     assert call(batch=0) == kv.KVATTN_OK                         # nothing to do, nothing launched
 

@@ -100,5 +100,10 @@ def test_rejects_too_many_rows():
     wl = inputs.make_workload("llama3_70b", lens=[100])   # g = 8
     g = GpuWorkload(wl)
     with pytest.raises(kv.KvattnError) as e:
-        g.decode_multi(inputs.multi_token_queries(wl, 9))   # 72 rows > 64
+        g.decode_multi(inputs.multi_token_queries(wl, 17))   # 136 rows > 128
+    assert e.value.status == kv.KVATTN_ERR_UNSUPPORTED
+    wl8 = inputs.make_workload("llama3_70b_fp8", lens=[100])
+    g8 = GpuWorkload(wl8)
+    with pytest.raises(kv.KvattnError) as e:
+        g8.decode_multi(inputs.multi_token_queries(wl8, 9))   # FP8: 72 rows > 64
     assert e.value.status == kv.KVATTN_ERR_UNSUPPORTED
