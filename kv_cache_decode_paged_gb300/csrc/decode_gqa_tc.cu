@@ -57,7 +57,9 @@ constexpr int QHALF = 128 * 128;        // Q half [128 rows x 64 dims]
 constexpr int OFF_Q = 0;
 constexpr int OFF_ST = 2 * QHALF;
 constexpr int OFF_ML = OFF_ST + NSTAGE * STAGE;    // the epilogue's row max / sum exchange
-constexpr int OFF_BAR = OFF_ML + 4 * 128 * 4;
+constexpr int OFF_XB = OFF_ML + 4 * 128 * 4;       // the epilogue's merge of the row copies
+constexpr int XB_BYTES = 2 * 3 * 32 * 32 * 4;      // [hh][copy - 1][row][32 columns], 4 copies
+constexpr int OFF_BAR = OFF_XB + XB_BYTES;
 constexpr int NBARS = 32;
 constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
 constexpr int THREADS = 448;
@@ -87,7 +89,10 @@ enum : int {
 };
 static_assert(gNumBars <= gtc::NBARS, "barrier slots");
 
-template <bool MQ>
+// DUP copies of the unit's rows fill the MMA's 128 rows (rows <= 128 / DUP):
+// copy c sits at rows [c * 128 / DUP, (c + 1) * 128 / DUP).  Their scores are
+// equal; each copy's threads take a different part of the tile's tokens.
+template <bool MQ, int DUP>
 __global__ void __launch_bounds__(gtc::THREADS, 1)
     gqa_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
@@ -156,10 +161,14 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           if (seg > 0 && !mbar_wait(&bars[gQEmpty], (seg - 1) & 1)) {
             ok = false;
           } else {
-            // rows j * g + i: the box [q_len][g][64 dims] at head kvh * g
-            mbar_arrive_expect_tx(&bars[gQFull], uint32_t(2 * 128 * p.rows));
-            tma_load_4d(smem + OFF_Q, &tmQ, 0, sg.kvh * p.g, 0, sg.b, &bars[gQFull]);
-            tma_load_4d(smem + OFF_Q + QHALF, &tmQ, 64, sg.kvh * p.g, 0, sg.b, &bars[gQFull]);
+            // rows j * g + i: the box [q_len][g][64 dims] at head kvh * g, once
+            // per copy
+            mbar_arrive_expect_tx(&bars[gQFull], uint32_t(2 * DUP * 128 * p.rows));
+            for (int cp = 0; cp < DUP; ++cp) {
+              uint8_t* qd = smem + OFF_Q + cp * (128 / DUP) * 128;
+              tma_load_4d(qd, &tmQ, 0, sg.kvh * p.g, 0, sg.b, &bars[gQFull]);
+              tma_load_4d(qd + QHALF, &tmQ, 64, sg.kvh * p.g, 0, sg.b, &bars[gQFull]);
+            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -298,22 +307,32 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
       __syncwarp();
     } else {
       // ---------------------------------------------------- softmax / epilogue
-      // Two threads per row: warps 2-5 take tokens 0-31 of each tile (hh = 0),
-      // warps 10-13 tokens 32-63 (hh = 1).  Each half keeps its own running
-      // max, sum and O accumulator (O_hh += P[:, half] V[half, :]), so the two
-      // threads of a row never wait for each other inside a segment; the
-      // epilogue merges the halves.  With one thread per row the softmax of a
-      // 64-token tile, one warp per SM sub-partition with nothing to hide its
-      // latencies, set the kernel's pace at ~1 us per tile.
-      const int r = 32 * (warp & 3) + lane;                 // row = TMEM lane
+      // Threads by MMA row (TMEM lane) m and token half hh: warps 2-5 take the
+      // tile's tokens 0-31 (hh = 0), warps 10-13 tokens 32-63 (hh = 1).  Row m
+      // is copy c = m / RP of unit row r = m % RP, and of its half the thread
+      // takes the TP tokens of part c.  Each (lane, half) keeps its own
+      // running max, sum and share of O_hh (O_hh += P[:, half] V[half, :]), so
+      // the threads never wait for each other inside a segment; the epilogue
+      // merges the 2 DUP states of each row.  (With one thread per row the
+      // softmax, one warp per SM sub-partition with nothing to hide its
+      // latencies, set the kernel's pace at ~1 us per 64-token tile; TMEM lane
+      // quadrant q is readable only from sub-partition q, so spare MMA rows
+      // spread the work only by holding copies.)
+      constexpr int RP = 128 / DUP;                         // rows per copy
+      constexpr int TP = 32 / DUP;                          // tokens per thread and tile
+      const int m = 32 * (warp & 3) + lane;                 // MMA row = TMEM lane
+      const int cpy = m / RP, r = m % RP;
       const int hh = warp >= 10 ? 1 : 0;
+      const int part = 32 * hh + TP * cpy;                  // first token of this thread's part
       const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
-      const int tid = hh * 128 + r;                         // 0..255
+      const int tid = hh * 128 + m;                         // 0..255
       const uint32_t tm_oh = TM_O + 128 * hh;               // this half's O
       const bool row_ok = r < p.rows;
       // causal limit among the new tokens: row r's token is r / g
       const int back = MQ ? p.qlen - 1 - min(r, p.rows - 1) / p.g : 0;
-      float* ml_s = reinterpret_cast<float*>(smem + OFF_ML);   // [2 halves][2][128]: m, l
+      float* ml_s = reinterpret_cast<float*>(smem + OFF_ML);   // [hh][m or l][128 lanes]
+      float4* xb = reinterpret_cast<float4*>(smem + OFF_XB);   // [hh][copy - 1][RP][8]
+      static_assert(2 * (DUP - 1) * RP * 8 * 16 <= XB_BYTES, "merge buffer");
       // every wait result is warp-uniform: the TMEM instructions that follow
       // are warp-collective
       auto wait_all = [](uint64_t* bar, uint32_t parity) {
@@ -334,17 +353,20 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           good = wait_all(&bars[gSFull0 + (t & 1)], (t >> 1) & 1);
           if (!good) break;
           tc_fence_after();
-          uint32_t sv[32];
-          tmem_ld32(tmem + lane_off + TM_S + 64 * (t & 1) + 32 * hh, sv);
+          uint32_t sv[TP];
+          const uint32_t sa = tmem + lane_off + TM_S + 64 * (t & 1) + part;
+          if constexpr (TP == 32) tmem_ld32(sa, sv);
+          else if constexpr (TP == 16) tmem_ld16(sa, sv);
+          else tmem_ld8(sa, sv);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[gSRead0 + (t & 1)]);
-          const int t0 = tok_beg + TT * k + 32 * hh;          // this half's first token
+          const int t0 = tok_beg + TT * k + part;           // this thread's first token
           const int nv = min(lim, tok_end) - t0;            // tokens n < nv are seen
           float mx = -INFINITY;
 #pragma unroll
-          for (int n = 0; n < 32; ++n)
+          for (int n = 0; n < TP; ++n)
             if (n < nv) mx = fmaxf(mx, __uint_as_float(sv[n]));
           mx *= p.qk_scale_log2;
           const bool grow = mx > m_ref + RESCALE;
@@ -375,16 +397,21 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           good = t < uint32_t(NP) || wait_all(&bars[gPVDone0 + t % NP], ((t - NP) / NP) & 1);
           if (!good) break;
           tc_fence_after();
-          uint32_t pk[16];
+          uint32_t pv[TP / 2];
           float ls = 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < TP / 2; ++j) {
             const float a0 = 2 * j < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j]), p.qk_scale_log2, -m_ref)) : 0.f;
             const float a1 = 2 * j + 1 < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j + 1]), p.qk_scale_log2, -m_ref)) : 0.f;
             ls += a0 + a1;
-            pk[j] = pack_bf16(a0, a1);
+            pv[j] = pack_bf16(a0, a1);
           }
           l += ls;
+          // this half's 32 tokens as 16 bf16 pairs: this copy's part, zeros
+          // elsewhere (the other copies' rows hold the other parts)
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = (i / (TP / 2) == cpy) ? pv[i % (TP / 2)] : 0u;
           tmem_st16(tmem + lane_off + TM_P + 32 * (t % NP) + 16 * hh, pk);
           tmem_st_wait();
           const int vt = len - (tok_beg + TT * k);   // cached rows of the tile that hold tokens
@@ -405,25 +432,38 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars[gPFull0 + t % NP]);
         }
-        // ---- epilogue: merge the two halves of each row.  Every softmax warp
-        // arrives here once per segment, failed or not, and they decide
-        // together (a bounded barrier would be needed otherwise).
+        // ---- epilogue: merge the 2 DUP states of each row.  Every softmax
+        // warp arrives here once per segment, failed or not, and they decide
+        // together.
         const uint32_t last = t - 1;
         good = good && wait_all(&bars[gPVDone0 + last % NP], (last / NP) & 1);
-        ml_s[(hh * 2) * 128 + r] = m_ref;
-        ml_s[(hh * 2 + 1) * 128 + r] = l;
+        ml_s[(hh * 2) * 128 + m] = m_ref;
+        ml_s[(hh * 2 + 1) * 128 + m] = l;
         if (!named_bar_and(1, 256, good)) {
           good = false;
           break;
         }
         tc_fence_after();
-        const float m0 = ml_s[r], l0 = ml_s[128 + r], m1 = ml_s[256 + r], l1 = ml_s[384 + r];
-        const float M = fmaxf(m0, m1);
-        const float a0 = m0 == -INFINITY ? 0.f : exp2_approx(m0 - M);
-        const float a1 = m1 == -INFINITY ? 0.f : exp2_approx(m1 - M);
-        const float L = l0 * a0 + l1 * a1;
-        float* dst;
-        float* dl;
+        float M = -INFINITY;
+#pragma unroll
+        for (int c2 = 0; c2 < DUP; ++c2)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) M = fmaxf(M, ml_s[(h2 * 2) * 128 + c2 * RP + r]);
+        float L = 0.f;
+#pragma unroll
+        for (int c2 = 0; c2 < DUP; ++c2)
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const float mm = ml_s[(h2 * 2) * 128 + c2 * RP + r];
+            if (mm != -INFINITY) L += ml_s[(h2 * 2 + 1) * 128 + c2 * RP + r] * exp2_approx(mm - M);
+          }
+        const float inv = L > 0.f ? p.v_mult / L : 0.f;
+        // this lane's two states: (copy, half 0) in O_0 and (copy, half 1) in O_1
+        const float m0 = ml_s[m], m1 = ml_s[256 + m];
+        const float f0 = m0 == -INFINITY ? 0.f : exp2_approx(m0 - M) * inv;
+        const float f1 = m1 == -INFINITY ? 0.f : exp2_approx(m1 - M) * inv;
+        float* dst = nullptr;
+        float* dl = nullptr;
         if (sg.full) {
           int64_t orow;
           if constexpr (MQ) {
@@ -440,27 +480,51 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           dst = p.part_out + (slot * p.rows + min(r, p.rows - 1)) * D;
           dl = p.part_lse + slot * p.rows + min(r, p.rows - 1);
         }
-        const float inv = L > 0.f ? p.v_mult / L : 0.f;
-        const float f0 = a0 * inv, f1 = a1 * inv;
-        // this thread writes columns 64 hh .. 64 hh + 63 of the merged row
+        // this thread's columns: 64 hh .. 64 hh + 63 of the merged row, 32 at
+        // a time; copies other than 0 hand their share to copy 0 through
+        // shared memory (16-byte pieces swizzled by row)
 #pragma unroll 1
         for (int cb = 64 * hh; cb < 64 * hh + 64; cb += 32) {
           uint32_t o0[32], o1[32];
           tmem_ld32(tmem + lane_off + TM_O + cb, o0);
           tmem_ld32(tmem + lane_off + TM_O + 128 + cb, o1);
           tmem_ld_wait();
-          if (row_ok) {
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = __uint_as_float(o0[j]) * f0 + __uint_as_float(o1[j]) * f1;
+          if constexpr (DUP > 1) {
+            float4* xr = xb + ((hh * (DUP - 1) + (cpy > 0 ? cpy - 1 : 0)) * RP + r) * 8;
+            if (cpy > 0) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                xr[j ^ (r & 7)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+            named_bar_sync(2, 256);
+            if (cpy == 0) {
+#pragma unroll
+              for (int c2 = 1; c2 < DUP; ++c2) {
+                const float4* xs = xb + ((hh * (DUP - 1) + c2 - 1) * RP + r) * 8;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 a = xs[j ^ (r & 7)];
+                  v[4 * j] += a.x;
+                  v[4 * j + 1] += a.y;
+                  v[4 * j + 2] += a.z;
+                  v[4 * j + 3] += a.w;
+                }
+              }
+            }
+            named_bar_sync(2, 256);   // the buffer is rewritten by the next round
+          }
+          if (cpy == 0 && row_ok) {
             float4* d4 = reinterpret_cast<float4*>(dst + cb);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              d4[j] = make_float4(
-                  __uint_as_float(o0[4 * j]) * f0 + __uint_as_float(o1[4 * j]) * f1,
-                  __uint_as_float(o0[4 * j + 1]) * f0 + __uint_as_float(o1[4 * j + 1]) * f1,
-                  __uint_as_float(o0[4 * j + 2]) * f0 + __uint_as_float(o1[4 * j + 2]) * f1,
-                  __uint_as_float(o0[4 * j + 3]) * f0 + __uint_as_float(o1[4 * j + 3]) * f1);
+            for (int j = 0; j < 8; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           }
         }
-        if (row_ok && hh == 0) *dl = L > 0.f ? (M + log2_approx(L)) * kLn2 : -INFINITY;
+        if (cpy == 0 && row_ok && hh == 0)
+          *dl = L > 0.f ? (M + log2_approx(L)) * kLn2 : -INFINITY;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[gOFree]);
@@ -486,8 +550,11 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
 // Up to 32 rows the mma.sync kernel measured faster (Llama-3-70B shapes, 4 new
 // tokens: 175 against 196 us per call); from 64 rows on this one (8 new
 // tokens: 200 against 277 us).
+#ifndef KV_GQA_TC_MIN_ROWS
+#define KV_GQA_TC_MIN_ROWS 33
+#endif
 bool gqa_tc_applies(int dtype, int rows, int d) {
-  return dtype == KVATTN_BF16 && d == gtc::D && rows > 32 && rows <= 128;
+  return dtype == KVATTN_BF16 && d == gtc::D && rows >= KV_GQA_TC_MIN_ROWS && rows <= 128;
 }
 
 int gqa_tc_ctas() {
@@ -496,12 +563,13 @@ int gqa_tc_ctas() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   std::call_once(flags[dev], [dev] {
-    cudaFuncSetAttribute(gqa_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         gtc::SMEM);
-    cudaFuncSetAttribute(gqa_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         gtc::SMEM);
+    const void* ks[6] = {(const void*)gqa_tc_kernel<true, 1>, (const void*)gqa_tc_kernel<true, 2>,
+                         (const void*)gqa_tc_kernel<true, 4>, (const void*)gqa_tc_kernel<false, 1>,
+                         (const void*)gqa_tc_kernel<false, 2>, (const void*)gqa_tc_kernel<false, 4>};
+    for (const void* k : ks)
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gtc::SMEM);
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_tc_kernel<false>, gtc::THREADS,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_tc_kernel<false, 1>, gtc::THREADS,
                                                       gtc::SMEM) != cudaSuccess)
       n = 0;
     const int sms = device_sm_count();
@@ -531,11 +599,18 @@ kvattn_status launch_gqa_tc(const GqaArgs& a, const GqaParams& prm, int G) {
       !encode_tensor_map_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->v, dims, strides, box,
                             CU_TENSOR_MAP_SWIZZLE_128B))
     return KVATTN_ERR_CUDA;
-  const cudaError_t e =
-      prm.qlen > 1 ? launch_pdl(gqa_tc_kernel<true>, dim3(G), dim3(THREADS), SMEM, a.stream, tmQ,
-                                tmK, tmV, prm)
-                   : launch_pdl(gqa_tc_kernel<false>, dim3(G), dim3(THREADS), SMEM, a.stream, tmQ,
-                                tmK, tmV, prm);
+  // rows <= 32: four copies of the rows in the MMA's 128, <= 64: two, else one
+  cudaError_t e;
+  const dim3 grid(G), block(THREADS);
+  if (prm.qlen > 1) {
+    e = prm.rows <= 32   ? launch_pdl(gqa_tc_kernel<true, 4>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
+        : prm.rows <= 64 ? launch_pdl(gqa_tc_kernel<true, 2>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
+                         : launch_pdl(gqa_tc_kernel<true, 1>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm);
+  } else {
+    e = prm.rows <= 32   ? launch_pdl(gqa_tc_kernel<false, 4>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
+        : prm.rows <= 64 ? launch_pdl(gqa_tc_kernel<false, 2>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
+                         : launch_pdl(gqa_tc_kernel<false, 1>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm);
+  }
   return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA;
 }
 

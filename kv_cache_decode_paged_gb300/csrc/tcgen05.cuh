@@ -139,6 +139,18 @@ KV_DEVI void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : KV_R8(0), KV_R8(8), KV_R8(16), KV_R8(24)
       : "r"(taddr));
 }
+KV_DEVI void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : KV_R8(0), KV_R8(8)
+      : "r"(taddr));
+}
+KV_DEVI void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : KV_R8(0)
+               : "r"(taddr));
+}
 KV_DEVI void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 KV_DEVI void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
