@@ -124,9 +124,8 @@ kvattn_status check_gqa_args(const void* q, const kvattn_cache* cache, const int
   if (cache->dtype == KVATTN_FP8_E4M3 && !(cache->k_scale > 0.f && cache->v_scale > 0.f))
     return KVATTN_ERR_INVALID_ARG;
   const int g = h / h_kv;
-  // rows per KV head: four 16-row m-tiles, or one 128-row tcgen05 tile (bf16, d_h 128)
-  if (int64_t(g) * q_len > (cache->dtype == KVATTN_BF16 && d_h == 128 ? 128 : 64))
-    return KVATTN_ERR_UNSUPPORTED;
+  // rows per KV head: four 16-row m-tiles, or one 128-row tcgen05 tile (d_h 128)
+  if (int64_t(g) * q_len > (d_h == 128 ? 128 : 64)) return KVATTN_ERR_UNSUPPORTED;
   if (d_h != 64 && d_h != 128) return KVATTN_ERR_UNSUPPORTED;
   if (cache->dtype == KVATTN_FP8_E4M3 && d_h != 128) return KVATTN_ERR_UNSUPPORTED;
   // whole 16-token TMA chunks per block, at most 16 of them

@@ -35,6 +35,7 @@
 //   warp 9     P.V issuer (one thread issuing both MMA chains, ~100 cycles
 //              per tcgen05.mma, set a period of ~1 us per tile)
 //   warps 2-5, 10-13  softmax and epilogue, two threads per row
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include <mutex>
@@ -49,19 +50,29 @@ namespace kv {
 namespace gtc {
 constexpr int D = 128;
 constexpr int TT = 64;                  // tokens per tile
-constexpr int HALF = TT * 128;          // one 64-dim half of K or V: [64 tokens x 128 B]
-constexpr int STAGE = 4 * HALF;         // K half 0, K half 1, V half 0, V half 1 (32 KB)
-constexpr int NSTAGE = 5;
+constexpr int HALF = TT * 128;          // [64 tokens x 128 B]: 64 bf16 dims, or 128 E4M3 codes
 constexpr int NSTAGE_MAX = 8;
-constexpr int QHALF = 128 * 128;        // Q half [128 rows x 64 dims]
+constexpr int QHALF = 128 * 128;        // [128 rows x 128 B]: Q's dims 0-63 / 64-127 (bf16), or
+                                        // its hi / lo E4M3 term (128 codes)
 constexpr int OFF_Q = 0;
 constexpr int OFF_ST = 2 * QHALF;
-constexpr int OFF_ML = OFF_ST + NSTAGE * STAGE;    // the epilogue's row max / sum exchange
-constexpr int OFF_XB = OFF_ML + 4 * 128 * 4;       // the epilogue's merge of the row copies
 constexpr int XB_BYTES = 2 * 3 * 32 * 32 * 4;      // [hh][copy - 1][row][32 columns], 4 copies
-constexpr int OFF_BAR = OFF_XB + XB_BYTES;
 constexpr int NBARS = 32;
-constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
+// Per cache format.  bf16: a stage is K dims 0-63, K dims 64-127, V dims 0-63,
+// V dims 64-127 (32 KB); E4M3: K codes, V codes (16 KB), so twice the stages.
+template <bool FP8>
+struct Lay {
+  static constexpr int STAGE = FP8 ? 2 * HALF : 4 * HALF;
+  static constexpr int NSTAGE = FP8 ? 8 : 5;
+  static constexpr int V_OFF = FP8 ? HALF : 2 * HALF;        // V within a stage
+  static constexpr int OFF_ML = OFF_ST + NSTAGE * STAGE;      // the epilogue's row max / sum exchange
+  static constexpr int OFF_QF = OFF_ML + 4 * 128 * 4;         // E4M3: each row's 2^-e
+  static constexpr int OFF_XB = OFF_QF + 128 * 4;             // the epilogue's merge of the row copies
+  static constexpr int OFF_BAR = OFF_XB + XB_BYTES;
+  static constexpr int SMEM = 1024 + OFF_BAR + NBARS * 8 + 16;
+  static_assert(SMEM <= 232448, "shared memory");
+  static_assert(NSTAGE <= NSTAGE_MAX, "barrier slots");
+};
 constexpr int THREADS = 448;
 constexpr int PV_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
@@ -70,8 +81,6 @@ constexpr uint32_t TM_P = 128;          // two P slots of 32 columns (bf16 pairs
 constexpr int NP = 2;                   // P slots: the softmax of tile t waits for P.V(t - 2)
 constexpr uint32_t TM_O = 256;          // O of tokens 0-31 of each tile, then of tokens 32-63
 constexpr float RESCALE = 8.f;          // log2 units
-static_assert(SMEM <= 232448, "shared memory");
-static_assert(NSTAGE <= NSTAGE_MAX, "barrier slots");
 }  // namespace gtc
 
 enum : int {
@@ -85,18 +94,95 @@ enum : int {
   gEmpty0 = gFull0 + gtc::NSTAGE_MAX,       // NSTAGE: P.V finished with the stage
   gAbort = gEmpty0 + gtc::NSTAGE_MAX,       // an int flag in this slot
   gDrain2 = gAbort + 1,                     // the P.V issuer's last MMAs completed
-  gNumBars = gDrain2 + 1
+  gNumBars = gDrain2 + 1,
+  gQBuilt = gQFull                          // E4M3: the softmax warps built Q's terms (no TMA)
 };
 static_assert(gNumBars <= gtc::NBARS, "barrier slots");
+
+// Two E4M3 terms of a float pair: hi = e4m3(x), lo = e4m3(x - hi), each a
+// 16-bit code pair (first value in the low byte).
+KV_DEVI void e4m3_two_terms_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = e4m3x2(x0, x1);
+  const uint32_t hf = e4m3x2_to_f16x2(uint16_t(hi));
+  const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hf));
+  lo = e4m3x2(x0 - h.x, x1 - h.y);
+}
+
+// E4M3 cache: MMA row m (copy of unit row r) of the query as two E4M3 terms,
+// x 2^e with e chosen so that the row's largest magnitude lands in [128, 256):
+// hi codes at q + m * 128, lo codes at q + QHALF + m * 128, in the 128-byte
+// swizzled K-major layout; 2^-e to qf[m].  Rows past the unit's are zero.
+KV_DEVI void build_q_terms(const GqaParams& p, const Seg& sg, int r, bool row_ok, uint8_t* q,
+                           int m, float* qf) {
+  int64_t qi = 0;
+  if (row_ok) {
+    if (p.qlen > 1) {
+      const int j = r / p.g, i = r - j * p.g;
+      qi = (int64_t(sg.b) * p.qlen + j) * p.h + sg.kvh * p.g + i;
+    } else {
+      qi = int64_t(sg.b) * p.h + sg.kvh * p.g + r;
+    }
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + qi * gtc::D);
+  auto lo16 = [](uint32_t w) { return __uint_as_float(w << 16); };
+  auto hi16 = [](uint32_t w) { return __uint_as_float(w & 0xffff0000u); };
+  // pass 1: the row's largest magnitude (eight loads in flight at a time)
+  float mx = 0.f;
+#pragma unroll 1
+  for (int g0 = 0; g0 < 16; g0 += 8) {
+    uint4 x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = row_ok ? __ldg(src + g0 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx = fmaxf(mx, fmaxf(fabsf(lo16(w[k])), fabsf(hi16(w[k]))));
+    }
+  }
+  const int e = mx > 0.f ? min(max(7 - (int((__float_as_uint(mx) >> 23) & 255) - 127), -120), 120) : 0;
+  const float sc = __uint_as_float(uint32_t(127 + e) << 23);
+  qf[m] = __uint_as_float(uint32_t(127 - e) << 23);
+  // pass 2: 16 dims (one 16-byte piece of codes per term) at a time
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    const uint4 x0 = row_ok ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
+    const uint4 x1 = row_ok ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+    const uint32_t wv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t h0, l0, h1, l1;
+      e4m3_two_terms_pair(lo16(wv[2 * k]) * sc, hi16(wv[2 * k]) * sc, h0, l0);
+      e4m3_two_terms_pair(lo16(wv[2 * k + 1]) * sc, hi16(wv[2 * k + 1]) * sc, h1, l1);
+      hw[k] = h0 | (h1 << 16);
+      lw[k] = l0 | (l1 << 16);
+    }
+    const int off = m * 128 + ((c ^ (m & 7)) << 4);
+    *reinterpret_cast<uint4*>(q + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(q + gtc::QHALF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
 
 // DUP copies of the unit's rows fill the MMA's 128 rows (rows <= 128 / DUP):
 // copy c sits at rows [c * 128 / DUP, (c + 1) * 128 / DUP).  Their scores are
 // equal; each copy's threads take a different part of the tile's tokens.
-template <bool MQ, int DUP>
+//
+// E4M3 cache (FP8): the MMAs are kind::f8f6f4 (K = 32, both operands E4M3).
+// The cached codes are used as stored; the query and the probabilities enter
+// as two E4M3 terms each, hi = e4m3(x) and lo = e4m3(x - hi).  The softmax
+// warps of the first token half build each row's query terms from bf16 at a
+// segment's start, scaled by 2^e that brings the row's largest magnitude into
+// [128, 256); the scores are multiplied back by 2^-e and k_scale, O by
+// v_scale.
+template <bool MQ, int DUP, bool FP8>
 __global__ void __launch_bounds__(gtc::THREADS, 1)
     gqa_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
   using namespace gtc;
+  using L = Lay<FP8>;
+  constexpr int STAGE = L::STAGE, NSTAGE = L::NSTAGE, V_OFF = L::V_OFF;
+  constexpr int OFF_ML = L::OFF_ML, OFF_QF = L::OFF_QF, OFF_XB = L::OFF_XB, OFF_BAR = L::OFF_BAR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -107,7 +193,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
   const int c = blockIdx.x;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[gQFull], 1);
+    mbar_init(&bars[gQFull], FP8 ? 4 : 1);   // TMA (bf16), or the four builder warps (E4M3)
     mbar_init(&bars[gQEmpty], 1);
     mbar_init(&bars[gOFree], 8);
     for (int i = 0; i < 2; ++i) {
@@ -157,7 +243,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
       uint32_t t = 0, seg = 0;
       bool ok = true;
       while (ok && w.next(sg)) {
-        if (warp == 0 && lane == 0) {
+        if (!FP8 && warp == 0 && lane == 0) {
           if (seg > 0 && !mbar_wait(&bars[gQEmpty], (seg - 1) & 1)) {
             ok = false;
           } else {
@@ -209,10 +295,15 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
               const int pg = ci < nch ? pg_l : oob_page;
               const int sub = ci % cpp;
               uint8_t* dst = smem + OFF_ST + s * STAGE + pc * (16 * 128);
-              tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
-              tma_load_3d(dst + HALF, &tmK, 64, sub * 16, pg, &bars[gFull0 + s], pol);
-              tma_load_3d(dst + 2 * HALF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
-              tma_load_3d(dst + 3 * HALF, &tmV, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+              if constexpr (FP8) {   // one box of 128 codes per row for K and for V
+                tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+                tma_load_3d(dst + V_OFF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+              } else {
+                tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+                tma_load_3d(dst + HALF, &tmK, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+                tma_load_3d(dst + V_OFF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+                tma_load_3d(dst + V_OFF + HALF, &tmV, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+              }
             }
             ++t;   // issued: the exit drain waits for it
             ok = __shfl_sync(0xffffffffu, lane == 0 ? (*abort_flag == 0) : true, 0);
@@ -225,7 +316,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           *abort_flag = 1;
         }
         // every load issued lands before the CTA exits
-        if (warp == 0 && seg > 0) mbar_wait(&bars[gQFull], (seg - 1) & 1, KV_DRAIN_WAIT_NS);
+        if (!FP8 && warp == 0 && seg > 0) mbar_wait(&bars[gQFull], (seg - 1) & 1, KV_DRAIN_WAIT_NS);
         for (uint32_t k = t > uint32_t(NSTAGE) ? t - NSTAGE : 0u; k < t; ++k)
           mbar_wait(&bars[gFull0 + k % NSTAGE], (k / NSTAGE) & 1, KV_DRAIN_WAIT_NS);
       }
@@ -238,7 +329,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
         uint32_t t = 0, seg = 0;
         bool ok = true;
         if (warp == 1) {
-          const uint32_t id_s = idesc_bf16(128, TT, false);
+          const uint32_t id_s = FP8 ? idesc_e4m3(128, TT, false) : idesc_bf16(128, TT, false);
           const uint64_t qa0 = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
           while (ok && w.next(sg)) {
             const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
@@ -255,12 +346,23 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
               }
               tc_fence_after();
               const uint64_t kd = sdesc_sw128(st0 + (t % NSTAGE) * STAGE, 16, 1024);
+              if constexpr (FP8) {
+                // 32 codes per MMA: the hi term of Q, then the lo term
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;     // K: half, 16 dims
-                const uint32_t qoff = (kk >> 2) * QHALF + (kk & 3) * 32;   // Q: same dims
-                umma_ss(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t(qoff >> 4),
-                        kd + uint64_t(off >> 4), id_s, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 32; ++kk) {
+                  umma_ss_f8(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t((kk * 32) >> 4),
+                             kd + uint64_t((kk * 32) >> 4), id_s, kk > 0 ? 1u : 0u);
+                  umma_ss_f8(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t((QHALF + kk * 32) >> 4),
+                             kd + uint64_t((kk * 32) >> 4), id_s, 1u);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                  const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;     // K: half, 16 dims
+                  const uint32_t qoff = (kk >> 2) * QHALF + (kk & 3) * 32;   // Q: same dims
+                  umma_ss(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t(qoff >> 4),
+                          kd + uint64_t(off >> 4), id_s, kk > 0 ? 1u : 0u);
+                }
               }
               umma_commit(&bars[gSFull0 + (t & 1)]);
               if (k == ntile - 1) umma_commit(&bars[gQEmpty]);   // every S of the segment issued
@@ -269,7 +371,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
             ++seg;
           }
         } else {
-          const uint32_t id_o = idesc_bf16(128, D, true);
+          const uint32_t id_o = FP8 ? idesc_e4m3(128, D, true) : idesc_bf16(128, D, true);
           while (ok && w.next(sg)) {
             const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
             for (int k = 0; k < ntile && ok; ++k, ++t) {
@@ -281,13 +383,25 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
                 break;
               }
               tc_fence_after();
-              const uint64_t vd = sdesc_sw128(st0 + (t % NSTAGE) * STAGE + 2 * HALF, HALF, 1024);
+              const uint64_t vd = sdesc_sw128(st0 + (t % NSTAGE) * STAGE + V_OFF, HALF, 1024);
               // tokens 0-31 into O_0, tokens 32-63 into O_1 (the two softmax halves)
+              if constexpr (FP8) {
+                // 32 tokens per MMA, for the hi and the lo term of P (P slot
+                // columns: hi half 0, hi half 1, lo half 0, lo half 1, 8 each)
 #pragma unroll
-              for (int kk = 0; kk < TT / 16; ++kk)
-                umma_ts(tmem + TM_O + 128 * (kk >> 1), tmem + TM_P + 32 * (t % NP) + 8 * kk,
-                        vd + uint64_t((kk * 16 * 128) >> 4), id_o,
-                        (k == 0 && (kk & 1) == 0) ? 0u : 1u);
+                for (int kk = 0; kk < 4; ++kk) {
+                  const int h2 = kk & 1, term = kk >> 1;
+                  umma_ts_f8(tmem + TM_O + 128 * h2, tmem + TM_P + 32 * (t % NP) + 16 * term + 8 * h2,
+                             vd + uint64_t((h2 * 32 * 128) >> 4), id_o,
+                             (k == 0 && term == 0) ? 0u : 1u);
+                }
+              } else {
+#pragma unroll
+                for (int kk = 0; kk < TT / 16; ++kk)
+                  umma_ts(tmem + TM_O + 128 * (kk >> 1), tmem + TM_P + 32 * (t % NP) + 8 * kk,
+                          vd + uint64_t((kk * 16 * 128) >> 4), id_o,
+                          (k == 0 && (kk & 1) == 0) ? 0u : 1u);
+              }
               umma_commit(&bars[gEmpty0 + t % NSTAGE]);
               umma_commit(&bars[gPVDone0 + t % NP]);
               if (*abort_flag) ok = false;
@@ -331,6 +445,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
       // causal limit among the new tokens: row r's token is r / g
       const int back = MQ ? p.qlen - 1 - min(r, p.rows - 1) / p.g : 0;
       float* ml_s = reinterpret_cast<float*>(smem + OFF_ML);   // [hh][m or l][128 lanes]
+      float* qf_s = reinterpret_cast<float*>(smem + OFF_QF);   // E4M3: [128 lanes] 2^-e
       float4* xb = reinterpret_cast<float4*>(smem + OFF_XB);   // [hh][copy - 1][RP][8]
       static_assert(2 * (DUP - 1) * RP * 8 * 16 <= XB_BYTES, "merge buffer");
       // every wait result is warp-uniform: the TMEM instructions that follow
@@ -349,6 +464,22 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
         const int tok_beg = sg.j0 * p.bs, tok_end = sg.j1 * p.bs;
         const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
         float m_ref = -INFINITY, l = 0.f;
+        float qk = p.qk_scale_log2;   // raw score -> log2 units (E4M3: times this row's 2^-e)
+        if constexpr (FP8) {
+          if (hh == 0) {
+            // This row's query as two E4M3 terms, once the previous segment's
+            // score MMAs (which read them) have completed.
+            good = seg == 0 || wait_all(&bars[gQEmpty], (seg - 1) & 1);
+            if (good) {
+              build_q_terms(p, sg, r, row_ok, smem + OFF_Q, m, qf_s);
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars[gQBuilt]);
+            }
+          }
+          good = good && wait_all(&bars[gQBuilt], seg & 1);
+          if (good) qk *= qf_s[m];
+        }
         for (int k = 0; k < ntile && good; ++k, ++t) {
           good = wait_all(&bars[gSFull0 + (t & 1)], (t >> 1) & 1);
           if (!good) break;
@@ -368,7 +499,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
 #pragma unroll
           for (int n = 0; n < TP; ++n)
             if (n < nv) mx = fmaxf(mx, __uint_as_float(sv[n]));
-          mx *= p.qk_scale_log2;
+          mx *= qk;
           const bool grow = mx > m_ref + RESCALE;
           if (__any_sync(0xffffffffu, grow)) {
             const float m_new = grow ? mx : m_ref;
@@ -397,32 +528,62 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           good = t < uint32_t(NP) || wait_all(&bars[gPVDone0 + t % NP], ((t - NP) / NP) & 1);
           if (!good) break;
           tc_fence_after();
-          uint32_t pv[TP / 2];
           float ls = 0.f;
+          if constexpr (FP8) {
+            // two E4M3 terms, four codes per TMEM column: this copy's part of
+            // the half's 32 tokens (8 columns per term), zeros elsewhere
+            uint32_t ph[TP / 4], pl[TP / 4];
 #pragma unroll
-          for (int j = 0; j < TP / 2; ++j) {
-            const float a0 = 2 * j < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j]), p.qk_scale_log2, -m_ref)) : 0.f;
-            const float a1 = 2 * j + 1 < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j + 1]), p.qk_scale_log2, -m_ref)) : 0.f;
-            ls += a0 + a1;
-            pv[j] = pack_bf16(a0, a1);
+            for (int j = 0; j < TP / 2; ++j) {
+              const float a0 = 2 * j < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j]), qk, -m_ref)) : 0.f;
+              const float a1 = 2 * j + 1 < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j + 1]), qk, -m_ref)) : 0.f;
+              ls += a0 + a1;
+              uint32_t h2, l2;
+              e4m3_two_terms_pair(a0, a1, h2, l2);
+              if (j & 1) {
+                ph[j >> 1] |= h2 << 16;
+                pl[j >> 1] |= l2 << 16;
+              } else {
+                ph[j >> 1] = h2;
+                pl[j >> 1] = l2;
+              }
+            }
+            uint32_t kh[8], kl[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              kh[i] = (i / (TP / 4) == cpy) ? ph[i % (TP / 4)] : 0u;
+              kl[i] = (i / (TP / 4) == cpy) ? pl[i % (TP / 4)] : 0u;
+            }
+            tmem_st8(tmem + lane_off + TM_P + 32 * (t % NP) + 8 * hh, kh);
+            tmem_st8(tmem + lane_off + TM_P + 32 * (t % NP) + 16 + 8 * hh, kl);
+          } else {
+            uint32_t pv[TP / 2];
+#pragma unroll
+            for (int j = 0; j < TP / 2; ++j) {
+              const float a0 = 2 * j < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j]), qk, -m_ref)) : 0.f;
+              const float a1 = 2 * j + 1 < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j + 1]), qk, -m_ref)) : 0.f;
+              ls += a0 + a1;
+              pv[j] = pack_bf16(a0, a1);
+            }
+            // this half's 32 tokens as 16 bf16 pairs: this copy's part, zeros
+            // elsewhere (the other copies' rows hold the other parts)
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = (i / (TP / 2) == cpy) ? pv[i % (TP / 2)] : 0u;
+            tmem_st16(tmem + lane_off + TM_P + 32 * (t % NP) + 16 * hh, pk);
           }
           l += ls;
-          // this half's 32 tokens as 16 bf16 pairs: this copy's part, zeros
-          // elsewhere (the other copies' rows hold the other parts)
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = (i / (TP / 2) == cpy) ? pv[i % (TP / 2)] : 0u;
-          tmem_st16(tmem + lane_off + TM_P + 32 * (t % NP) + 16 * hh, pk);
           tmem_st_wait();
           const int vt = len - (tok_beg + TT * k);   // cached rows of the tile that hold tokens
           if (vt < TT) {
             // Zero the V rows past the sequence's end (stale or never-written
             // slots of its last page); rows past the CTA's range came from
             // the out-of-range page and are zero already.
-            uint8_t* vb = smem + OFF_ST + (t % NSTAGE) * STAGE + 2 * HALF;
+            uint8_t* vb = smem + OFF_ST + (t % NSTAGE) * STAGE + V_OFF;
             const int v0 = max(vt, 0);
-            for (int idx = tid; idx < (TT - v0) * 16; idx += 256) {
-              const int row = v0 + (idx >> 4), piece = idx & 15;
+            constexpr int PIECES = FP8 ? 8 : 16;   // 16-byte pieces of a row (both bf16 halves)
+            for (int idx = tid; idx < (TT - v0) * PIECES; idx += 256) {
+              const int row = v0 + idx / PIECES, piece = idx % PIECES;
               *reinterpret_cast<uint4*>(vb + (piece >> 3) * HALF + row * 128 + (piece & 7) * 16) =
                   make_uint4(0, 0, 0, 0);
             }
@@ -553,8 +714,13 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
 #ifndef KV_GQA_TC_MIN_ROWS
 #define KV_GQA_TC_MIN_ROWS 33
 #endif
+#ifndef KV_GQA_TC_MIN_ROWS_FP8
+#define KV_GQA_TC_MIN_ROWS_FP8 17
+#endif
 bool gqa_tc_applies(int dtype, int rows, int d) {
-  return dtype == KVATTN_BF16 && d == gtc::D && rows >= KV_GQA_TC_MIN_ROWS && rows <= 128;
+  if (d != gtc::D || rows > 128) return false;
+  if (dtype == KVATTN_BF16) return rows >= KV_GQA_TC_MIN_ROWS;
+  return dtype == KVATTN_FP8_E4M3 && rows >= KV_GQA_TC_MIN_ROWS_FP8;
 }
 
 int gqa_tc_ctas() {
@@ -563,14 +729,21 @@ int gqa_tc_ctas() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   std::call_once(flags[dev], [dev] {
-    const void* ks[6] = {(const void*)gqa_tc_kernel<true, 1>, (const void*)gqa_tc_kernel<true, 2>,
-                         (const void*)gqa_tc_kernel<true, 4>, (const void*)gqa_tc_kernel<false, 1>,
-                         (const void*)gqa_tc_kernel<false, 2>, (const void*)gqa_tc_kernel<false, 4>};
+    using gtc::Lay;
+    const void* ks[6] = {(const void*)gqa_tc_kernel<true, 1, false>, (const void*)gqa_tc_kernel<true, 2, false>,
+                         (const void*)gqa_tc_kernel<true, 4, false>, (const void*)gqa_tc_kernel<false, 1, false>,
+                         (const void*)gqa_tc_kernel<false, 2, false>, (const void*)gqa_tc_kernel<false, 4, false>};
+    const void* k8[6] = {(const void*)gqa_tc_kernel<true, 1, true>, (const void*)gqa_tc_kernel<true, 2, true>,
+                         (const void*)gqa_tc_kernel<true, 4, true>, (const void*)gqa_tc_kernel<false, 1, true>,
+                         (const void*)gqa_tc_kernel<false, 2, true>, (const void*)gqa_tc_kernel<false, 4, true>};
     for (const void* k : ks)
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gtc::SMEM);
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<false>::SMEM);
+    for (const void* k : k8)
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<true>::SMEM);
+    // both forms hold one CTA per SM (shared memory and 448 threads)
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_tc_kernel<false, 1>, gtc::THREADS,
-                                                      gtc::SMEM) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gqa_tc_kernel<false, 1, false>,
+                                                      gtc::THREADS, Lay<false>::SMEM) != cudaSuccess)
       n = 0;
     const int sms = device_sm_count();
     cache[dev] = (n > 0 && sms > 0) ? n * sms : -1;
@@ -578,39 +751,49 @@ int gqa_tc_ctas() {
   return cache[dev];
 }
 
+template <bool FP8>
+static cudaError_t launch_tc(const GqaArgs& a, const GqaParams& prm, int G, const CUtensorMap& tmQ,
+                             const CUtensorMap& tmK, const CUtensorMap& tmV) {
+  using namespace gtc;
+  constexpr int SM = Lay<FP8>::SMEM;
+  const dim3 grid(G), block(THREADS);
+  // rows <= 32: four copies of the rows in the MMA's 128, <= 64: two, else one
+  if (prm.qlen > 1)
+    return prm.rows <= 32   ? launch_pdl(gqa_tc_kernel<true, 4, FP8>, grid, block, SM, a.stream, tmQ, tmK, tmV, prm)
+           : prm.rows <= 64 ? launch_pdl(gqa_tc_kernel<true, 2, FP8>, grid, block, SM, a.stream, tmQ, tmK, tmV, prm)
+                            : launch_pdl(gqa_tc_kernel<true, 1, FP8>, grid, block, SM, a.stream, tmQ, tmK, tmV, prm);
+  return prm.rows <= 32   ? launch_pdl(gqa_tc_kernel<false, 4, FP8>, grid, block, SM, a.stream, tmQ, tmK, tmV, prm)
+         : prm.rows <= 64 ? launch_pdl(gqa_tc_kernel<false, 2, FP8>, grid, block, SM, a.stream, tmQ, tmK, tmV, prm)
+                          : launch_pdl(gqa_tc_kernel<false, 1, FP8>, grid, block, SM, a.stream, tmQ, tmK, tmV, prm);
+}
+
 kvattn_status launch_gqa_tc(const GqaArgs& a, const GqaParams& prm, int G) {
   using namespace gtc;
   if (gqa_tc_ctas() <= 0) return KVATTN_ERR_CUDA;   // also sets the shared-memory attribute
   const kvattn_cache* cc = a.cache;
+  const bool fp8 = cc->dtype == KVATTN_FP8_E4M3;
   alignas(64) CUtensorMap tmQ, tmK, tmV;
-  // q [B][q_len][h][d] as (d, h, q_len, B); a box is one unit's rows
+  // q [B][q_len][h][d] as (d, h, q_len, B); a box is one unit's rows (the
+  // E4M3 form builds its query terms without it)
   const uint64_t qdims[4] = {uint64_t(D), uint64_t(prm.h), uint64_t(prm.qlen), uint64_t(prm.B)};
   const uint64_t qstr[3] = {uint64_t(D) * 2, uint64_t(prm.h) * D * 2,
                             uint64_t(prm.qlen) * prm.h * D * 2};
   const uint32_t qbox[4] = {64u, uint32_t(prm.g), uint32_t(prm.qlen), 1u};
+  // K and V pools as (d, block_size, blocks x KV heads); boxes of 16 tokens x
+  // 128 bytes (64 bf16 dims or 128 E4M3 codes)
+  const uint64_t eb = fp8 ? 1 : 2;
   const uint64_t dims[3] = {uint64_t(D), uint64_t(cc->block_size),
                             uint64_t(cc->num_blocks) * uint64_t(cc->h_kv)};
-  const uint64_t strides[2] = {uint64_t(D) * 2, uint64_t(D) * 2 * uint64_t(cc->block_size)};
-  const uint32_t box[3] = {64u, 16u, 1u};
+  const uint64_t strides[2] = {uint64_t(D) * eb, uint64_t(D) * eb * uint64_t(cc->block_size)};
+  const uint32_t box[3] = {uint32_t(128 / eb), 16u, 1u};
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!encode_tensor_map_4d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, qdims, qstr, qbox,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map_3d(&tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->k, dims, strides, box,
-                            CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cc->v, dims, strides, box,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tensor_map_3d(&tmK, dt, cc->k, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_3d(&tmV, dt, cc->v, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return KVATTN_ERR_CUDA;
-  // rows <= 32: four copies of the rows in the MMA's 128, <= 64: two, else one
-  cudaError_t e;
-  const dim3 grid(G), block(THREADS);
-  if (prm.qlen > 1) {
-    e = prm.rows <= 32   ? launch_pdl(gqa_tc_kernel<true, 4>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
-        : prm.rows <= 64 ? launch_pdl(gqa_tc_kernel<true, 2>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
-                         : launch_pdl(gqa_tc_kernel<true, 1>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm);
-  } else {
-    e = prm.rows <= 32   ? launch_pdl(gqa_tc_kernel<false, 4>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
-        : prm.rows <= 64 ? launch_pdl(gqa_tc_kernel<false, 2>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm)
-                         : launch_pdl(gqa_tc_kernel<false, 1>, grid, block, SMEM, a.stream, tmQ, tmK, tmV, prm);
-  }
+  const cudaError_t e = fp8 ? launch_tc<true>(a, prm, G, tmQ, tmK, tmV)
+                            : launch_tc<false>(a, prm, G, tmQ, tmK, tmV);
   return e == cudaSuccess ? KVATTN_OK : KVATTN_ERR_CUDA;
 }
 

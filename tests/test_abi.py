@@ -99,8 +99,8 @@ def _gqa_cache(**kw):
     (dict(maxb=0), {}, kv.KVATTN_ERR_INVALID_ARG),
     (dict(d=96), dict(d_h=96), kv.KVATTN_ERR_UNSUPPORTED),              # head dim not built
     (dict(h=130, h_kv=1), dict(h_kv=1), kv.KVATTN_ERR_UNSUPPORTED),     # g > 128
-    (dict(h=80, h_kv=1), dict(h_kv=1, dtype=kv.KVATTN_FP8_E4M3),
-     kv.KVATTN_ERR_UNSUPPORTED),                                        # FP8: g > 64
+    (dict(h=130, h_kv=1), dict(h_kv=1, dtype=kv.KVATTN_FP8_E4M3),
+     kv.KVATTN_ERR_UNSUPPORTED),                                        # FP8: g > 128
     (dict(h=80, h_kv=1, d=64), dict(h_kv=1, d_h=64), kv.KVATTN_ERR_UNSUPPORTED),  # d 64: g > 64
     ({}, dict(block_size=8), kv.KVATTN_ERR_UNSUPPORTED),
     ({}, dict(block_size=40), kv.KVATTN_ERR_UNSUPPORTED),             # not whole 16-token chunks

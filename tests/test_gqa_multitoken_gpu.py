@@ -105,5 +105,5 @@ def test_rejects_too_many_rows():
     wl8 = inputs.make_workload("llama3_70b_fp8", lens=[100])
     g8 = GpuWorkload(wl8)
     with pytest.raises(kv.KvattnError) as e:
-        g8.decode_multi(inputs.multi_token_queries(wl8, 9))   # FP8: 72 rows > 64
+        g8.decode_multi(inputs.multi_token_queries(wl8, 17))   # FP8: 136 rows > 128
     assert e.value.status == kv.KVATTN_ERR_UNSUPPORTED

@@ -1,5 +1,5 @@
-"""The tcgen05 form of the GQA decode (units of 33..128 rows, bf16 cache, d_h
-128) on the GPU vs the float64 oracle.
+"""The tcgen05 form of the GQA decode (d_h 128; bf16 caches with 33..128 rows
+per unit, FP8-E4M3 caches with 17..128) on the GPU vs the float64 oracle.
 
 A unit's rows are the q_len new tokens x g query heads of one KV head
 (single-token decode: the g heads).  With more than 32 of them the library
@@ -23,7 +23,7 @@ def _multi(oracle, wl, q_len, num_ctas=0, seqs=None, seed=0, qm=None):
     g = GpuWorkload(wl)
     out, lse = g.decode_multi(qm, num_ctas=num_ctas)
     ref_o, ref_l = oracle_multi(oracle, wl, qm, seqs)
-    assert_parity(out, lse, ref_o, ref_l)
+    assert_parity(out, lse, ref_o, ref_l, fp8=wl.kv_dtype == "fp8")
     assert g.err_bits() == 0
     return g, qm, out, lse
 
@@ -108,4 +108,50 @@ def test_full_size_sampled(oracle):
     # the benchmark's multi-token launch: Llama-3-70B, 32 x 8192, 8 new tokens
     # (64 rows per KV head), default CTAs; three sampled sequences
     wl = inputs.make_workload("llama3_70b")
+    _multi(oracle, wl, 8, seqs=[0, 13, 31])
+
+
+# ---- FP8-E4M3 cache: kind::f8f6f4 MMAs, query and probabilities as two E4M3
+# terms each, against the oracle's decode of the stored codes
+
+
+@pytest.mark.parametrize("q_len", [3, 4, 8, 12, 16])
+def test_fp8_row_counts(oracle, q_len):
+    # g = 8: 24, 32, 64, 96 and 128 rows (four, four, two, one, one copies)
+    _multi(oracle, inputs.make_workload("llama3_70b_fp8", lens=[2000, 129, 7, 64, 0]), q_len)
+
+
+@pytest.mark.parametrize("num_ctas", [1, 7, 300])
+def test_fp8_forced_splits(oracle, num_ctas):
+    _multi(oracle, inputs.make_workload("llama3_70b_fp8", lens=[3000, 700, 65, 1]), 8,
+           num_ctas=num_ctas)
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_fp8_block_sizes(oracle, bs):
+    _multi(oracle, inputs.make_workload("llama3_70b_fp8", lens=[1000, 300, 77], block_size=bs), 8,
+           num_ctas=5)
+
+
+def test_fp8_large_logits(oracle):
+    wl = inputs.make_workload("llama3_70b_fp8", lens=[900, 2000])
+    qm = inputs.multi_token_queries(wl, 8)
+    qm = inputs.bf16_bits(inputs.bf16_to_f32(qm) * np.float32(8.0))
+    _multi(oracle, wl, 8, num_ctas=9, qm=qm)
+
+
+def test_fp8_single_token_mqa(oracle):
+    # long_mqa's FP8 twin read by 32 query heads per KV head, single token
+    wl = inputs.make_workload("long_mqa", lens=[1500, 30000, 1, 64])
+    wl.kv_dtype = "fp8"
+    wl.k_scale = inputs.fp8_scale(wl.k)
+    wl.v_scale = inputs.fp8_scale(wl.v)
+    g = GpuWorkload(wl)
+    out, lse = g.decode()
+    ref_o, ref_l = oracle_all(oracle, wl)
+    assert_parity(out, lse, ref_o, ref_l, fp8=True)
+
+
+def test_fp8_full_size_sampled(oracle):
+    wl = inputs.make_workload("llama3_70b_fp8")
     _multi(oracle, wl, 8, seqs=[0, 13, 31])
