@@ -31,7 +31,9 @@
 //              each producer warp issues one chunk's four boxes per tile (one
 //              warp issuing all 16 boxes of a tile serialises them at ~120
 //              cycles apiece, ~1 us per tile: the HBM needs one per ~0.7 us)
-//   warp 1     TMEM owner and S issuer: S(t) into one of two S slots
+//   warps 1, 14  TMEM owner (1) and S issuers: S(t) into S slot t % 2, even
+//              tiles from warp 1, odd ones from warp 14 (one thread issuing
+//              every tile's MMAs at ~110 cycles apiece set the pace)
 //   warp 9     P.V issuer (one thread issuing both MMA chains, ~100 cycles
 //              per tcgen05.mma, set a period of ~1 us per tile)
 //   warps 2-5, 10-13  softmax and epilogue, two threads per row
@@ -57,7 +59,7 @@ constexpr int QHALF = 128 * 128;        // [128 rows x 128 B]: Q's dims 0-63 / 6
 constexpr int OFF_Q = 0;
 constexpr int OFF_ST = 2 * QHALF;
 constexpr int XB_BYTES = 2 * 3 * 32 * 32 * 4;      // [hh][copy - 1][row][32 columns], 4 copies
-constexpr int NBARS = 32;
+constexpr int NBARS = 40;
 // Per cache format.  bf16: a stage is K dims 0-63, K dims 64-127, V dims 0-63,
 // V dims 64-127 (32 KB); E4M3: K codes, V codes (16 KB), so twice the stages.
 template <bool FP8>
@@ -73,8 +75,9 @@ struct Lay {
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(NSTAGE <= NSTAGE_MAX, "barrier slots");
 };
-constexpr int THREADS = 448;
+constexpr int THREADS = 480;
 constexpr int PV_WARP = 9;
+constexpr int S2_WARP = 14;             // the second S issuer (odd tiles)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;            // two S slots of 64 columns
 constexpr uint32_t TM_P = 128;          // two P slots of 32 columns (bf16 pairs)
@@ -94,7 +97,8 @@ enum : int {
   gEmpty0 = gFull0 + gtc::NSTAGE_MAX,       // NSTAGE: P.V finished with the stage
   gAbort = gEmpty0 + gtc::NSTAGE_MAX,       // an int flag in this slot
   gDrain2 = gAbort + 1,                     // the P.V issuer's last MMAs completed
-  gNumBars = gDrain2 + 1,
+  gDrain3 = gDrain2 + 1,                    // the second S issuer's last MMAs completed
+  gNumBars = gDrain3 + 1,
   gQBuilt = gQFull                          // E4M3: the softmax warps built Q's terms (no TMA)
 };
 static_assert(gNumBars <= gtc::NBARS, "barrier slots");
@@ -108,12 +112,14 @@ KV_DEVI void e4m3_two_terms_pair(float x0, float x1, uint32_t& hi, uint32_t& lo)
   lo = e4m3x2(x0 - h.x, x1 - h.y);
 }
 
-// E4M3 cache: MMA row m (copy of unit row r) of the query as two E4M3 terms,
+// E4M3 cache: MMA row m (copy of unit row r) of the query as two E4M3 terms
+// (dims 64 hh .. 64 hh + 63 from this thread; both threads of a row find the
+// same scale),
 // x 2^e with e chosen so that the row's largest magnitude lands in [128, 256):
 // hi codes at q + m * 128, lo codes at q + QHALF + m * 128, in the 128-byte
 // swizzled K-major layout; 2^-e to qf[m].  Rows past the unit's are zero.
 KV_DEVI void build_q_terms(const GqaParams& p, const Seg& sg, int r, bool row_ok, uint8_t* q,
-                           int m, float* qf) {
+                           int m, int hh, float* qf) {
   int64_t qi = 0;
   if (row_ok) {
     if (p.qlen > 1) {
@@ -142,10 +148,11 @@ KV_DEVI void build_q_terms(const GqaParams& p, const Seg& sg, int r, bool row_ok
   }
   const int e = mx > 0.f ? min(max(7 - (int((__float_as_uint(mx) >> 23) & 255) - 127), -120), 120) : 0;
   const float sc = __uint_as_float(uint32_t(127 + e) << 23);
-  qf[m] = __uint_as_float(uint32_t(127 - e) << 23);
-  // pass 2: 16 dims (one 16-byte piece of codes per term) at a time
+  if (hh == 0) qf[m] = __uint_as_float(uint32_t(127 - e) << 23);
+  // pass 2: this thread's 64 dims, 16 (one 16-byte piece of codes per term)
+  // at a time
 #pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 4 * hh; c < 4 * hh + 4; ++c) {
     const uint4 x0 = row_ok ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
     const uint4 x1 = row_ok ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
     const uint32_t wv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -193,8 +200,9 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
   const int c = blockIdx.x;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[gQFull], FP8 ? 4 : 1);   // TMA (bf16), or the four builder warps (E4M3)
-    mbar_init(&bars[gQEmpty], 1);
+    mbar_init(&bars[gQFull], FP8 ? 8 : 1);   // TMA (bf16), or the eight builder warps (E4M3)
+    mbar_init(&bars[gQEmpty], 2);            // both S issuers
+
     mbar_init(&bars[gOFree], 8);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[gSFull0 + i], 1);
@@ -206,6 +214,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
     }
     mbar_init(&bars[gDrain], 1);
     mbar_init(&bars[gDrain2], 1);
+    mbar_init(&bars[gDrain3], 1);
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&bars[gFull0 + i], 1);
       mbar_init(&bars[gEmpty0 + i], 1);
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
         for (uint32_t k = t > uint32_t(NSTAGE) ? t - NSTAGE : 0u; k < t; ++k)
           mbar_wait(&bars[gFull0 + k % NSTAGE], (k / NSTAGE) & 1, KV_DRAIN_WAIT_NS);
       }
-    } else if (warp == 1 || warp == PV_WARP) {
+    } else if (warp == 1 || warp == PV_WARP || warp == S2_WARP) {
       // ---------------------------------------------- MMA issuers: S, and P.V
       if (lane == 0) {
         const uint32_t st0 = smem_u32(smem + OFF_ST);
@@ -328,7 +337,8 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
         Seg sg;
         uint32_t t = 0, seg = 0;
         bool ok = true;
-        if (warp == 1) {
+        if (warp != PV_WARP) {
+          const uint32_t sp = warp == 1 ? 0u : 1u;   // the tiles t with t % 2 == sp
           const uint32_t id_s = FP8 ? idesc_e4m3(128, TT, false) : idesc_bf16(128, TT, false);
           const uint64_t qa0 = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
           while (ok && w.next(sg)) {
@@ -338,6 +348,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
               break;
             }
             for (int k = 0; k < ntile && ok; ++k, ++t) {
+              if ((t & 1) != sp) continue;
               // the tile's K and V, and its S slot: the softmax has read S(t - 2)
               if ((t >= 2 && !mbar_wait(&bars[gSRead0 + (t & 1)], ((t - 2) >> 1) & 1)) ||
                   !mbar_wait(&bars[gFull0 + t % NSTAGE], (t / NSTAGE) & 1)) {
@@ -365,9 +376,11 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
                 }
               }
               umma_commit(&bars[gSFull0 + (t & 1)]);
-              if (k == ntile - 1) umma_commit(&bars[gQEmpty]);   // every S of the segment issued
               if (*abort_flag) ok = false;
             }
+            // every S of this issuer in the segment is issued (the barrier
+            // completes when both issuers' score MMAs have)
+            if (ok) umma_commit(&bars[gQEmpty]);
             ++seg;
           }
         } else {
@@ -414,7 +427,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           *abort_flag = 1;
         }
         // no MMA of this thread may still write TMEM when it is released
-        uint64_t* drain = &bars[warp == 1 ? gDrain : gDrain2];
+        uint64_t* drain = &bars[warp == 1 ? gDrain : warp == PV_WARP ? gDrain2 : gDrain3];
         umma_commit(drain);
         mbar_wait(drain, 0, KV_DRAIN_WAIT_NS);
       }
@@ -466,16 +479,15 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
         float m_ref = -INFINITY, l = 0.f;
         float qk = p.qk_scale_log2;   // raw score -> log2 units (E4M3: times this row's 2^-e)
         if constexpr (FP8) {
-          if (hh == 0) {
-            // This row's query as two E4M3 terms, once the previous segment's
-            // score MMAs (which read them) have completed.
-            good = seg == 0 || wait_all(&bars[gQEmpty], (seg - 1) & 1);
-            if (good) {
-              build_q_terms(p, sg, r, row_ok, smem + OFF_Q, m, qf_s);
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&bars[gQBuilt]);
-            }
+          // This row's query as two E4M3 terms (this thread: the half hh of
+          // its dims), once the previous segment's score MMAs (which read
+          // them) have completed.
+          good = seg == 0 || wait_all(&bars[gQEmpty], (seg - 1) & 1);
+          if (good) {
+            build_q_terms(p, sg, r, row_ok, smem + OFF_Q, m, hh, qf_s);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[gQBuilt]);
           }
           good = good && wait_all(&bars[gQBuilt], seg & 1);
           if (good) qk *= qf_s[m];
