@@ -447,6 +447,8 @@ def run_reference(args, wl, rank):
 
 ALL_CONFIGS = ["tiny", "llama3_8b", "llama3_70b", "llama3_70b_fp8", "deepseek_v3_mla",
                "deepseek_v3_mla_fp8", "long_gqa8", "long_mqa"]
+# multi-token decode (new tokens verified per pass), timed the same way
+MT_CONFIGS = [("llama3_70b", 8), ("llama3_70b_fp8", 8)]
 FLUSH_BYTES = 512 * 2**20   # 4x L2
 
 
@@ -544,12 +546,64 @@ def time_all_configs(args, sampler, headline, dev):
         if g is not headline:
             del g
         torch.cuda.empty_cache()
+    for name, q_len in MT_CONFIGS:
+        res[f"{name}_q{q_len}"] = time_multi_token(name, q_len, args, sampler, dev, stream, peak,
+                                                   flush, n)
+        torch.cuda.empty_cache()
     res["mla_prefill"] = time_prefill(args, sampler, dev, stream, flushed_by=(flush, n))
     res["how"] = ("decode call replayed from a CUDA graph %d times; us_decode_call = (flush + "
                   "decode replays - flush replays) / %d with an L2 flush (sum over a %d MB "
                   "buffer) before every decode; gbs, frac and pct use it" % (n, n,
                                                                              FLUSH_BYTES >> 20))
     return res
+
+
+def time_multi_token(name, q_len, args, sampler, dev, stream, peak, flush, n):
+    """The multi-token decode call of a GQA workload (q_len new tokens per
+    sequence, the last q_len cached ones), back to back and after an L2 flush,
+    as for the single-token entries."""
+    import torch
+
+    import kv_cache_decode_paged_gb300 as kv
+    from kv_cache_decode_paged_gb300 import inputs
+    from kv_cache_decode_paged_gb300.device import GpuWorkload, dev_bits
+
+    wl = inputs.make_workload(name, seed=args.seed)
+    g = GpuWorkload(wl, poison=False, device=dev)
+    qm = dev_bits(inputs.multi_token_queries(wl, q_len, args.seed), dev)
+    ws = kv.workspace_for(kv.KVATTN_GQA, wl.B, wl.h * q_len, wl.h_kv, wl.d, 0, dev)
+    out = torch.empty((wl.B, q_len, wl.h, wl.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((wl.B, q_len, wl.h), dtype=torch.float32, device=dev)
+    desc = g.cache.descriptor()
+
+    def decode():
+        kv.kvattn_decode_gqa_multi(qm, desc, g.bt, g.seq_lens, q_len, wl.h, wl.h_kv, wl.d,
+                                   wl.scale, out, lse, ws, err=g.err)
+
+    def flushed():
+        flush()
+        decode()
+
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    warm = replay_us(torch, decode, n, stream)
+    both = replay_us(torch, flushed, n, stream)
+    alone = replay_us(torch, flush, n, stream)
+    t1 = time.monotonic()
+    cold = max(both - alone, 1e-3)
+    kvb = wl.kv_bytes()
+    rows = q_len * wl.h // wl.h_kv
+    fp8 = wl.kv_dtype == "fp8"
+    return {"kernel": "GQA multi-token decode" + (", FP8-E4M3 cache" if fp8 else "") +
+                      (" (tcgen05)" if rows > (16 if fp8 else 32) else " (mma.sync)"),
+            "batch": wl.B, "h": wl.h, "h_kv": wl.h_kv, "q_len": q_len, "rows_per_unit": rows,
+            "kv_bytes": kvb, "us_decode_call": cold, "us_decode_call_back_to_back": warm,
+            "us_l2_flush": alone, "gbs": kvb / cold / 1e3,
+            "frac_of_measured_hbm": kvb / cold / 1e3 / peak,
+            "pct_of_8tbs": 100.0 * kvb / cold / 1e3 / NOMINAL_HBM_GBS,
+            "gbs_back_to_back": kvb / warm / 1e3,
+            "flop_per_byte": 4.0 * wl.d * rows / (2.0 * wl.d * (1 if fp8 else 2)),
+            "clocks": sampler.summary(t0, t1), "device_err_bits": g.err_bits()}
 
 
 def prefill_flops(S, q_len, h, B):
