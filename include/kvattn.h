@@ -176,7 +176,8 @@ KVATTN_API int kvattn_default_num_ctas(int kind, int dtype, int h, int h_kv, int
  *   block_table: device, [batch][max_blocks_per_seq] int32.
  *   seq_lens:    device, [batch] int32, tokens cached per sequence (the
  *                current token included).
- *   h % h_kv == 0, g = h / h_kv <= 64; d_h in {64, 128} (FP8: 128);
+ *   h % h_kv == 0, g = h / h_kv <= 128 for d_h 128 (<= 64 for d_h 64);
+ *   d_h in {64, 128} (FP8: 128);
  *   block_size a multiple of 16, at most 256 (vLLM's 16 up to one block of
  *   a short sequence).
  *   scale:       softmax scale (1/sqrt(d_h) in the pages' formula).
@@ -187,8 +188,11 @@ KVATTN_API int kvattn_default_num_ctas(int kind, int dtype, int h, int h_kv, int
  *   num_ctas:    0 = default; otherwise the number of CTAs the page range is
  *                split over (tests use this to force split counts).
  * Launches three kernels on `stream`: the split planner, the decode kernel
- * and the split-KV combine.  Results depend on num_ctas only through rounding
- * (the softmax weights enter P.V in bf16, or f16 for FP8 caches). */
+ * and the split-KV combine.  Units of more than 32 rows (g, or q_len * g for
+ * kvattn_decode_gqa_multi) with bf16, and of more than 16 with FP8, run on
+ * the tensor cores' tcgen05 MMAs, the others on warp-level MMAs.  Results
+ * depend on num_ctas only through rounding (the softmax weights enter P.V in
+ * bf16, or as f16 or two E4M3 terms for FP8 caches). */
 KVATTN_API kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* cache,
                                 const int32_t* block_table, const int32_t* seq_lens, int batch,
                                 int max_blocks_per_seq, int h, int h_kv, int d_h, float scale,
@@ -207,8 +211,8 @@ KVATTN_API kvattn_status kvattn_decode_gqa(const void* q, const kvattn_cache* ca
  * KV head.
  *   q:    device, [batch][q_len][h][d_h] bf16.
  *   out:  device, [batch][q_len][h][d_h] float32;  lse: [batch][q_len][h].
- *   q_len >= 1 (KVATTN_ERR_INVALID_ARG otherwise), q_len * g <= 64
- *   (KVATTN_ERR_UNSUPPORTED otherwise).
+ *   q_len >= 1 (KVATTN_ERR_INVALID_ARG otherwise), q_len * g <= 128 for
+ *   d_h 128, <= 64 for d_h 64 (KVATTN_ERR_UNSUPPORTED otherwise).
  *   workspace: >= kvattn_decode_workspace_bytes(KVATTN_GQA, batch, h * q_len,
  *   h_kv, d_h, num_ctas) bytes.
  * Other arguments, and the three launches, as for kvattn_decode_gqa, which is
