@@ -11,29 +11,32 @@
 // m-tile of a chunk through its own warps, and its fixed-latency MMA chains
 // cap it at 190-250 TFLOP/s whatever the bytes.  Here the unit's rows are the
 // M dimension of tcgen05 MMAs (M = 128; rows past q_len * g are padding that
-// no thread writes out):
-//   S = Q K^T   M = 128 rows, N = 64 tokens, K = 128 dims: 8 MMAs per tile
-//   O += P V    M = 128 rows, N = 128 dims, K = 64 tokens: 4 MMAs, P from TMEM
+// no thread writes out), over tiles of TT tokens (64 for bf16 caches, 128 for
+// E4M3):
+//   S = Q K^T   M = 128 rows, N = TT tokens, K = 128 dims
+//   O += P V    M = 128 rows, N = 128 dims, K = TT tokens, P from TMEM
 // with S, P and O in tensor memory.  Thread r of the four softmax warps owns
 // TMEM lane r, i.e. row r, so the online softmax (lazy rescale of O when a
 // row's max grows by more than 2^8) needs no exchange between threads.
 //
-// A tile is 64 tokens = four 16-token chunks; a chunk of K (or V) arrives as
+// A tile is TT / 16 chunks of 16 tokens; a chunk of bf16 K (or V) arrives as
 // two TMA boxes [16 tokens x 64 dims] (128-byte swizzle) at row 16c of the
 // tile's two 64-dim halves, which makes each half one swizzled [64 x 64]
-// operand.  Chunks past the CTA's range are loaded from an out-of-range page
+// operand (E4M3: one box [16 tokens x 128 codes] into a [128 x 128] one).  Chunks past the CTA's range are loaded from an out-of-range page
 // (zero fill); cached rows past the sequence's length are zeroed in shared
 // memory by the softmax warps before P.V reads them (P is 0 there, but 0 * NaN
 // would be NaN).  The planner, the partial slots and the combine are those of
 // the mma.sync kernel.
 //   warps 0, 6-8  TMA producers: warp 0 loads the unit's Q per segment (a 4-D
 //              box [q_len][g][64 dims], twice) and arms each tile's barrier;
-//              each producer warp issues one chunk's four boxes per tile (one
-//              warp issuing all 16 boxes of a tile serialises them at ~120
-//              cycles apiece, ~1 us per tile: the HBM needs one per ~0.7 us)
-//   warps 1, 14  TMEM owner (1) and S issuers: S(t) into S slot t % 2, even
-//              tiles from warp 1, odd ones from warp 14 (one thread issuing
-//              every tile's MMAs at ~110 cycles apiece set the pace)
+//              producer warp pc issues the boxes of chunks pc, pc + 4, ... of
+//              each tile (one warp issuing all 16 boxes of a bf16 tile
+//              serialises them at ~120 cycles apiece, ~1 us per tile: the HBM
+//              needs one per ~0.7 us)
+//   warps 1, 14  TMEM owner (1) and S issuers: even tiles from warp 1, odd
+//              ones from warp 14 (one thread issuing every tile's MMAs at
+//              ~110 cycles apiece set the pace), into S slot t % 2 (bf16) or
+//              the one S slot (E4M3)
 //   warp 9     P.V issuer (one thread issuing both MMA chains, ~100 cycles
 //              per tcgen05.mma, set a period of ~1 us per tile)
 //   warps 2-5, 10-13  softmax and epilogue, two threads per row
@@ -51,8 +54,6 @@ namespace kv {
 
 namespace gtc {
 constexpr int D = 128;
-constexpr int TT = 64;                  // tokens per tile
-constexpr int HALF = TT * 128;          // [64 tokens x 128 B]: 64 bf16 dims, or 128 E4M3 codes
 constexpr int NSTAGE_MAX = 8;
 constexpr int QHALF = 128 * 128;        // [128 rows x 128 B]: Q's dims 0-63 / 64-127 (bf16), or
                                         // its hi / lo E4M3 term (128 codes)
@@ -60,13 +61,20 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_ST = 2 * QHALF;
 constexpr int XB_BYTES = 2 * 3 * 32 * 32 * 4;      // [hh][copy - 1][row][32 columns], 4 copies
 constexpr int NBARS = 40;
-// Per cache format.  bf16: a stage is K dims 0-63, K dims 64-127, V dims 0-63,
-// V dims 64-127 (32 KB); E4M3: K codes, V codes (16 KB), so twice the stages.
+// Per cache format.  bf16: a tile is 64 tokens and a stage holds K dims 0-63,
+// K dims 64-127, V dims 0-63, V dims 64-127 (32 KB).  E4M3: a tile is 128
+// tokens (a 64-token tile of codes is 16 KB, and the softmax's fixed cost per
+// tile, not the bytes, then set the pace) and a stage holds K codes, V codes
+// (32 KB).
 template <bool FP8>
 struct Lay {
+  static constexpr int TT = FP8 ? 128 : 64;                   // tokens per tile
+  static constexpr int HALF = TT * 128;                       // [TT tokens x 128 B]
   static constexpr int STAGE = FP8 ? 2 * HALF : 4 * HALF;
-  static constexpr int NSTAGE = FP8 ? 8 : 5;
+  static constexpr int NSTAGE = 5;
   static constexpr int V_OFF = FP8 ? HALF : 2 * HALF;        // V within a stage
+  static constexpr int NS = FP8 ? 1 : 2;                      // S slots of TT columns
+  static constexpr int PCOLS = TT / 2;                        // columns of a P slot
   static constexpr int OFF_ML = OFF_ST + NSTAGE * STAGE;      // the epilogue's row max / sum exchange
   static constexpr int OFF_QF = OFF_ML + 4 * 128 * 4;         // E4M3: each row's 2^-e
   static constexpr int OFF_XB = OFF_QF + 128 * 4;             // the epilogue's merge of the row copies
@@ -79,17 +87,20 @@ constexpr int THREADS = 480;
 constexpr int PV_WARP = 9;
 constexpr int S2_WARP = 14;             // the second S issuer (odd tiles)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;            // two S slots of 64 columns
-constexpr uint32_t TM_P = 128;          // two P slots of 32 columns (bf16 pairs)
+constexpr uint32_t TM_S = 0;            // S slots: two of 64 columns (bf16), one of 128 (E4M3)
+constexpr uint32_t TM_P = 128;          // two P slots of TT / 2 columns (bf16 pairs, E4M3 quads
+                                        // of the two terms)
 constexpr int NP = 2;                   // P slots: the softmax of tile t waits for P.V(t - 2)
-constexpr uint32_t TM_O = 256;          // O of tokens 0-31 of each tile, then of tokens 32-63
+constexpr uint32_t TM_O = 256;          // O of each tile's first half of tokens, then of its second
 constexpr float RESCALE = 8.f;          // log2 units
+static_assert(Lay<false>::NS * Lay<false>::TT <= 128 && Lay<true>::NS * Lay<true>::TT <= 128, "S");
+static_assert(NP * Lay<false>::PCOLS <= 128 && NP * Lay<true>::PCOLS <= 128, "P");
 }  // namespace gtc
 
 enum : int {
   gQFull = 0, gQEmpty = 1, gOFree = 2,
-  gSFull0 = 3,    // 2
-  gSRead0 = 5,    // 2: the softmax warps have read S slot t % 2
+  gSFull0 = 3,    // 2: S(t) is in its slot, by the parity of t
+  gSRead0 = 5,    // 2: the softmax warps have read S(t), by the parity of t
   gPFull0 = 7,    // NP: P(t) is in P slot t % NP (and the tile's tail rows zeroed)
   gPVDone0 = 10,  // NP: P.V(t) has completed (P slot t % NP free)
   gDrain = 13,
@@ -188,7 +199,9 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
                   const __grid_constant__ CUtensorMap tmV, const GqaParams p) {
   using namespace gtc;
   using L = Lay<FP8>;
-  constexpr int STAGE = L::STAGE, NSTAGE = L::NSTAGE, V_OFF = L::V_OFF;
+  constexpr int TT = L::TT, HALF = L::HALF, STAGE = L::STAGE, NSTAGE = L::NSTAGE, V_OFF = L::V_OFF;
+  constexpr int NS = L::NS, PCOLS = L::PCOLS;
+  constexpr int CPT = TT / 16;   // 16-token chunks per tile
   constexpr int OFF_ML = L::OFF_ML, OFF_QF = L::OFF_QF, OFF_XB = L::OFF_XB, OFF_BAR = L::OFF_BAR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -281,10 +294,10 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
             else
               page = blk * p.hkv + sg.kvh;
           }
-          // tiles of four chunks; a tile never straddles two groups of 32 pages
+          // tiles of CPT chunks; a tile never straddles two groups of 32 pages
           const int c0 = (pb - sg.j0) * cpp;
           const int c1 = min(pb + 32 - sg.j0, sg.j1 - sg.j0) * cpp;
-          for (int cc = c0; cc < c1 && ok; cc += 4) {
+          for (int cc = c0; cc < c1 && ok; cc += CPT) {
             const int s = int(t % NSTAGE);
             int lok = 1;
             if (lane == 0) {
@@ -297,21 +310,24 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
               ok = false;
               break;
             }
-            const int ci = cc + pc;                                    // this warp's chunk
-            const int src = min(max(ci / cpp - (pb - sg.j0), 0), 31);  // lane holding its page
-            const int pg_l = __shfl_sync(0xffffffffu, page, src);
-            if (lane == 0) {
-              const int pg = ci < nch ? pg_l : oob_page;
-              const int sub = ci % cpp;
-              uint8_t* dst = smem + OFF_ST + s * STAGE + pc * (16 * 128);
-              if constexpr (FP8) {   // one box of 128 codes per row for K and for V
-                tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
-                tma_load_3d(dst + V_OFF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
-              } else {
-                tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
-                tma_load_3d(dst + HALF, &tmK, 64, sub * 16, pg, &bars[gFull0 + s], pol);
-                tma_load_3d(dst + V_OFF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
-                tma_load_3d(dst + V_OFF + HALF, &tmV, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+#pragma unroll
+            for (int qc = 0; qc < CPT / 4; ++qc) {
+              const int ci = cc + pc + 4 * qc;                           // this warp's chunk
+              const int src = min(max(ci / cpp - (pb - sg.j0), 0), 31);  // lane holding its page
+              const int pg_l = __shfl_sync(0xffffffffu, page, src);
+              if (lane == 0) {
+                const int pg = ci < nch ? pg_l : oob_page;
+                const int sub = ci % cpp;
+                uint8_t* dst = smem + OFF_ST + s * STAGE + (pc + 4 * qc) * (16 * 128);
+                if constexpr (FP8) {   // one box of 128 codes per row for K and for V
+                  tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+                  tma_load_3d(dst + V_OFF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+                } else {
+                  tma_load_3d(dst, &tmK, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+                  tma_load_3d(dst + HALF, &tmK, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+                  tma_load_3d(dst + V_OFF, &tmV, 0, sub * 16, pg, &bars[gFull0 + s], pol);
+                  tma_load_3d(dst + V_OFF + HALF, &tmV, 64, sub * 16, pg, &bars[gFull0 + s], pol);
+                }
               }
             }
             ++t;   // issued: the exit drain waits for it
@@ -342,28 +358,34 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           const uint32_t id_s = FP8 ? idesc_e4m3(128, TT, false) : idesc_bf16(128, TT, false);
           const uint64_t qa0 = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
           while (ok && w.next(sg)) {
-            const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
+            const int ntile = ((sg.j1 - sg.j0) * cpp + CPT - 1) / CPT;
             if (!mbar_wait(&bars[gQFull], seg & 1)) {
               ok = false;
               break;
             }
             for (int k = 0; k < ntile && ok; ++k, ++t) {
               if ((t & 1) != sp) continue;
-              // the tile's K and V, and its S slot: the softmax has read S(t - 2)
-              if ((t >= 2 && !mbar_wait(&bars[gSRead0 + (t & 1)], ((t - 2) >> 1) & 1)) ||
+              // the tile's K and V, and its S slot: the softmax has read S(t - NS).
+              // The barriers go by tile parity whatever the slots: an issuer
+              // sees every completion of the barrier it waits on, so its
+              // parity cannot alias (with one slot, a single barrier would
+              // complete twice between this issuer's waits).
+              const uint32_t tr = t - NS;
+              if ((t >= uint32_t(NS) && !mbar_wait(&bars[gSRead0 + (tr & 1)], (tr >> 1) & 1)) ||
                   !mbar_wait(&bars[gFull0 + t % NSTAGE], (t / NSTAGE) & 1)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               const uint64_t kd = sdesc_sw128(st0 + (t % NSTAGE) * STAGE, 16, 1024);
+              const uint32_t sd = tmem + TM_S + TT * (t % NS);
               if constexpr (FP8) {
                 // 32 codes per MMA: the hi term of Q, then the lo term
 #pragma unroll
                 for (int kk = 0; kk < D / 32; ++kk) {
-                  umma_ss_f8(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t((kk * 32) >> 4),
-                             kd + uint64_t((kk * 32) >> 4), id_s, kk > 0 ? 1u : 0u);
-                  umma_ss_f8(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t((QHALF + kk * 32) >> 4),
+                  umma_ss_f8(sd, qa0 + uint64_t((kk * 32) >> 4), kd + uint64_t((kk * 32) >> 4), id_s,
+                             kk > 0 ? 1u : 0u);
+                  umma_ss_f8(sd, qa0 + uint64_t((QHALF + kk * 32) >> 4),
                              kd + uint64_t((kk * 32) >> 4), id_s, 1u);
                 }
               } else {
@@ -371,7 +393,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                   const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;     // K: half, 16 dims
                   const uint32_t qoff = (kk >> 2) * QHALF + (kk & 3) * 32;   // Q: same dims
-                  umma_ss(tmem + TM_S + 64 * (t & 1), qa0 + uint64_t(qoff >> 4),
+                  umma_ss(sd, qa0 + uint64_t(qoff >> 4),
                           kd + uint64_t(off >> 4), id_s, kk > 0 ? 1u : 0u);
                 }
               }
@@ -386,7 +408,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
         } else {
           const uint32_t id_o = FP8 ? idesc_e4m3(128, D, true) : idesc_bf16(128, D, true);
           while (ok && w.next(sg)) {
-            const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
+            const int ntile = ((sg.j1 - sg.j0) * cpp + CPT - 1) / CPT;
             for (int k = 0; k < ntile && ok; ++k, ++t) {
               // O (+)= P(t) V(t): the first tile of a segment overwrites O, once
               // the previous segment's epilogue has read it
@@ -397,21 +419,24 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
               }
               tc_fence_after();
               const uint64_t vd = sdesc_sw128(st0 + (t % NSTAGE) * STAGE + V_OFF, HALF, 1024);
-              // tokens 0-31 into O_0, tokens 32-63 into O_1 (the two softmax halves)
+              // the tile's first half of tokens into O_0, its second into O_1
+              // (the two softmax halves)
               if constexpr (FP8) {
                 // 32 tokens per MMA, for the hi and the lo term of P (P slot
-                // columns: hi half 0, hi half 1, lo half 0, lo half 1, 8 each)
+                // columns: hi half 0, hi half 1, lo half 0, lo half 1, TT / 8
+                // each)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const int h2 = kk & 1, term = kk >> 1;
-                  umma_ts_f8(tmem + TM_O + 128 * h2, tmem + TM_P + 32 * (t % NP) + 16 * term + 8 * h2,
-                             vd + uint64_t((h2 * 32 * 128) >> 4), id_o,
-                             (k == 0 && term == 0) ? 0u : 1u);
+                for (int kk = 0; kk < TT / 16; ++kk) {
+                  const int ks = kk % (TT / 64), h2 = (kk / (TT / 64)) & 1, term = kk / (TT / 32);
+                  umma_ts_f8(tmem + TM_O + 128 * h2,
+                             tmem + TM_P + PCOLS * (t % NP) + (TT / 4) * term + (TT / 8) * h2 + 8 * ks,
+                             vd + uint64_t(((h2 * (TT / 2) + ks * 32) * 128) >> 4), id_o,
+                             (k == 0 && term == 0 && ks == 0) ? 0u : 1u);
                 }
               } else {
 #pragma unroll
                 for (int kk = 0; kk < TT / 16; ++kk)
-                  umma_ts(tmem + TM_O + 128 * (kk >> 1), tmem + TM_P + 32 * (t % NP) + 8 * kk,
+                  umma_ts(tmem + TM_O + 128 * (kk >> 1), tmem + TM_P + PCOLS * (t % NP) + 8 * kk,
                           vd + uint64_t((kk * 16 * 128) >> 4), id_o,
                           (k == 0 && (kk & 1) == 0) ? 0u : 1u);
               }
@@ -435,7 +460,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
     } else {
       // ---------------------------------------------------- softmax / epilogue
       // Threads by MMA row (TMEM lane) m and token half hh: warps 2-5 take the
-      // tile's tokens 0-31 (hh = 0), warps 10-13 tokens 32-63 (hh = 1).  Row m
+      // tile's first TT / 2 tokens (hh = 0), warps 10-13 the rest (hh = 1).  Row m
       // is copy c = m / RP of unit row r = m % RP, and of its half the thread
       // takes the TP tokens of part c.  Each (lane, half) keeps its own
       // running max, sum and share of O_hh (O_hh += P[:, half] V[half, :]), so
@@ -446,11 +471,11 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
       // quadrant q is readable only from sub-partition q, so spare MMA rows
       // spread the work only by holding copies.)
       constexpr int RP = 128 / DUP;                         // rows per copy
-      constexpr int TP = 32 / DUP;                          // tokens per thread and tile
+      constexpr int TP = TT / 2 / DUP;                      // tokens per thread and tile
       const int m = 32 * (warp & 3) + lane;                 // MMA row = TMEM lane
       const int cpy = m / RP, r = m % RP;
       const int hh = warp >= 10 ? 1 : 0;
-      const int part = 32 * hh + TP * cpy;                  // first token of this thread's part
+      const int part = (TT / 2) * hh + TP * cpy;            // first token of this thread's part
       const uint32_t lane_off = uint32_t(32 * (warp & 3)) << 16;
       const int tid = hh * 128 + m;                         // 0..255
       const uint32_t tm_oh = TM_O + 128 * hh;               // this half's O
@@ -475,7 +500,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
         len = max(0, min(len, sg.n * p.bs));
         const int lim = row_ok ? len - back : 0;            // this row sees tokens [0, lim)
         const int tok_beg = sg.j0 * p.bs, tok_end = sg.j1 * p.bs;
-        const int ntile = ((sg.j1 - sg.j0) * cpp + 3) / 4;
+        const int ntile = ((sg.j1 - sg.j0) * cpp + CPT - 1) / CPT;
         float m_ref = -INFINITY, l = 0.f;
         float qk = p.qk_scale_log2;   // raw score -> log2 units (E4M3: times this row's 2^-e)
         if constexpr (FP8) {
@@ -497,10 +522,17 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           if (!good) break;
           tc_fence_after();
           uint32_t sv[TP];
-          const uint32_t sa = tmem + lane_off + TM_S + 64 * (t & 1) + part;
-          if constexpr (TP == 32) tmem_ld32(sa, sv);
-          else if constexpr (TP == 16) tmem_ld16(sa, sv);
-          else tmem_ld8(sa, sv);
+          const uint32_t sa = tmem + lane_off + TM_S + TT * (t % NS) + part;
+          if constexpr (TP == 64) {
+            tmem_ld32(sa, *reinterpret_cast<uint32_t(*)[32]>(sv));
+            tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+          } else if constexpr (TP == 32) {
+            tmem_ld32(sa, sv);
+          } else if constexpr (TP == 16) {
+            tmem_ld16(sa, sv);
+          } else {
+            tmem_ld8(sa, sv);
+          }
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
@@ -543,8 +575,10 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           float ls = 0.f;
           if constexpr (FP8) {
             // two E4M3 terms, four codes per TMEM column: this copy's part of
-            // the half's 32 tokens (8 columns per term), zeros elsewhere
-            uint32_t ph[TP / 4], pl[TP / 4];
+            // the half's TT / 2 tokens (TT / 8 columns per term), zeros
+            // elsewhere
+            constexpr int HC = TT / 8, MC = TP / 4;   // columns of the half, of this part
+            uint32_t ph[MC], pl[MC];
 #pragma unroll
             for (int j = 0; j < TP / 2; ++j) {
               const float a0 = 2 * j < nv ? exp2_approx(fmaf(__uint_as_float(sv[2 * j]), qk, -m_ref)) : 0.f;
@@ -560,14 +594,15 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
                 pl[j >> 1] = l2;
               }
             }
-            uint32_t kh[8], kl[8];
+            uint32_t kh[HC], kl[HC];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              kh[i] = (i / (TP / 4) == cpy) ? ph[i % (TP / 4)] : 0u;
-              kl[i] = (i / (TP / 4) == cpy) ? pl[i % (TP / 4)] : 0u;
+            for (int i = 0; i < HC; ++i) {
+              kh[i] = (i / MC == cpy) ? ph[i % MC] : 0u;
+              kl[i] = (i / MC == cpy) ? pl[i % MC] : 0u;
             }
-            tmem_st8(tmem + lane_off + TM_P + 32 * (t % NP) + 8 * hh, kh);
-            tmem_st8(tmem + lane_off + TM_P + 32 * (t % NP) + 16 + 8 * hh, kl);
+            static_assert(HC == 16, "P store");
+            tmem_st16(tmem + lane_off + TM_P + PCOLS * (t % NP) + HC * hh, kh);
+            tmem_st16(tmem + lane_off + TM_P + PCOLS * (t % NP) + 2 * HC + HC * hh, kl);
           } else {
             uint32_t pv[TP / 2];
 #pragma unroll
@@ -582,7 +617,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = (i / (TP / 2) == cpy) ? pv[i % (TP / 2)] : 0u;
-            tmem_st16(tmem + lane_off + TM_P + 32 * (t % NP) + 16 * hh, pk);
+            tmem_st16(tmem + lane_off + TM_P + PCOLS * (t % NP) + 16 * hh, pk);
           }
           l += ls;
           tmem_st_wait();

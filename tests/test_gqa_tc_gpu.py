@@ -111,8 +111,9 @@ def test_full_size_sampled(oracle):
     _multi(oracle, wl, 8, seqs=[0, 13, 31])
 
 
-# ---- FP8-E4M3 cache: kind::f8f6f4 MMAs, query and probabilities as two E4M3
-# terms each, against the oracle's decode of the stored codes
+# ---- FP8-E4M3 cache: kind::f8f6f4 MMAs over 128-token tiles, query and
+# probabilities as two E4M3 terms each, against the oracle's decode of the
+# stored codes
 
 
 @pytest.mark.parametrize("q_len", [3, 4, 8, 12, 16])
@@ -127,8 +128,10 @@ def test_fp8_forced_splits(oracle, num_ctas):
            num_ctas=num_ctas)
 
 
-@pytest.mark.parametrize("bs", [32, 64, 128])
+@pytest.mark.parametrize("bs", [16, 32, 48, 64, 128, 256])
 def test_fp8_block_sizes(oracle, bs):
+    # an E4M3 tile is 128 tokens: 8 pages, 4, 2 and 2/3 of a page, 2, 1, half
+    # of one
     _multi(oracle, inputs.make_workload("llama3_70b_fp8", lens=[1000, 300, 77], block_size=bs), 8,
            num_ctas=5)
 
