@@ -491,6 +491,17 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
       auto wait_all = [](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
       };
+      if constexpr (FP8) {
+        // zero this row's columns of this half in both P slots, both terms
+        // (each tile then writes only its own part)
+        const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int sl = 0; sl < NP; ++sl)
+#pragma unroll
+          for (int term = 0; term < 2; ++term)
+            tmem_st16(tmem + lane_off + TM_P + PCOLS * sl + (TT / 4) * term + (TT / 8) * hh, z);
+        tmem_st_wait();
+      }
       Walker w{p.cum, p.hkv, st, en};
       Seg sg;
       uint32_t t = 0, seg = 0;
@@ -594,15 +605,20 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
                 pl[j >> 1] = l2;
               }
             }
-            uint32_t kh[HC], kl[HC];
-#pragma unroll
-            for (int i = 0; i < HC; ++i) {
-              kh[i] = (i / MC == cpy) ? ph[i % MC] : 0u;
-              kl[i] = (i / MC == cpy) ? pl[i % MC] : 0u;
+            // only this part's columns: the rest of the row stays zero from
+            // the start of the kernel (no other thread writes this row)
+            const uint32_t pa = tmem + lane_off + TM_P + PCOLS * (t % NP) + HC * hh + MC * cpy;
+            if constexpr (MC == 16) {
+              tmem_st16(pa, ph);
+              tmem_st16(pa + 2 * HC, pl);
+            } else if constexpr (MC == 8) {
+              tmem_st8(pa, ph);
+              tmem_st8(pa + 2 * HC, pl);
+            } else {
+              static_assert(MC == 4, "P store");
+              tmem_st4(pa, ph);
+              tmem_st4(pa + 2 * HC, pl);
             }
-            static_assert(HC == 16, "P store");
-            tmem_st16(tmem + lane_off + TM_P + PCOLS * (t % NP) + HC * hh, kh);
-            tmem_st16(tmem + lane_off + TM_P + PCOLS * (t % NP) + 2 * HC + HC * hh, kl);
           } else {
             uint32_t pv[TP / 2];
 #pragma unroll

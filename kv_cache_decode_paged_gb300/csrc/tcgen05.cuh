@@ -174,6 +174,11 @@ KV_DEVI void tmem_st8(uint32_t taddr, const uint32_t* r) {
                KV_W8(0)
                : "memory");
 }
+KV_DEVI void tmem_st4(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
 KV_DEVI void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 #undef KV_R8
