@@ -491,15 +491,20 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
       auto wait_all = [](uint64_t* bar, uint32_t parity) {
         return __all_sync(0xffffffffu, mbar_wait(bar, parity) ? 1 : 0) != 0;
       };
-      if constexpr (FP8) {
-        // zero this row's columns of this half in both P slots, both terms
-        // (each tile then writes only its own part)
+      {
+        // zero this row's columns of this half in both P slots (both terms for
+        // E4M3): each tile then writes only its own part
         const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int sl = 0; sl < NP; ++sl)
+        for (int sl = 0; sl < NP; ++sl) {
+          if constexpr (FP8) {
 #pragma unroll
-          for (int term = 0; term < 2; ++term)
-            tmem_st16(tmem + lane_off + TM_P + PCOLS * sl + (TT / 4) * term + (TT / 8) * hh, z);
+            for (int term = 0; term < 2; ++term)
+              tmem_st16(tmem + lane_off + TM_P + PCOLS * sl + (TT / 4) * term + (TT / 8) * hh, z);
+          } else {
+            tmem_st16(tmem + lane_off + TM_P + PCOLS * sl + 16 * hh, z);
+          }
+        }
         tmem_st_wait();
       }
       Walker w{p.cum, p.hkv, st, en};
@@ -628,12 +633,18 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
               ls += a0 + a1;
               pv[j] = pack_bf16(a0, a1);
             }
-            // this half's 32 tokens as 16 bf16 pairs: this copy's part, zeros
-            // elsewhere (the other copies' rows hold the other parts)
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = (i / (TP / 2) == cpy) ? pv[i % (TP / 2)] : 0u;
-            tmem_st16(tmem + lane_off + TM_P + PCOLS * (t % NP) + 16 * hh, pk);
+            // this half's 32 tokens are 16 bf16 pairs; this thread stores its
+            // copy's part (the other copies' rows hold the other parts, and
+            // these columns of this row stay zero from the start)
+            const uint32_t pa = tmem + lane_off + TM_P + PCOLS * (t % NP) + 16 * hh + (TP / 2) * cpy;
+            if constexpr (TP / 2 == 16) {
+              tmem_st16(pa, pv);
+            } else if constexpr (TP / 2 == 8) {
+              tmem_st8(pa, pv);
+            } else {
+              static_assert(TP / 2 == 4, "P store");
+              tmem_st4(pa, pv);
+            }
           }
           l += ls;
           tmem_st_wait();
