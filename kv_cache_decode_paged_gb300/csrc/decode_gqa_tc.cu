@@ -115,12 +115,20 @@ enum : int {
 static_assert(gNumBars <= gtc::NBARS, "barrier slots");
 
 // Two E4M3 terms of a float pair: hi = e4m3(x), lo = e4m3(x - hi), each a
-// 16-bit code pair (first value in the low byte).
+// 16-bit code pair (first value in the low byte).  x is first rounded to f16
+// (both callers pass values below 2^9, and E4M3 keeps 4 significant bits per
+// term, so the f16 rounding is far below the terms' own); then hi is exact in
+// f16 and so is x - hi, which one f16x2 subtraction gives for both values.
 KV_DEVI void e4m3_two_terms_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = e4m3x2(x0, x1);
-  const uint32_t hf = e4m3x2_to_f16x2(uint16_t(hi));
-  const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hf));
-  lo = e4m3x2(x0 - h.x, x1 - h.y);
+  const uint32_t xf = pack_f16(x0, x1);
+  uint16_t h, l;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(xf));
+  const uint32_t hf = e4m3x2_to_f16x2(h);
+  uint32_t rf;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rf) : "r"(xf), "r"(hf));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(rf));
+  hi = h;
+  lo = l;
 }
 
 // E4M3 cache: MMA row m (copy of unit row r) of the query as two E4M3 terms
