@@ -234,12 +234,21 @@ KV_DEVI int q_row_exp(const uint16_t* qrow, bool live, uint32_t rank, float r_ra
   return mx > 0.f ? min(max(7 - (int((__float_as_uint(mx) >> 23) & 255) - 127), -120), 120) : 0;
 }
 // Two E4M3 terms of a float pair: hi = e4m3(x), lo = e4m3(x - hi), each a
-// 16-bit code pair (first value in the low byte).
+// 16-bit code pair (first value in the low byte).  x is first rounded to f16
+// (the query is scaled below 2^8 and P stays below 2^9, and E4M3 keeps 4
+// significant bits per term, so the f16 rounding is far below the terms'
+// own); then hi is exact in f16 and so is x - hi, which one f16x2
+// subtraction gives for both values.
 KV_DEVI void e4m3_two_terms(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = e4m3x2(x0, x1);
-  const uint32_t hf = e4m3x2_to_f16x2(uint16_t(hi));
-  const float2 hd = __half22float2(*reinterpret_cast<const __half2*>(&hf));
-  lo = e4m3x2(x0 - hd.x, x1 - hd.y);
+  const uint32_t xf = pack_f16(x0, x1);
+  uint16_t h, l;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(xf));
+  const uint32_t hf = e4m3x2_to_f16x2(h);
+  uint32_t rf;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rf) : "r"(xf), "r"(hf));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(rf));
+  hi = h;
+  lo = l;
 }
 KV_DEVI void build_q_e4m3(const uint16_t* qrow, bool live, uint32_t rank, float r_ratio, int e,
                           uint32_t tq, uint8_t* lo_c, uint8_t* lo_r, int r) {
