@@ -599,8 +599,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
           float ls = 0.f;
           if constexpr (FP8) {
             // two E4M3 terms, four codes per TMEM column: this copy's part of
-            // the half's TT / 2 tokens (TT / 8 columns per term), zeros
-            // elsewhere
+            // the half's TT / 2 tokens (the half has TT / 8 columns per term)
             constexpr int HC = TT / 8, MC = TP / 4;   // columns of the half, of this part
             uint32_t ph[MC], pl[MC];
 #pragma unroll
