@@ -50,6 +50,17 @@
 #include "tcgen05.cuh"
 #include "walk.cuh"
 
+// Test builds only (-DKV_TEST_DROP_CHUNK=n, with a short KV_WAIT_NS): CTA 0's
+// first producer warp issues none of its loads of tile n, as copies that never
+// land would, so that the tile's barrier never completes, the bounded waits on
+// it run out and the abort path (error bit, stop, drain, exit) runs on the
+// GPU.  The library is built without it.
+#ifdef KV_TEST_DROP_CHUNK
+#define KV_TEST_DROPS_TILE(t, w) (blockIdx.x == 0 && (w) == 0 && (t) == uint32_t(KV_TEST_DROP_CHUNK))
+#else
+#define KV_TEST_DROPS_TILE(t, w) false
+#endif
+
 namespace kv {
 
 namespace gtc {
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(gtc::THREADS, 1)
               const int ci = cc + pc + 4 * qc;                           // this warp's chunk
               const int src = min(max(ci / cpp - (pb - sg.j0), 0), 31);  // lane holding its page
               const int pg_l = __shfl_sync(0xffffffffu, page, src);
-              if (lane == 0) {
+              if (lane == 0 && !KV_TEST_DROPS_TILE(t, warp)) {
                 const int pg = ci < nch ? pg_l : oob_page;
                 const int sub = ci % cpp;
                 uint8_t* dst = smem + OFF_ST + s * STAGE + (pc + 4 * qc) * (16 * 128);

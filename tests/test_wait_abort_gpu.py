@@ -1,4 +1,4 @@
-"""The bounded-wait abort path of the GQA decode kernel, run on the GPU.
+"""The bounded-wait abort path of the GQA decode kernels, run on the GPU.
 
 Every wait of the decode kernels on an mbarrier gives up after a time limit,
 reports KVATTN_DEVERR_TIMEOUT in the caller's error word and ends the kernel
@@ -15,6 +15,12 @@ Checks: the call returns, the stream synchronises within a second, the error
 word holds the timeout bit and nothing else, the sequences that other CTAs
 walked are still right, and afterwards the library's own build decodes the
 same cache correctly in the same context.
+
+The same build drops tile 3 of CTA 0's walk in the tcgen05 kernel (units of
+many rows: 8 new tokens on Llama-3-70B shapes, bf16 and E4M3 caches): the
+first producer warp issues none of that tile's loads, so its barrier never
+completes and the score issuer, the softmax warps and then every other role
+of CTA 0 take the abort path, the producers draining with the full limit.
 """
 import ctypes
 import time
@@ -24,9 +30,9 @@ import pytest
 
 import kv_cache_decode_paged_gb300 as kv
 from kv_cache_decode_paged_gb300 import _build, inputs
-from kv_cache_decode_paged_gb300.device import GpuWorkload
+from kv_cache_decode_paged_gb300.device import GpuWorkload, dev_bits
 
-from _harness import assert_parity, oracle_all
+from _harness import assert_parity, oracle_all, oracle_multi
 
 pytestmark = pytest.mark.gpu
 
@@ -70,3 +76,47 @@ def test_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle):
     ref_out, ref_lse = oracle_all(oracle, wl)
     assert_parity(o2, l2, ref_out, ref_lse)
     assert np.isfinite(o2).all()
+
+
+@pytest.mark.parametrize("name", ["llama3_70b", "llama3_70b_fp8"])
+def test_tc_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle, name):
+    import torch
+    lib = kv.open_library(_build.build_wait_test())
+    # 8 sequences of 1024 tokens, 8 KV heads, over 8 CTAs: CTA c owns pages
+    # [c T / 8, (c + 1) T / 8) of the (sequence, KV head, page) order, so CTA 0
+    # walks the eight units of sequence 0 and no other.  8 new tokens: 64 rows
+    # per unit, the tcgen05 kernel.
+    wl = inputs.make_workload(name, lens=[1024] * 8)
+    q_len = 8
+    qm = inputs.multi_token_queries(wl, q_len)
+    g = GpuWorkload(wl)
+    q = dev_bits(qm)
+    ws = kv.workspace_for(kv.KVATTN_GQA, wl.B, wl.h * q_len, wl.h_kv, wl.d, 8, "cuda")
+    out = torch.full((wl.B, q_len, wl.h, wl.d), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((wl.B, q_len, wl.h), float("nan"), dtype=torch.float32, device="cuda")
+    g.err.zero_()
+    torch.cuda.synchronize()
+    desc = g.cache.descriptor()
+    t0 = time.monotonic()
+    status = lib.kvattn_decode_gqa_multi(
+        q.data_ptr(), ctypes.byref(desc), g.bt.data_ptr(), g.seq_lens.data_ptr(), wl.B,
+        wl.max_blocks, q_len, wl.h, wl.h_kv, wl.d, wl.scale, out.data_ptr(), lse.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), 8, g.err.data_ptr(),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert status == kv.KVATTN_OK
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert elapsed < 1.0, f"aborted decode took {elapsed:.3f} s"
+    assert g.err_bits() == kv.KVATTN_DEVERR_TIMEOUT
+
+    fp8 = wl.kv_dtype == "fp8"
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    ref_out, ref_lse = oracle_multi(oracle, wl, qm, seqs=range(1, wl.B))
+    assert_parity(o, l, ref_out, ref_lse, fp8=fp8)
+
+    # the library's own build decodes the same cache in the same context
+    g.err.zero_()
+    o2, l2 = g.decode_multi(qm, num_ctas=8)
+    assert g.err_bits() == 0
+    ref_out, ref_lse = oracle_multi(oracle, wl, qm)
+    assert_parity(o2, l2, ref_out, ref_lse, fp8=fp8)
