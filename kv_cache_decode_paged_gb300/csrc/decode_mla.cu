@@ -62,6 +62,17 @@
 #include "tcgen05.cuh"
 #include "walk.cuh"
 
+// Test builds only (-DKV_TEST_DROP_CHUNK=n, with a short KV_WAIT_NS): the
+// producer of CTA 0 (rank 0 of pair 0) arms tile n's barrier but issues none
+// of its loads, as copies that never land would, so that the waits on that
+// tile (and through the exchange, the peer's) run out and both ranks take the
+// abort path on the GPU.  The library is built without it.
+#ifdef KV_TEST_DROP_CHUNK
+#define KV_TEST_DROPS_MLA_TILE(it) (blockIdx.x == 0 && (it) == uint32_t(KV_TEST_DROP_CHUNK))
+#else
+#define KV_TEST_DROPS_MLA_TILE(it) false
+#endif
+
 namespace kv {
 
 namespace mla {
@@ -476,10 +487,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::THREADS, 1)
             } else {
               uint8_t* stg = smem + OFF_V + s * VF_BYTES;
               mbar_arrive_expect_tx(&bars[kKVFull0 + s], uint32_t(VSTAGE + RH_BYTES));
-              for (int b = 0; b < G::NVB; ++b)
-                tma_load_3d(stg + b * VBOX, &tmLF, vx0 + G::BOX_DIMS * b, 0, pg,
-                            &bars[kKVFull0 + s], pol);
-              tma_load_3d(smem + OFF_R + q * RH_BYTES, &tmLH, rx, 0, pg, &bars[kKVFull0 + s], pol);
+              if (!KV_TEST_DROPS_MLA_TILE(it)) {
+                for (int b = 0; b < G::NVB; ++b)
+                  tma_load_3d(stg + b * VBOX, &tmLF, vx0 + G::BOX_DIMS * b, 0, pg,
+                              &bars[kKVFull0 + s], pol);
+                tma_load_3d(smem + OFF_R + q * RH_BYTES, &tmLH, rx, 0, pg, &bars[kKVFull0 + s], pol);
+              }
               issued = 1;
               if (*abort_flag) ok = false;
             }

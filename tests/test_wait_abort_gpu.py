@@ -21,6 +21,11 @@ many rows: 8 new tokens on Llama-3-70B shapes, bf16 and E4M3 caches): the
 first producer warp issues none of that tile's loads, so its barrier never
 completes and the score issuer, the softmax warps and then every other role
 of CTA 0 take the abort path, the producers draining with the full limit.
+
+And the MLA decode's CTA pair (bf16 and E4M3 latent caches): rank 0 of pair
+0 arms tile 3's barrier but loads nothing, so its score MMAs never run, the
+peer waits in vain for that tile's partial scores, and both ranks abort,
+drain the exchange and meet at the final cluster barrier.
 """
 import ctypes
 import time
@@ -119,4 +124,42 @@ def test_tc_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle, name):
     o2, l2 = g.decode_multi(qm, num_ctas=8)
     assert g.err_bits() == 0
     ref_out, ref_lse = oracle_multi(oracle, wl, qm)
+    assert_parity(o2, l2, ref_out, ref_lse, fp8=fp8)
+
+
+@pytest.mark.parametrize("name", ["deepseek_v3_mla", "deepseek_v3_mla_fp8"])
+def test_mla_pair_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle, name):
+    import torch
+    lib = kv.open_library(_build.build_wait_test())
+    # 8 sequences of 1024 tokens on 8 CTA pairs: one pair per sequence (no
+    # split, no merge), so pair 0 (CTAs 0 and 1) walks sequence 0 alone
+    wl = inputs.make_workload(name, lens=[1024] * 8)
+    g = GpuWorkload(wl)
+    ws = g.workspace(num_ctas=8)
+    out = torch.full((wl.B, wl.h, wl.d_c), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((wl.B, wl.h), float("nan"), dtype=torch.float32, device="cuda")
+    g.err.zero_()
+    torch.cuda.synchronize()
+    desc = g.cache.descriptor()
+    t0 = time.monotonic()
+    status = lib.kvattn_decode_mla(
+        g.q.data_ptr(), ctypes.byref(desc), g.bt.data_ptr(), g.seq_lens.data_ptr(), wl.B,
+        wl.max_blocks, wl.h, wl.d_c, wl.d_rope, wl.scale, out.data_ptr(), lse.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), 8, g.err.data_ptr(),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert status == kv.KVATTN_OK
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert elapsed < 2.0, f"aborted decode took {elapsed:.3f} s"
+    assert g.err_bits() == kv.KVATTN_DEVERR_TIMEOUT
+
+    fp8 = wl.kv_dtype == "fp8"
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    ref_out, ref_lse = oracle_all(oracle, wl, seqs=range(1, wl.B))
+    assert_parity(o, l, ref_out, ref_lse, fp8=fp8)
+
+    g.err.zero_()
+    o2, l2 = g.decode(num_ctas=8)
+    assert g.err_bits() == 0
+    ref_out, ref_lse = oracle_all(oracle, wl)
     assert_parity(o2, l2, ref_out, ref_lse, fp8=fp8)
