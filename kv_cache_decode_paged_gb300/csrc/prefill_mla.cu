@@ -33,6 +33,18 @@
 #include "internal.h"
 #include "tcgen05.cuh"
 
+// Test builds only (-DKV_TEST_DROP_CHUNK=n, with a short KV_WAIT_NS): the
+// producer of the CTA of (query tile 0, head 0, sequence 0) arms chunk n's
+// barrier but issues none of its loads, as copies that never land would, so
+// that the waits on it run out and the abort path runs on the GPU.  The
+// library is built without it.
+#ifdef KV_TEST_DROP_CHUNK
+#define KV_TEST_DROPS_PREFILL_CHUNK(g) \
+  (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (g) == uint32_t(KV_TEST_DROP_CHUNK))
+#else
+#define KV_TEST_DROPS_PREFILL_CHUNK(g) false
+#endif
+
 namespace kv {
 
 namespace pf {
@@ -172,10 +184,12 @@ __global__ void __launch_bounds__(pf::THREADS, 1)
           }
           uint8_t* dst = smem + OFF_CH + slot * CH_BYTES;
           mbar_arrive_expect_tx(&bars[pChFull0 + slot], CH_BYTES);
-          tma_load_3d_nohint(dst, &tmL, 64 * ch, 0, pg0, &bars[pChFull0 + slot]);
-          tma_load_3d_nohint(dst + BOX / 2, &tmL, 64 * ch, 0, pg1, &bars[pChFull0 + slot]);
-          tma_load_3d_nohint(dst + BOX, &tmWK, 64 * ch, 0, head, &bars[pChFull0 + slot]);
-          tma_load_3d_nohint(dst + 2 * BOX, &tmWV, 64 * ch, 0, head, &bars[pChFull0 + slot]);
+          if (!KV_TEST_DROPS_PREFILL_CHUNK(g)) {
+            tma_load_3d_nohint(dst, &tmL, 64 * ch, 0, pg0, &bars[pChFull0 + slot]);
+            tma_load_3d_nohint(dst + BOX / 2, &tmL, 64 * ch, 0, pg1, &bars[pChFull0 + slot]);
+            tma_load_3d_nohint(dst + BOX, &tmWK, 64 * ch, 0, head, &bars[pChFull0 + slot]);
+            tma_load_3d_nohint(dst + 2 * BOX, &tmWV, 64 * ch, 0, head, &bars[pChFull0 + slot]);
+          }
         }
         if (*abort_flag) ok = false;
       }

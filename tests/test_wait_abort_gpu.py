@@ -26,6 +26,11 @@ And the MLA decode's CTA pair (bf16 and E4M3 latent caches): rank 0 of pair
 0 arms tile 3's barrier but loads nothing, so its score MMAs never run, the
 peer waits in vain for that tile's partial scores, and both ranks abort,
 drain the exchange and meet at the final cluster barrier.
+
+And the explicit-form MLA prefill: the CTA of (query tile 0, head 0,
+sequence 0) arms chunk 3 of its expansion but loads nothing; its MMA issuer
+and compute warps time out and it drains, while the other (head, sequence)
+CTAs finish normally.
 """
 import ctypes
 import time
@@ -37,7 +42,8 @@ import kv_cache_decode_paged_gb300 as kv
 from kv_cache_decode_paged_gb300 import _build, inputs
 from kv_cache_decode_paged_gb300.device import GpuWorkload, dev_bits
 
-from _harness import assert_parity, oracle_all, oracle_multi
+from _harness import (TOL_ABS_BF16, TOL_LSE, TOL_RELRMS, assert_parity, errors, oracle_all,
+                      oracle_multi)
 
 pytestmark = pytest.mark.gpu
 
@@ -163,3 +169,59 @@ def test_mla_pair_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle, name
     assert g.err_bits() == 0
     ref_out, ref_lse = oracle_all(oracle, wl)
     assert_parity(o2, l2, ref_out, ref_lse, fp8=fp8)
+
+
+def test_prefill_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle):
+    import torch
+    lib = kv.open_library(_build.build_wait_test())
+    h, q_len = 4, 16
+    wl = inputs.make_workload("deepseek_v3_mla", lens=[300, 200], heads=h)
+    g = GpuWorkload(wl)
+    qn, qr = inputs.prefill_queries(wl.B, q_len, h=h)
+    pj = inputs.mla_projections(1, h=h)
+    dq, dr, wk, wv = (dev_bits(x) for x in (qn, qr, pj.w_uk, pj.w_uv))
+
+    def run(call):
+        out = torch.full((wl.B, q_len, h, 128), float("nan"), dtype=torch.float32, device="cuda")
+        lse = torch.full((wl.B, q_len, h), float("nan"), dtype=torch.float32, device="cuda")
+        g.err.zero_()
+        torch.cuda.synchronize()
+        t0 = time.monotonic()
+        call(out, lse)
+        torch.cuda.synchronize()
+        return out.cpu().numpy(), lse.cpu().numpy(), time.monotonic() - t0
+
+    desc = g.cache.descriptor()
+    o, l, elapsed = run(lambda out, lse: lib.kvattn_mla_prefill(
+        dq.data_ptr(), dr.data_ptr(), ctypes.byref(desc), g.bt.data_ptr(), g.seq_lens.data_ptr(),
+        wl.B, wl.max_blocks, q_len, h, 128, 128, wk.data_ptr(), wv.data_ptr(), wl.scale,
+        out.data_ptr(), lse.data_ptr(), g.err.data_ptr(),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))
+    assert elapsed < 1.0, f"aborted prefill took {elapsed:.3f} s"
+    assert g.err_bits() == kv.KVATTN_DEVERR_TIMEOUT
+
+    f64 = lambda bits: inputs.bf16_to_f32(bits).astype(np.float64)
+
+    def check(o, l, skip):
+        for b in range(wl.B):
+            sl = wl.seq_slice(b)
+            ref_o, ref_l = oracle.mla_prefill(f64(qn[b]), f64(qr[b]), f64(wl.c_kv[sl]),
+                                              f64(wl.k_r[sl]), f64(pj.w_uk), f64(pj.w_uv),
+                                              wl.scale)
+            for hd in range(h):
+                if (b, hd) == skip:
+                    continue
+                got = o[b][:, hd]
+                assert np.isfinite(got).all()
+                max_abs, rel = errors(got, ref_o[:, hd])
+                assert max_abs <= TOL_ABS_BF16 and rel <= TOL_RELRMS, (b, hd, max_abs, rel)
+                assert np.abs(l[b][:, hd] - ref_l[:, hd]).max() <= TOL_LSE
+
+    # every (sequence, head) but the aborted CTA's is right
+    check(o, l, skip=(0, 0))
+
+    # the library's own build, same context: all of them
+    o2, l2, _ = run(lambda out, lse: kv.kvattn_mla_prefill(
+        dq, dr, g.cache.descriptor(), g.bt, g.seq_lens, wk, wv, wl.scale, out, lse, err=g.err))
+    assert g.err_bits() == 0
+    check(o2, l2, skip=None)
