@@ -25,6 +25,20 @@
 #include "internal.h"
 #include "tcgen05.cuh"
 
+// Test builds only (-DKV_TEST_DROP_CHUNK=n, with a short KV_WAIT_NS): the CTA
+// of head 0 and batch tile 0 arms a barrier but issues none of its loads (the
+// query absorption: part 1 of W_UK; the up-projection: chunk n of W_UV), as
+// copies that never land would, so that the waits on it run out and the
+// abort path runs on the GPU.  The library is built without it.
+#ifdef KV_TEST_DROP_CHUNK
+#define KV_TEST_DROPS_ABSORB_PART(part) \
+  (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (part) == 1)
+#define KV_TEST_DROPS_UPV_CHUNK(c) (blockIdx.x == 0 && blockIdx.y == 0 && (c) == KV_TEST_DROP_CHUNK)
+#else
+#define KV_TEST_DROPS_ABSORB_PART(part) false
+#define KV_TEST_DROPS_UPV_CHUNK(c) false
+#endif
+
 namespace kv {
 
 namespace absorb {
@@ -153,9 +167,10 @@ __global__ void __launch_bounds__(absorb::THREADS)
         }
         for (int e = 0; e < np; ++e) {
           mbar_arrive_expect_tx(&wfull[e], 4 * BOX);
-          for (int nb = 0; nb < 4; ++nb)      // W_UK,i columns 256 (2g+e) + 64 nb.., all rows
-            tma_load_3d_nohint(smem + Q_OFF_W + e * Q_WSLOT + nb * BOX, &tmW,
-                               QN * (2 * g + e) + 64 * nb, 0, i, &wfull[e]);
+          if (!KV_TEST_DROPS_ABSORB_PART(2 * g + e))
+            for (int nb = 0; nb < 4; ++nb)    // W_UK,i columns 256 (2g+e) + 64 nb.., all rows
+              tma_load_3d_nohint(smem + Q_OFF_W + e * Q_WSLOT + nb * BOX, &tmW,
+                                 QN * (2 * g + e) + 64 * nb, 0, i, &wfull[e]);
         }
       }
       __syncwarp();
@@ -175,8 +190,9 @@ __global__ void __launch_bounds__(absorb::THREADS)
           }
         } else {
           ok = false;
-          mbar_wait(afull, 0);                // the loads may still land: wait once more
-          mbar_wait(&wfull[e], g & 1);
+          // the loads may still land: wait once more, with the drain's limit
+          mbar_wait(afull, 0, KV_DRAIN_WAIT_NS);
+          mbar_wait(&wfull[e], g & 1, KV_DRAIN_WAIT_NS);
           if (lane == 0) mbar_arrive(&mdone[e]);   // release the readers; nothing is stored
         }
         __syncwarp();
@@ -307,8 +323,9 @@ __global__ void __launch_bounds__(absorb::THREADS)
   auto load_w = [&](int c) {   // chunk c into slot c % 4
     uint8_t* sb = smem + V_OFF_B + (c % V_BSLOTS) * 2 * BOX;
     mbar_arrive_expect_tx(&bfull[c % V_BSLOTS], 2 * BOX);
-    for (int kb = 0; kb < 2; ++kb)   // W_UV,i rows 0..127, columns VK c + 64 kb..
-      tma_load_3d_nohint(sb + kb * BOX, &tmW, VK * c + 64 * kb, 0, i, &bfull[c % V_BSLOTS]);
+    if (!KV_TEST_DROPS_UPV_CHUNK(c))
+      for (int kb = 0; kb < 2; ++kb)   // W_UV,i rows 0..127, columns VK c + 64 kb..
+        tma_load_3d_nohint(sb + kb * BOX, &tmW, VK * c + 64 * kb, 0, i, &bfull[c % V_BSLOTS]);
     issued = c + 1;
   };
   if (tid == 0)
@@ -396,11 +413,11 @@ __global__ void __launch_bounds__(absorb::THREADS)
   ok = __syncthreads_and(ok) != 0;
   if (warp == 0 && !ok) {
     if (lane == 0) report(p.err, KVATTN_DEVERR_TIMEOUT);
-    // the newest load of each slot may still be landing: wait once more
-    // (lane 0 counted the loads it issued)
+    // the newest load of each slot may still be landing: wait once more,
+    // with the drain's limit (lane 0 counted the loads it issued)
     const int n = __shfl_sync(0xffffffffu, issued, 0);
     for (int c = n > V_BSLOTS ? n - V_BSLOTS : 0; c < n; ++c)
-      mbar_wait(&bfull[c % V_BSLOTS], (c / V_BSLOTS) & 1);
+      mbar_wait(&bfull[c % V_BSLOTS], (c / V_BSLOTS) & 1, KV_DRAIN_WAIT_NS);
   }
   __syncwarp();
   tc_fence_after();

@@ -31,6 +31,11 @@ And the explicit-form MLA prefill: the CTA of (query tile 0, head 0,
 sequence 0) arms chunk 3 of its expansion but loads nothing; its MMA issuer
 and compute warps time out and it drains, while the other (head, sequence)
 CTAs finish normally.
+
+And the two per-head projection GEMMs around the MLA decode: the CTA of
+head 0 arms part 1 of W_UK (query absorption) or chunk 3 of W_UV (value
+up-projection) but loads nothing; it times out and drains, and the other
+heads' results are right.
 """
 import ctypes
 import time
@@ -225,3 +230,84 @@ def test_prefill_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle):
         dq, dr, g.cache.descriptor(), g.bt, g.seq_lens, wk, wv, wl.scale, out, lse, err=g.err))
     assert g.err_bits() == 0
     check(o2, l2, skip=None)
+
+
+def _absorb_bounds_ok(oracle, got, pj, heads):
+    f32 = lambda bits: inputs.bf16_to_f32(bits).astype(np.float64)
+    w = f32(pj.w_uk)
+    d_c = pj.w_uk.shape[2]
+    for b in range(pj.q_nope.shape[0]):
+        qc = f32(pj.q_nope[b])
+        ref = oracle.mla_absorb_query(qc, w)
+        absdot = np.einsum("hj,hjc->hc", np.abs(qc), np.abs(w))
+        # products exact in float32, a K-term float32 sum, then bf16 rounding
+        bound = 2.0 ** -8 * np.abs(ref) + (1 + 2.0 ** -8) * qc.shape[1] * 2.0 ** -23 * absdot
+        g = f32(got[b, :, :d_c])
+        assert not (np.abs(g - ref) > bound)[heads].any(), b
+        np.testing.assert_array_equal(got[b, heads, d_c:], pj.q_rope[b, heads])
+
+
+def test_absorb_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle):
+    import torch
+    lib = kv.open_library(_build.build_wait_test())
+    B, h = 4, 4
+    pj = inputs.mla_projections(B, h=h, seed=11)
+    qn, qr, wk = dev_bits(pj.q_nope), dev_bits(pj.q_rope), dev_bits(pj.w_uk)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_abs = torch.full((B, h, 576), -1, dtype=torch.int16, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    status = lib.kvattn_mla_absorb_q(qn.data_ptr(), qr.data_ptr(), wk.data_ptr(), B, h, 128, 512,
+                                     64, q_abs.data_ptr(), err.data_ptr(),
+                                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert status == kv.KVATTN_OK
+    torch.cuda.synchronize()
+    assert time.monotonic() - t0 < 1.0
+    assert int(err.item()) == kv.KVATTN_DEVERR_TIMEOUT
+    _absorb_bounds_ok(oracle, q_abs.cpu().numpy().view(np.uint16), pj, slice(1, h))
+
+    err.zero_()
+    q_abs.fill_(-1)
+    kv.kvattn_mla_absorb_q(qn, qr, wk, q_abs, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _absorb_bounds_ok(oracle, q_abs.cpu().numpy().view(np.uint16), pj, slice(0, h))
+
+
+def test_up_v_wait_that_runs_out_ends_the_kernel_with_a_timeout(oracle):
+    import torch
+    lib = kv.open_library(_build.build_wait_test())
+    B, h, d_c = 4, 4, 512
+    pj = inputs.mla_projections(B, h=h, d_c=d_c, seed=13)
+    d_v = pj.w_uv.shape[1]
+    u = inputs.rng_for(B, "u_tilde").standard_normal((B, h, d_c), dtype=np.float32) * np.float32(0.05)
+    ud, wv = torch.from_numpy(u).cuda(), dev_bits(pj.w_uv)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    v = torch.full((B, h, d_v), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    status = lib.kvattn_mla_up_v(ud.data_ptr(), wv.data_ptr(), B, h, d_c, d_v, v.data_ptr(),
+                                 err.data_ptr(),
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert status == kv.KVATTN_OK
+    torch.cuda.synchronize()
+    assert time.monotonic() - t0 < 1.0
+    assert int(err.item()) == kv.KVATTN_DEVERR_TIMEOUT
+    w = inputs.bf16_to_f32(pj.w_uv).astype(np.float64)
+
+    def check(got, heads):
+        for b in range(B):
+            ub = u[b].astype(np.float64)
+            ref = oracle.mla_apply_wuv(ub, w)
+            absdot = np.einsum("hc,hvc->hv", np.abs(ub), np.abs(w))
+            # u~ rounded to bf16, then a K-term float32 sum
+            bound = (2.0 ** -8 + d_c * 2.0 ** -23) * absdot * (1 + 2.0 ** -8)
+            assert not (np.abs(got[b] - ref) > bound)[heads].any(), b
+
+    check(v.cpu().numpy().astype(np.float64), slice(1, h))
+    err.zero_()
+    v.fill_(float("nan"))
+    kv.kvattn_mla_up_v(ud, wv, v, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    check(v.cpu().numpy().astype(np.float64), slice(0, h))
